@@ -1,0 +1,149 @@
+"""Layer-step maths for the oracle (test infrastructure only).
+
+Everything is float64.  bf16 inputs are widened exactly; int4 weights arrive
+dequantised (see ``oracle.int4``).  Sources, by page title and section:
+
+* "The Other Half of the Memory Wall" §3.1 "Math contract": an expert computes
+  down(silu(gate(x)) * up(x)).
+* §3.2 "Motivation"/"Head": the head of layer N reads layer N's post-attention norm
+  output; fc1 -> erf-GELU -> fc2 plus a linear residual path; input feature =
+  [hidden ; one-hot of the experts this layer routed to at this token ; one-hot of
+  those at the previous token] (dimension d + 2E).
+* §3.2 "Prediction-as-routing" and Appendix A: routing weights are the softmax of
+  the logits, restricted to the K selected experts and renormalised.
+* §3.3: the recovery LoRA is served unmerged, y = W_int4(x) + (alpha/r) * B(A(x)).
+
+Readings (the pages do not say):
+* x = RMSNorm(h) = h / sqrt(mean(h^2) + 1e-6) with unit gain is the "post-attention
+  norm output" that the head, the router, the experts and the LoRA linear consume;
+  the layer adds its output to the residual h (pre-norm block).
+* the one-hot blocks are binary K-hot vectors; an absent previous step is all zero.
+* the shared expert is added without a gate; the LoRA linear's output is added to
+  the residual stream as well.
+* h_out is the bf16 rounding (nearest even) of h + delta.
+"""
+import math
+
+import numpy as np
+
+from .bf16 import bf16_to_f64, f64_to_bf16
+from .routing import renorm_weights, softmax_topk
+
+RMS_EPS = 1e-6
+
+
+def rmsnorm(h: np.ndarray) -> np.ndarray:
+    h = np.asarray(h, dtype=np.float64)
+    return h / math.sqrt(float(np.mean(h * h)) + RMS_EPS)
+
+
+def silu(u: np.ndarray) -> np.ndarray:
+    u = np.asarray(u, dtype=np.float64)
+    return u / (1.0 + np.exp(-u))
+
+
+_erf = np.frompyfunc(math.erf, 1, 1)
+
+
+def gelu_erf(u: np.ndarray) -> np.ndarray:
+    """Exact (erf) GELU: 0.5 * u * (1 + erf(u / sqrt(2)))."""
+    u = np.asarray(u, dtype=np.float64)
+    return 0.5 * u * (1.0 + _erf(u / math.sqrt(2.0)).astype(np.float64))
+
+
+def router_logits(x: np.ndarray, R_bf16: np.ndarray) -> np.ndarray:
+    """A layer's own gate: z = R x with R bf16 [E][d]."""
+    return bf16_to_f64(R_bf16) @ np.asarray(x, dtype=np.float64)
+
+
+def onehot(ids, E: int) -> np.ndarray:
+    v = np.zeros(E, dtype=np.float64)
+    if ids is not None:
+        for e in np.asarray(ids).reshape(-1):
+            v[int(e)] = 1.0
+    return v
+
+
+def prerouter_logits(x: np.ndarray, ids_cur, ids_prev, head: dict) -> np.ndarray:
+    """Cross-token prerouter head: predicted next-layer logits for the next token.
+
+    head: W1 bf16 [H][d+2E], b1 bf16 [H] or None, W2 bf16 [E][H], b2 bf16 [E] or None,
+    Lres bf16 [E][d].  H == 0 (no W1/W2) leaves only the linear residual path.
+    """
+    Lres = bf16_to_f64(head["Lres"])
+    E, d = Lres.shape
+    zhat = Lres @ x
+    if head.get("W1") is not None:
+        feat = np.concatenate([x, onehot(ids_cur, E), onehot(ids_prev, E)])
+        W1 = bf16_to_f64(head["W1"])
+        assert W1.shape[1] == d + 2 * E
+        u = W1 @ feat
+        if head.get("b1") is not None:
+            u = u + bf16_to_f64(head["b1"])
+        p = gelu_erf(u)
+        zhat = zhat + bf16_to_f64(head["W2"]) @ p
+    if head.get("b2") is not None:
+        zhat = zhat + bf16_to_f64(head["b2"])
+    return zhat
+
+
+def expert(x: np.ndarray, Wg: np.ndarray, Wu: np.ndarray, Wd: np.ndarray) -> np.ndarray:
+    """down(silu(gate(x)) * up(x)) with dequantised fp64 weights."""
+    return Wd @ (silu(Wg @ x) * (Wu @ x))
+
+
+def lora_linear(x: np.ndarray, W: np.ndarray, A_bf16, B_bf16, alpha: float, r: int) -> np.ndarray:
+    """Unmerged recovery LoRA: W x + (alpha/r) B (A x); B None or r == 0 -> base only."""
+    y = W @ x
+    if B_bf16 is None or r == 0:
+        return y
+    A = bf16_to_f64(A_bf16)
+    B = bf16_to_f64(B_bf16)
+    return y + (alpha / r) * (B @ (A @ x))
+
+
+def layer_step(h_bf16, layer: dict, ids, logits, ids_prev=None, K: int | None = None):
+    """One MoE decode layer-step for one token.
+
+    layer: {"expert": callable e -> (Wg, Wu, Wd) fp64, "shared": (Wg, Wu, Wd) or None,
+            "lora": (W, A_bf16, B_bf16, alpha, r) or None, "head": dict or None}
+    ids/logits: this layer's committed routing; the combine weights are the
+    renormalised softmax of ``logits`` over ``ids``.
+    Returns dict(x, delta, h_out (bf16 bits), weights, next_logits, next_ids).
+    """
+    h = bf16_to_f64(h_bf16)
+    x = rmsnorm(h)
+    ids = np.asarray(ids, dtype=np.int64)
+    w = renorm_weights(logits, ids)
+    delta = np.zeros_like(x)
+    for k, e in enumerate(ids):
+        Wg, Wu, Wd = layer["expert"](int(e))
+        delta += w[k] * expert(x, Wg, Wu, Wd)
+    if layer.get("shared") is not None:
+        delta += expert(x, *layer["shared"])
+    if layer.get("lora") is not None:
+        delta += lora_linear(x, *layer["lora"])
+    out = {"x": x, "delta": delta, "h_out": f64_to_bf16(h + delta), "weights": w,
+           "next_logits": None, "next_ids": None}
+    if layer.get("head") is not None:
+        zhat = prerouter_logits(x, ids, ids_prev, layer["head"])
+        out["next_logits"] = zhat
+        out["next_ids"], _ = softmax_topk(zhat, K if K is not None else ids.size)
+    return out
+
+
+def prefill_chunk(H_bf16: np.ndarray, layer: dict, logits: np.ndarray, K: int):
+    """T tokens through one layer, routed by top-K of the given logits (no prerouter)."""
+    T = H_bf16.shape[0]
+    outs = []
+    for t in range(T):
+        ids, _ = softmax_topk(logits[t], K)
+        lay = dict(layer)
+        lay["head"] = None
+        outs.append(layer_step(H_bf16[t], lay, ids, logits[t]))
+    return outs
+
+
+def residual_increment(h_out_bf16, delta_bf16):
+    """Attention stand-in between layers: h_next = bf16(h_out + Delta)."""
+    return f64_to_bf16(bf16_to_f64(h_out_bf16) + bf16_to_f64(delta_bf16))
