@@ -1,0 +1,260 @@
+/*
+ * e0.h — C ABI of libe0: the MoE decode layer-step with a cross-token prerouter,
+ * int4 group-64 experts and an unmerged recovery LoRA, for NVIDIA GB300 (sm_103a).
+ *
+ * What the calls compute comes from "The Other Half of the Memory Wall: Serving 35B
+ * MoEs from SSD with Trained Routing Prediction" (Edge0):
+ *   §3.1 "Problem", "Executor paths", "Math contract" — int4 affine group-64 expert
+ *        weights with per-group scale and bias; an expert is down(silu(gate x) * up x);
+ *        staged experts addressed through a slot table that never leaves the GPU.
+ *   §3.2 "Head", "Prediction-as-routing" — the head of layer N reads layer N's norm
+ *        output plus the one-hots of this layer's routing at this token and at the
+ *        previous token; fc1 -> erf-GELU -> fc2 plus a linear residual gives the
+ *        logits that ARE the routing of layer N+1 at the next token.
+ *   §3.3 — the recovery LoRA is served unmerged: y = W_int4 x + (alpha/r) B A x.
+ *   Appendix A "Softmax-topk" — w = softmax(l)[ids] / sum over ids.
+ *
+ * Conventions (every call):
+ *   - All tensor pointers are DEVICE pointers unless a comment says "host".  The
+ *     caller owns all memory; the library never frees a caller pointer.  Device
+ *     pointers must be 16-byte aligned.
+ *   - bf16 tensors are passed as uint16_t bit patterns.  Matrices are row-major.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default).
+ *   - Argument and shape errors return a negative e0_status before anything is
+ *     launched; e0_last_error() then describes the problem (thread-local text).
+ *   - Errors found on the device (bad expert id, expert not resident in its slot
+ *     pool, a wait that ran out of time) never trap: they set bits in the status
+ *     word of the workspace, the kernel finishes early, and the caller reads the
+ *     word with e0_get_device_status() after synchronising.  After a non-zero
+ *     status the workspace must be cleared with e0_workspace_reset().
+ *   - A workspace is caller-allocated device memory of e0_*_workspace_size()
+ *     bytes, ZERO-FILLED before its first use (cudaMemset or e0_workspace_reset).
+ *     Calls that share a workspace must be ordered on one stream.  Holding it
+ *     between calls carries the engine's counters; nothing else persists.
+ *
+ * int4 format ("affine group-64"): a group is 64 consecutive input columns of one
+ * output row; scale s = bf16((max-min)/15), bias b = bf16(min), code
+ * q = clamp(rint((w-b)/s), 0, 15) in fp32 (q = 0 when s == 0); weight = s*q + b.
+ *   E0_LAYOUT_ROWS:    q uint32 [rows][cols/8] (column j at bits 4*(j%8) of word j/8),
+ *                      scale, bias bf16 [rows][cols/64].
+ *   E0_LAYOUT_COLSLAB: the same codes stored 32 columns at a time:
+ *                      q uint32 [cols/32][rows][4], scale, bias bf16 [cols/64][rows].
+ *   Both layouts are batched over a leading index (experts).
+ */
+#ifndef E0_H
+#define E0_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* e0_stream;   /* == cudaStream_t */
+typedef struct CUevent_st*  e0_event;    /* == cudaEvent_t  */
+typedef int32_t e0_status;
+
+enum {
+  E0_OK = 0,
+  E0_ERR_INVALID = -1,      /* bad pointer, alignment or argument */
+  E0_ERR_SHAPE = -2,        /* unsupported or inconsistent dimensions */
+  E0_ERR_CUDA = -3,         /* a CUDA runtime call failed (text in e0_last_error) */
+  E0_ERR_TIMEOUT = -4,      /* host-side wait ran out of time */
+  E0_ERR_NOMEM = -5,        /* workspace too small / allocation failed */
+  E0_ERR_UNSUPPORTED = -6,  /* valid request this build does not implement */
+  E0_ERR_DEVICE = -7        /* e0_get_device_status() reported device-side errors */
+};
+
+/* Bits of the device status word. */
+enum {
+  E0_DEV_TIMEOUT = 1,       /* a bounded spin-wait gave up */
+  E0_DEV_BAD_ID = 2,        /* an expert id outside [0, E) or repeated; expert skipped */
+  E0_DEV_NOT_RESIDENT = 4,  /* slot_of[id] < 0: expert absent from its slot pool; skipped */
+  E0_DEV_ABORTED = 8        /* another CTA aborted; this one stopped early */
+};
+
+enum { E0_LAYOUT_ROWS = 0, E0_LAYOUT_COLSLAB = 1 };
+
+/* Thread-local description of the last error returned on this thread. */
+const char* e0_last_error(void);
+const char* e0_version(void);
+
+/* --------------------------------------------------------------------------------
+ * e0_pack_int4 — quantise fp32 weights to int4 affine group-64 (§3.1, §2
+ * "Quantization").  w: fp32 [batch][rows][cols] (device).  cols % 64 == 0 and
+ * group == 64.  For E0_LAYOUT_COLSLAB cols % 32 == 0 (implied).  Outputs per the
+ * layout comments above.  Bit-exact: IEEE fp32 arithmetic, no fast-math.
+ * ------------------------------------------------------------------------------ */
+e0_status e0_pack_int4(const float* w, int64_t batch, int64_t rows, int64_t cols,
+                       int32_t group, int32_t layout,
+                       uint32_t* q, uint16_t* scale, uint16_t* bias, e0_stream stream);
+
+/* One packed int4 matrix (layout given by where it is used). */
+typedef struct {
+  const uint32_t* q;
+  const uint16_t* scale;
+  const uint16_t* bias;
+} e0_q4;
+
+/* A stack of SwiGLU experts (§3.1 "nine stacked tensors per layer").
+ *   gate_up: E0_LAYOUT_ROWS, [n][2F][d]; row 2j is gate row j, row 2j+1 is up row j.
+ *   down:    E0_LAYOUT_COLSLAB, [n][d][F] (i.e. q [n][F/32][d][4], s/b [n][F/64][d]).
+ *   n:       experts stored (E for a full stack, 1 for a shared expert, S slots).
+ *   slot_of: int16 [E] expert id -> stored index, < 0 = not resident; NULL = identity.
+ */
+typedef struct {
+  e0_q4 gate_up;
+  e0_q4 down;
+  int32_t n;
+  const int16_t* slot_of;
+} e0_experts;
+
+/* Unmerged recovery LoRA linear (§3.3): y = W x + (alpha/r) * B (A x).
+ *   w: E0_LAYOUT_ROWS [out][in];  a: bf16 [r][in];  bt: bf16 [r][out] (B transposed).
+ *   r == 0 or a/bt NULL -> base only. */
+typedef struct {
+  e0_q4 w;
+  const uint16_t* a;
+  const uint16_t* bt;
+  int32_t out;
+  int32_t r;
+  float alpha;
+} e0_qlora;
+
+/* Cross-token prerouter head (§3.2 "Head").  The feature is [x ; onehot(ids_cur) ;
+ * onehot(ids_prev)] with x the RMS-normed hidden state; fc1 is stored split:
+ *   w1h [H][d] (hidden block), w1c_t [E][H] and w1p_t [E][H] (the two one-hot
+ *   blocks, transposed so a committed id selects one contiguous row).
+ *   b1 [H] (nullable), w2t [H][E] (fc2 transposed), b2 [E] (nullable),
+ *   lres [E][d] (linear residual path).  H == 0 leaves only lres (+ b2): a plain
+ *   linear router. */
+typedef struct {
+  int32_t H;
+  const uint16_t* w1h;
+  const uint16_t* w1c_t;
+  const uint16_t* w1p_t;
+  const uint16_t* b1;
+  const uint16_t* w2t;
+  const uint16_t* b2;
+  const uint16_t* lres;
+} e0_prerouter;
+
+typedef struct {
+  int32_t d;    /* hidden width: 256, 512, 1024 or 2048 */
+  int32_t E;    /* routed experts, multiple of 8, <= 1024 */
+  int32_t F;    /* expert width, multiple of 64 */
+  int32_t K;    /* experts per token, 1..16 */
+} e0_dims;
+
+/* Workspace for every engine call below; layers = 1 for single-layer calls. */
+size_t e0_workspace_size(const e0_dims* dims, int32_t layers);
+/* Zero a workspace on `stream` (use after allocation and after a device error). */
+e0_status e0_workspace_reset(void* workspace, size_t bytes, e0_stream stream);
+/* Read the device status word (blocks until `stream` is idle). */
+e0_status e0_get_device_status(const void* workspace, uint32_t* status_out, e0_stream stream);
+
+/* --------------------------------------------------------------------------------
+ * e0_prerouter_forward — one head evaluation per token (§3.2 "Head"; Appendix A).
+ *   h: bf16 [T][d], the layer's hidden state; the head reads x = RMSNorm(h)
+ *      (unit gain, eps 1e-6) — the "post-attention norm output".
+ *   ids_cur, ids_prev: int32 [T][K] distinct ids in [0, E); ids_prev nullable
+ *      (previous one-hot all zero).
+ *   logit_bias: fp32 [E] added to the logits before top-K (nullable).
+ *   logits_out fp32 [T][E]; ids_out int32 [T][K] (descending, ties -> lower id);
+ *   weights_out fp32 [T][K] renormalised softmax over ids_out (nullable).
+ * ------------------------------------------------------------------------------ */
+e0_status e0_prerouter_forward(const e0_prerouter* head, int32_t d, int32_t E,
+                               const uint16_t* h, const int32_t* ids_cur,
+                               const int32_t* ids_prev, int32_t T, int32_t K,
+                               const float* logit_bias, float* logits_out,
+                               int32_t* ids_out, float* weights_out,
+                               void* workspace, size_t workspace_bytes, e0_stream stream);
+
+/* --------------------------------------------------------------------------------
+ * e0_qlinear_lora — y[T][out] = (accumulate ? y : 0) + W x + (alpha/r) B A x (§3.3).
+ *   x: bf16 [T][in] used as given (no norm); in in {256, 512, 1024, 2048}.
+ *   y: bf16 [T][out] (written, and read when accumulate != 0); y_f32 fp32 [T][out]
+ *   (nullable) receives the same sum before bf16 rounding.
+ * ------------------------------------------------------------------------------ */
+e0_status e0_qlinear_lora(const e0_qlora* lora, int32_t in, const uint16_t* x, int32_t T,
+                          int32_t accumulate, uint16_t* y, float* y_f32,
+                          void* workspace, size_t workspace_bytes, e0_stream stream);
+
+/* --------------------------------------------------------------------------------
+ * e0_moe_decode_layer — one MoE layer-step for T tokens (north star parts 1-4).
+ *   x = RMSNorm(h_in);  delta = sum_k w_k E_{ids_k}(x) + E_shared(x) + LoRA(x);
+ *   h_out = bf16(h_in + delta).  w = softmax(logits)[ids] renormalised (App. A).
+ *   routed: the layer's expert stack (slot_of for slot pools); shared, lora, head
+ *   nullable.  ids: int32 [T][K] this layer's committed routing, logits fp32 [T][E]
+ *   the logits it was committed from.  ids_prev int32 [T][K] nullable (the ids
+ *   this layer used at the previous token; only read by the head).
+ *   delta_f32 fp32 [T][d] nullable.  If head != NULL the call also commits the next
+ *   layer's routing for the next token: next_logits fp32 [T][E], next_ids int32
+ *   [T][K], next_weights fp32 [T][K] (nullable).
+ *   T == 1 runs the streaming GEMV engine; T > 1 runs the tokens one after another
+ *   through the same engine.
+ * ------------------------------------------------------------------------------ */
+e0_status e0_moe_decode_layer(const e0_dims* dims, const e0_experts* routed,
+                              const e0_experts* shared, const e0_qlora* lora,
+                              const e0_prerouter* head, const uint16_t* h_in,
+                              const int32_t* ids, const float* logits,
+                              const int32_t* ids_prev, int32_t T, uint16_t* h_out,
+                              float* delta_f32, float* next_logits, int32_t* next_ids,
+                              float* next_weights, void* workspace,
+                              size_t workspace_bytes, e0_stream stream);
+
+/* --------------------------------------------------------------------------------
+ * Decode stack: L layer-steps for one token in ONE launch (§3.2 "Two consumption
+ * profiles": routing for layer l at token t is the prediction made by head l-1 at
+ * token t-1, on layers whose previous layer owns a head; other layers, and every
+ * layer at the first token, route with their own gate R·x).
+ * The stack object is library-owned (layer descriptors and the CTA work plan in
+ * device memory); the weights it points to stay caller-owned and must outlive it.
+ * ------------------------------------------------------------------------------ */
+typedef struct {
+  e0_experts routed;
+  e0_experts shared;            /* n == 0 -> none */
+  e0_qlora lora;                /* w.q == NULL -> none */
+  e0_prerouter head;            /* lres == NULL -> no head on this layer */
+  const uint16_t* router;       /* bf16 [E][d]; required on layers that may self-route */
+} e0_layer;
+
+typedef struct e0_stack e0_stack;
+
+/* layers: HOST array of L descriptors (copied). prerouted_from: HOST int8 [L],
+ * 1 where layer l takes its routing from head l-1 after the first token. */
+e0_status e0_stack_create(e0_stack** out, const e0_dims* dims, const e0_layer* layers,
+                          int32_t L, const int8_t* prerouted_from);
+void e0_stack_destroy(e0_stack* stack);
+size_t e0_stack_workspace_size(const e0_stack* stack);
+
+/* One decode token through all L layers.
+ *   step: token index (0 = first token: every layer routes with its own gate).
+ *   h0: bf16 [d]; incr: bf16 [L][d] per-layer residual increments standing in for
+ *   attention (h_l = bf16(h_out_{l-1} + incr_l), h_out_{-1} = h0);
+ *   h_out: bf16 [d] output of the last layer.
+ *   ids_out int32 [L][K], weights_out fp32 [L][K], h_trace bf16 [L][d]: nullable
+ *   diagnostics (routing used per layer; each layer's input hidden state). */
+e0_status e0_stack_step(e0_stack* stack, int32_t step, const uint16_t* h0,
+                        const uint16_t* incr, uint16_t* h_out, int32_t* ids_out,
+                        float* weights_out, uint16_t* h_trace, void* workspace,
+                        size_t workspace_bytes, e0_stream stream);
+
+/* --------------------------------------------------------------------------------
+ * Input generation (not part of the method): the seeded counter-based generator
+ * "e0synth" (SplitMix64 draws, Irwin-Hall-12 normal) writing n values of tensor
+ * (seed, stream) starting at element `offset`; out is fp32 (bf16 != 0: bf16 bits).
+ * ------------------------------------------------------------------------------ */
+e0_status e0_synth_normal(void* out, int64_t n, uint64_t seed, uint32_t stream_id,
+                          int64_t offset, double sigma, int32_t bf16, e0_stream stream);
+
+/* Debug / tests: make the next engine launch on this workspace wait on a flag that
+ * nothing sets, with the given time limit (ns), so the timeout path can be tested.
+ * limit_ns == 0 restores normal operation. */
+e0_status e0_debug_inject_stall(void* workspace, uint64_t limit_ns, e0_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* E0_H */

@@ -1,0 +1,232 @@
+"""Thin Python binding over libe0 (argument marshalling only; every step runs in the
+library's CUDA kernels).  Names follow the C ABI in include/e0.h.
+
+Tensors are torch tensors on the current CUDA device; bf16 data is carried in
+``torch.int16``/``torch.bfloat16`` tensors and passed as raw bit patterns.  All calls
+are enqueued on ``torch.cuda.current_stream()`` unless a stream is given.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import _lib as L
+from ._lib import check, lib
+
+
+def _p(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+# ------------------------------------------------------------------ data holders
+@dataclass
+class Q4:
+    q: torch.Tensor       # int32 words
+    scale: torch.Tensor   # bf16 bits (int16)
+    bias: torch.Tensor
+
+    def c(self) -> L.e0_q4:
+        return L.e0_q4(_p(self.q), _p(self.scale), _p(self.bias))
+
+
+@dataclass
+class Experts:
+    gate_up: Q4           # row layout [n][2F][d], rows interleaved gate/up
+    down: Q4              # column-slab layout [n][d][F]
+    n: int
+    slot_of: Optional[torch.Tensor] = None   # int16 [E]
+
+    def c(self) -> L.e0_experts:
+        return L.e0_experts(self.gate_up.c(), self.down.c(), self.n, _p(self.slot_of))
+
+
+@dataclass
+class QLora:
+    w: Q4                 # row layout [out][in]
+    a: Optional[torch.Tensor]   # bf16 [r][in]
+    bt: Optional[torch.Tensor]  # bf16 [r][out]
+    out: int
+    r: int
+    alpha: float
+
+    def c(self) -> L.e0_qlora:
+        return L.e0_qlora(self.w.c(), _p(self.a), _p(self.bt), self.out, self.r, self.alpha)
+
+
+@dataclass
+class Prerouter:
+    H: int
+    w1h: Optional[torch.Tensor]
+    w1c_t: Optional[torch.Tensor]
+    w1p_t: Optional[torch.Tensor]
+    b1: Optional[torch.Tensor]
+    w2t: Optional[torch.Tensor]
+    b2: Optional[torch.Tensor]
+    lres: torch.Tensor
+
+    def c(self) -> L.e0_prerouter:
+        return L.e0_prerouter(self.H, _p(self.w1h), _p(self.w1c_t), _p(self.w1p_t), _p(self.b1), _p(self.w2t),
+                              _p(self.b2), _p(self.lres))
+
+
+def dims(d: int, E: int, F: int, K: int) -> L.e0_dims:
+    return L.e0_dims(d, E, F, K)
+
+
+# ------------------------------------------------------------------ calls
+def e0_pack_int4(w: torch.Tensor, layout: int = L.E0_LAYOUT_ROWS, out: Optional[Q4] = None, stream=None) -> Q4:
+    """fp32 [batch][rows][cols] (or [rows][cols]) -> packed int4 in the given layout.
+
+    ``out`` (optional) receives the result in caller-provided flat tensors."""
+    if w.dim() == 2:
+        w = w.unsqueeze(0)
+    assert w.dtype == torch.float32
+    b, rows, cols = w.shape
+    if out is None:
+        q = torch.empty(b * rows * cols // 8, dtype=torch.int32, device=w.device)
+        s = torch.empty(b * rows * cols // 64, dtype=torch.int16, device=w.device)
+        out = Q4(q, s, torch.empty_like(s))
+    assert out.q.numel() == b * rows * cols // 8 and out.scale.numel() == b * rows * cols // 64
+    check(lib().e0_pack_int4(_p(w.contiguous()), b, rows, cols, 64, layout, _p(out.q), _p(out.scale),
+                             _p(out.bias), _stream(stream)))
+    return out
+
+
+def e0_workspace(dm: L.e0_dims, layers: int = 1, device=None) -> torch.Tensor:
+    n = lib().e0_workspace_size(C.byref(dm), layers)
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def e0_workspace_reset(ws: torch.Tensor, stream=None) -> None:
+    check(lib().e0_workspace_reset(_p(ws), ws.numel(), _stream(stream)))
+
+
+def e0_get_device_status(ws: torch.Tensor, stream=None) -> int:
+    v = L.u32(0)
+    check(lib().e0_get_device_status(_p(ws), C.byref(v), _stream(stream)))
+    return int(v.value)
+
+
+def e0_debug_inject_stall(ws: torch.Tensor, limit_ns: int, stream=None) -> None:
+    check(lib().e0_debug_inject_stall(_p(ws), limit_ns, _stream(stream)))
+
+
+def e0_synth_normal(out: torch.Tensor, seed: int, stream_id: int, offset: int = 0, sigma: float = 1.0,
+                    stream=None) -> torch.Tensor:
+    bf = 1 if out.dtype in (torch.int16, torch.bfloat16) else 0
+    if not bf:
+        assert out.dtype == torch.float32
+    check(lib().e0_synth_normal(_p(out), out.numel(), seed, stream_id, offset, sigma, bf, _stream(stream)))
+    return out
+
+
+def e0_moe_decode_layer(dm: L.e0_dims, routed: Experts, shared: Optional[Experts], lora: Optional[QLora],
+                        head: Optional[Prerouter], h_in: torch.Tensor, ids: torch.Tensor, logits: torch.Tensor,
+                        ids_prev: Optional[torch.Tensor], ws: torch.Tensor, want_delta: bool = True, stream=None):
+    """Returns dict(h_out, delta, next_logits, next_ids, next_weights) for T = h_in.shape[0] tokens."""
+    T = h_in.shape[0] if h_in.dim() == 2 else 1
+    dev = h_in.device
+    h_out = torch.empty((T, dm.d), dtype=torch.int16, device=dev)
+    delta = torch.empty((T, dm.d), dtype=torch.float32, device=dev) if want_delta else None
+    nl = ni = nw = None
+    if head is not None:
+        nl = torch.empty((T, dm.E), dtype=torch.float32, device=dev)
+        ni = torch.empty((T, dm.K), dtype=torch.int32, device=dev)
+        nw = torch.empty((T, dm.K), dtype=torch.float32, device=dev)
+    r, s_, l_, h_ = routed.c(), (shared.c() if shared else None), (lora.c() if lora else None), \
+        (head.c() if head else None)
+    check(lib().e0_moe_decode_layer(C.byref(dm), C.byref(r), C.byref(s_) if s_ else None,
+                                    C.byref(l_) if l_ else None, C.byref(h_) if h_ else None, _p(h_in), _p(ids),
+                                    _p(logits), _p(ids_prev), T, _p(h_out), _p(delta), _p(nl), _p(ni), _p(nw),
+                                    _p(ws), ws.numel(), _stream(stream)))
+    return {"h_out": h_out, "delta": delta, "next_logits": nl, "next_ids": ni, "next_weights": nw}
+
+
+def e0_prerouter_forward(head: Prerouter, d: int, E: int, K: int, h: torch.Tensor, ids_cur, ids_prev,
+                         ws: torch.Tensor, logit_bias=None, stream=None):
+    T = h.shape[0] if h.dim() == 2 else 1
+    dev = h.device
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    ids = torch.empty((T, K), dtype=torch.int32, device=dev)
+    w = torch.empty((T, K), dtype=torch.float32, device=dev)
+    hc = head.c()
+    check(lib().e0_prerouter_forward(C.byref(hc), d, E, _p(h), _p(ids_cur), _p(ids_prev), T, K, _p(logit_bias),
+                                     _p(logits), _p(ids), _p(w), _p(ws), ws.numel(), _stream(stream)))
+    return logits, ids, w
+
+
+def e0_qlinear_lora(lora: QLora, x: torch.Tensor, ws: torch.Tensor, y: Optional[torch.Tensor] = None,
+                    accumulate: bool = False, want_f32: bool = True, stream=None):
+    T = x.shape[0] if x.dim() == 2 else 1
+    inn = x.shape[-1]
+    if y is None:
+        y = torch.zeros((T, lora.out), dtype=torch.int16, device=x.device)
+    yf = torch.empty((T, lora.out), dtype=torch.float32, device=x.device) if want_f32 else None
+    lc = lora.c()
+    check(lib().e0_qlinear_lora(C.byref(lc), inn, _p(x), T, 1 if accumulate else 0, _p(y), _p(yf), _p(ws),
+                                ws.numel(), _stream(stream)))
+    return y, yf
+
+
+class Stack:
+    """Owns an e0_stack (layer descriptors + work plan on the device)."""
+
+    def __init__(self, dm: L.e0_dims, layers: list, prerouted: list[int], keepalive=None):
+        self.dm = dm
+        self.L = len(layers)
+        arr = (L.e0_layer * self.L)()
+        for i, ly in enumerate(layers):
+            arr[i] = ly
+        pre = (C.c_int8 * self.L)(*prerouted)
+        h = C.c_void_p()
+        check(lib().e0_stack_create(C.byref(h), C.byref(dm), arr, self.L, C.cast(pre, C.c_void_p)))
+        self.handle = h
+        self.keepalive = keepalive
+
+    def workspace(self, device=None) -> torch.Tensor:
+        n = lib().e0_stack_workspace_size(self.handle)
+        return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+    def step(self, step: int, h0: torch.Tensor, incr: torch.Tensor, h_out: torch.Tensor, ws: torch.Tensor,
+             ids_out=None, w_out=None, h_trace=None, stream=None) -> None:
+        check(lib().e0_stack_step(self.handle, step, _p(h0), _p(incr), _p(h_out), _p(ids_out), _p(w_out),
+                                  _p(h_trace), _p(ws), ws.numel(), _stream(stream)))
+
+    def close(self):
+        if self.handle:
+            lib().e0_stack_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def e0_layer_struct(routed: Experts, shared: Optional[Experts], lora: Optional[QLora], head: Optional[Prerouter],
+                    router: torch.Tensor) -> L.e0_layer:
+    ly = L.e0_layer()
+    ly.routed = routed.c()
+    if shared is not None:
+        ly.shared = shared.c()
+    if lora is not None:
+        ly.lora = lora.c()
+    if head is not None:
+        ly.head = head.c()
+    ly.router = _p(router)
+    return ly

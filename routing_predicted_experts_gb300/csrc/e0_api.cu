@@ -1,0 +1,593 @@
+// Host side of libe0: argument checks, the per-CTA work planner and the C ABI
+// entry points that launch the streaming engine (e0_engine.cu).
+#include <algorithm>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "e0_engine.cuh"
+
+namespace e0 {
+static thread_local std::string g_err;
+void set_error(const std::string& msg) { g_err = msg; }
+e0_status fail(e0_status code, const std::string& msg) {
+  g_err = msg;
+  return code;
+}
+e0_status cuda_fail(cudaError_t err, const char* what) {
+  g_err = std::string(what) + ": " + cudaGetErrorString(err);
+  return E0_ERR_CUDA;
+}
+}  // namespace e0
+
+namespace e0eng {
+cudaError_t launch_engine(const EngineParams& P, cudaStream_t stream);
+int max_ctas_per_sm(int d);
+}  // namespace e0eng
+
+using namespace e0eng;
+
+extern "C" const char* e0_last_error(void) { return e0::g_err.c_str(); }
+extern "C" const char* e0_version(void) { return "libe0 0.1 (sm_103a)"; }
+
+namespace {
+
+constexpr uint64_t DEFAULT_TIMEOUT_NS = 2000000000ull;  // 2 s per bounded wait
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+e0_status device_ctas(int d, int* ncta) {
+  int dev = 0;
+  E0_CHECK_CUDA(cudaGetDevice(&dev));
+  int sms = 0;
+  E0_CHECK_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  int coop = 0;
+  E0_CHECK_CUDA(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev));
+  E0_REQUIRE(coop, E0_ERR_UNSUPPORTED, "device does not support cooperative launches");
+  const int per = max_ctas_per_sm(d);
+  E0_REQUIRE(per >= 1, E0_ERR_UNSUPPORTED, "engine kernel cannot be resident (shared memory)");
+  *ncta = std::min(sms, MAX_CTAS);
+  return E0_OK;
+}
+
+e0_status check_dims(const e0_dims* dm) {
+  E0_REQUIRE(dm, E0_ERR_INVALID, "dims is NULL");
+  E0_REQUIRE(dm->d == 256 || dm->d == 512 || dm->d == 1024 || dm->d == 2048, E0_ERR_SHAPE,
+             "d must be 256, 512, 1024 or 2048");
+  E0_REQUIRE(dm->E >= 8 && dm->E <= EMAX && dm->E % 8 == 0, E0_ERR_SHAPE, "E must be a multiple of 8 in [8, 1024]");
+  E0_REQUIRE(dm->F >= 64 && dm->F % 64 == 0 && dm->F <= 8192, E0_ERR_SHAPE, "F must be a multiple of 64");
+  E0_REQUIRE(dm->K >= 1 && dm->K <= KMAX && dm->K <= dm->E, E0_ERR_SHAPE, "K must be in [1, min(16, E)]");
+  return E0_OK;
+}
+
+// ------------------------------------------------------------------ planner
+struct PlanSpec {
+  int d = 0, E = 0, F = 0, K = 0;
+  bool routed = false, shared = false, lora = false, lora_ab = false, head = false, lres = false, router = false;
+  int lout = 0, lr = 0, H = 0;
+  bool operator<(const PlanSpec& o) const {
+    return std::memcmp(this, &o, sizeof(PlanSpec)) < 0;
+  }
+};
+
+struct Granule {
+  uint8_t type;
+  int row;
+  int rows;
+  double cost;
+};
+
+// Relative cost of a streamed byte: int4 rows need about twice the ALU work per
+// byte of bf16 rows.
+constexpr double W_INT4 = 1.25;
+constexpr double W_BF16 = 1.0;
+
+e0_status build_plan(const PlanSpec& s, int ncta, Unit* units, uint8_t* counts) {
+  std::vector<std::vector<Unit>> lists(ncta);
+  std::vector<double> load(ncta, 0.0);
+  const int d = s.d;
+  // 1. expert slabs, round robin
+  if (s.routed || s.shared) {
+    const double c_exp = W_INT4 * (64.0 * q4_row_bytes(d) + 20.0 * d);
+    int idx = 0;
+    const int kmax = s.routed ? s.K : 0;
+    for (int k = 0; k <= kmax; ++k) {
+      if (k < kmax || s.shared) {
+        if (k == kmax && !s.shared) break;
+        for (int sl = 0; sl < s.F / 32; ++sl) {
+          const int c = idx++ % ncta;
+          lists[c].push_back(Unit{U_EXPERT, (uint8_t)(k < kmax ? k : s.K), (uint16_t)sl, (uint16_t)(sl + 1), 0});
+          load[c] += c_exp;
+        }
+      }
+    }
+  }
+  // 2. divisible work as granules
+  std::vector<Granule> gs;
+  if (s.lora)
+    for (int r = 0; r < s.lout; r += 16) gs.push_back({U_QROWS, r, 16, W_INT4 * 16.0 * q4_row_bytes(d)});
+  if (s.lora_ab)
+    for (int q = 0; q < s.lr; ++q) gs.push_back({U_LORA_AB, q, 1, W_BF16 * (2.0 * d + 2.0 * s.lout)});
+  if (s.lres)
+    for (int e = 0; e < s.E; e += 8) gs.push_back({U_LRES, e, 8, W_BF16 * 8.0 * 2.0 * d});
+  if (s.head)
+    for (int i = 0; i < s.H; i += 8)
+      gs.push_back({U_HEAD, i, 8, W_BF16 * 8.0 * (2.0 * d + 2.0 * s.E + 2.0 * (1 + 2 * s.K))});
+  if (s.router)
+    for (int e = 0; e < s.E; e += 8) gs.push_back({U_ROUTER, e, 8, W_BF16 * 8.0 * 2.0 * d});
+  double total = 0.0;
+  for (double v : load) total += v;
+  for (auto& g : gs) total += g.cost;
+  const double target = total / ncta;
+  // 3. water-fill granules over CTAs with cumulative capacity (rounding spreads evenly)
+  double cum_cap = 0.0, cum_assigned = 0.0;
+  size_t g = 0;
+  for (int c = 0; c < ncta && g < gs.size(); ++c) {
+    cum_cap += std::max(0.0, target - load[c]);
+    const bool last = (c == ncta - 1);
+    while (g < gs.size() && (last || cum_assigned + 0.5 * gs[g].cost <= cum_cap)) {
+      const Granule& gr = gs[g];
+      auto& L = lists[c];
+      // merge with the previous unit when contiguous and of the same type
+      bool merged = false;
+      for (auto& u : L) {
+        if (u.type == gr.type && u.r1 == gr.row) {
+          const int limit = gr.type == U_HEAD ? HEAD_ROWS : (gr.type == U_LORA_AB ? RANKS_MAX : 65535);
+          if ((int)u.r1 - (int)u.r0 + gr.rows <= limit) {
+            u.r1 = (uint16_t)(gr.row + gr.rows);
+            merged = true;
+          }
+          break;
+        }
+      }
+      if (!merged) lists[c].push_back(Unit{gr.type, 0, (uint16_t)gr.row, (uint16_t)(gr.row + gr.rows), 0});
+      load[c] += gr.cost;
+      cum_assigned += gr.cost;
+      ++g;
+    }
+  }
+  // 4. order: id-independent work first, experts last
+  auto rank = [](uint8_t t) {
+    switch (t) {
+      case U_ROUTER: return 0;
+      case U_QROWS: return 1;
+      case U_LORA_AB: return 2;
+      case U_LRES: return 3;
+      case U_HEAD: return 4;
+      default: return 5;
+    }
+  };
+  for (int c = 0; c < ncta; ++c) {
+    auto& L = lists[c];
+    std::stable_sort(L.begin(), L.end(), [&](const Unit& a, const Unit& b) { return rank(a.type) < rank(b.type); });
+    E0_REQUIRE((int)L.size() <= MAXU, E0_ERR_UNSUPPORTED, "work plan needs more units per CTA than supported");
+    counts[c] = (uint8_t)L.size();
+    for (size_t i = 0; i < L.size(); ++i) units[(size_t)c * MAXU + i] = L[i];
+    for (size_t i = L.size(); i < (size_t)MAXU; ++i) units[(size_t)c * MAXU + i] = Unit{U_NONE, 0, 0, 0, 0};
+  }
+  return E0_OK;
+}
+
+struct CachedPlan {
+  std::vector<Unit> units;
+  std::vector<uint8_t> counts;
+};
+std::mutex g_plan_mu;
+std::map<std::pair<PlanSpec, int>, CachedPlan> g_plans;
+
+e0_status get_plan(const PlanSpec& s, int ncta, const CachedPlan** out) {
+  std::lock_guard<std::mutex> lk(g_plan_mu);
+  auto key = std::make_pair(s, ncta);
+  auto it = g_plans.find(key);
+  if (it == g_plans.end()) {
+    CachedPlan cp;
+    cp.units.assign((size_t)ncta * MAXU, Unit{});
+    cp.counts.assign(ncta, 0);
+    e0_status st = build_plan(s, ncta, cp.units.data(), cp.counts.data());
+    if (st != E0_OK) return st;
+    it = g_plans.emplace(key, std::move(cp)).first;
+  }
+  *out = &it->second;
+  return E0_OK;
+}
+
+// ------------------------------------------------------------------ descriptors
+e0_status fill_experts(const e0_experts* ex, const e0_dims* dm, bool routed, LayerDesc* L) {
+  E0_REQUIRE(ex->gate_up.q && ex->gate_up.scale && ex->gate_up.bias && ex->down.q && ex->down.scale && ex->down.bias,
+             E0_ERR_INVALID, "expert stack has a NULL tensor");
+  E0_REQUIRE(al16(ex->gate_up.q) && al16(ex->gate_up.scale) && al16(ex->gate_up.bias) && al16(ex->down.q) &&
+                 al16(ex->down.scale) && al16(ex->down.bias),
+             E0_ERR_INVALID, "expert tensors must be 16-byte aligned");
+  E0_REQUIRE(ex->n >= 1, E0_ERR_INVALID, "expert stack needs n >= 1");
+  if (routed) {
+    L->gu_q = ex->gate_up.q; L->gu_s = ex->gate_up.scale; L->gu_b = ex->gate_up.bias;
+    L->dn_q = ex->down.q; L->dn_s = ex->down.scale; L->dn_b = ex->down.bias;
+    L->slot_of = ex->slot_of;
+    L->n_routed = ex->n;
+    E0_REQUIRE(ex->slot_of || ex->n >= dm->E, E0_ERR_INVALID, "routed stack without slot_of must hold all E experts");
+  } else {
+    L->sgu_q = ex->gate_up.q; L->sgu_s = ex->gate_up.scale; L->sgu_b = ex->gate_up.bias;
+    L->sdn_q = ex->down.q; L->sdn_s = ex->down.scale; L->sdn_b = ex->down.bias;
+    L->has_shared = 1;
+  }
+  return E0_OK;
+}
+
+e0_status fill_lora(const e0_qlora* lo, int in, LayerDesc* L, bool* has_ab) {
+  E0_REQUIRE(lo->w.q && lo->w.scale && lo->w.bias, E0_ERR_INVALID, "LoRA base W has a NULL tensor");
+  E0_REQUIRE(al16(lo->w.q) && al16(lo->w.scale) && al16(lo->w.bias), E0_ERR_INVALID, "LoRA W must be 16-byte aligned");
+  E0_REQUIRE(lo->out >= 16 && lo->out % 16 == 0 && lo->out <= OUTMAX, E0_ERR_SHAPE,
+             "LoRA out must be a multiple of 16 in [16, 4096]");
+  E0_REQUIRE(lo->r >= 0 && lo->r <= RANKS_MAX, E0_ERR_SHAPE, "LoRA rank must be in [0, 64]");
+  L->lw_q = lo->w.q; L->lw_s = lo->w.scale; L->lw_b = lo->w.bias;
+  L->lout = lo->out;
+  L->has_lora = 1;
+  *has_ab = lo->r > 0 && lo->a && lo->bt;
+  if (*has_ab) {
+    E0_REQUIRE(al16(lo->a) && al16(lo->bt), E0_ERR_INVALID, "LoRA A/Bt must be 16-byte aligned");
+    L->la = lo->a; L->lbt = lo->bt; L->lr = lo->r;
+    L->lscale = lo->alpha / (float)lo->r;
+  }
+  (void)in;
+  return E0_OK;
+}
+
+e0_status fill_head(const e0_prerouter* hd, const e0_dims* dm, LayerDesc* L) {
+  E0_REQUIRE(hd->lres && al16(hd->lres), E0_ERR_INVALID, "prerouter lres must be non-NULL and 16-byte aligned");
+  E0_REQUIRE(hd->H >= 0 && hd->H % 8 == 0 && hd->H <= 8192, E0_ERR_SHAPE, "prerouter H must be a multiple of 8");
+  L->has_head = 1;
+  L->H = hd->H;
+  L->lres = hd->lres;
+  L->b2 = hd->b2;
+  if (hd->H > 0) {
+    E0_REQUIRE(hd->w1h && hd->w1c_t && hd->w1p_t && hd->w2t, E0_ERR_INVALID, "prerouter fc1/fc2 tensor is NULL");
+    E0_REQUIRE(al16(hd->w1h) && al16(hd->w1c_t) && al16(hd->w1p_t) && al16(hd->w2t) && (!hd->b1 || al16(hd->b1)),
+               E0_ERR_INVALID, "prerouter tensors must be 16-byte aligned");
+    L->w1h = hd->w1h; L->w1c_t = hd->w1c_t; L->w1p_t = hd->w1p_t; L->b1 = hd->b1; L->w2t = hd->w2t;
+  }
+  (void)dm;
+  return E0_OK;
+}
+
+void base_params(EngineParams& P, int d, int E, int F, int K, int L, int ncta, int mode) {
+  std::memset(&P, 0, sizeof(P));
+  P.d = d; P.E = E; P.F = F; P.K = K; P.L = L; P.ncta = ncta; P.mode = mode;
+  P.norm = 1; P.out_dim = d; P.kinds = 1;
+  P.timeout_ns = DEFAULT_TIMEOUT_NS;
+  P.wl = ws_layout(E, L);
+}
+
+void set_inline_plan(EngineParams& P, const CachedPlan& cp) {
+  std::memcpy(P.inline_plan, cp.units.data(), sizeof(Unit) * cp.units.size());
+  std::memcpy(P.inline_n, cp.counts.data(), cp.counts.size());
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+extern "C" size_t e0_workspace_size(const e0_dims* dims, int32_t layers) {
+  if (!dims || layers < 1) return 0;
+  return ws_layout(std::max(dims->E, 8), layers).total;
+}
+
+extern "C" e0_status e0_workspace_reset(void* ws, size_t bytes, e0_stream stream) {
+  E0_REQUIRE(ws && bytes >= sizeof(WsHeader), E0_ERR_INVALID, "e0_workspace_reset: bad workspace");
+  E0_CHECK_CUDA(cudaMemsetAsync(ws, 0, bytes, (cudaStream_t)stream));
+  return E0_OK;
+}
+
+extern "C" e0_status e0_get_device_status(const void* ws, uint32_t* status_out, e0_stream stream) {
+  E0_REQUIRE(ws && status_out, E0_ERR_INVALID, "e0_get_device_status: NULL argument");
+  E0_CHECK_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+  WsHeader h;
+  E0_CHECK_CUDA(cudaMemcpy(&h, ws, sizeof(h), cudaMemcpyDeviceToHost));
+  *status_out = h.status;
+  return E0_OK;
+}
+
+extern "C" e0_status e0_debug_inject_stall(void* ws, uint64_t limit_ns, e0_stream stream) {
+  E0_REQUIRE(ws, E0_ERR_INVALID, "e0_debug_inject_stall: NULL workspace");
+  E0_CHECK_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+  E0_CHECK_CUDA(cudaMemcpy(reinterpret_cast<uint8_t*>(ws) + offsetof(WsHeader, stall_ns), &limit_ns,
+                           sizeof(limit_ns), cudaMemcpyHostToDevice));
+  return E0_OK;
+}
+
+static e0_status check_ws(const e0_dims* dm, int L, void* ws, size_t bytes) {
+  E0_REQUIRE(ws && al16(ws), E0_ERR_INVALID, "workspace must be non-NULL and 16-byte aligned");
+  E0_REQUIRE(bytes >= ws_layout(dm->E, L).total, E0_ERR_NOMEM, "workspace smaller than e0_workspace_size()");
+  return E0_OK;
+}
+
+extern "C" e0_status e0_moe_decode_layer(const e0_dims* dims, const e0_experts* routed, const e0_experts* shared,
+                                         const e0_qlora* lora, const e0_prerouter* head, const uint16_t* h_in,
+                                         const int32_t* ids, const float* logits, const int32_t* ids_prev,
+                                         int32_t T, uint16_t* h_out, float* delta_f32, float* next_logits,
+                                         int32_t* next_ids, float* next_weights, void* workspace,
+                                         size_t workspace_bytes, e0_stream stream) {
+  e0_status st = check_dims(dims);
+  if (st) return st;
+  E0_REQUIRE(routed && h_in && ids && logits && h_out, E0_ERR_INVALID, "e0_moe_decode_layer: NULL required argument");
+  E0_REQUIRE(T >= 0, E0_ERR_INVALID, "T must be >= 0");
+  if (T == 0) return E0_OK;
+  st = check_ws(dims, 1, workspace, workspace_bytes);
+  if (st) return st;
+  E0_REQUIRE(al16(h_in) && al16(h_out) && (!delta_f32 || al16(delta_f32)), E0_ERR_INVALID,
+             "activation buffers must be 16-byte aligned");
+  int ncta;
+  st = device_ctas(dims->d, &ncta);
+  if (st) return st;
+
+  static thread_local EngineParams P;
+  base_params(P, dims->d, dims->E, dims->F, dims->K, 1, ncta, MODE_LAYER);
+  LayerDesc& L = P.inline_layer;
+  PlanSpec ps;
+  ps.d = dims->d; ps.E = dims->E; ps.F = dims->F; ps.K = dims->K;
+  st = fill_experts(routed, dims, true, &L);
+  if (st) return st;
+  ps.routed = true;
+  if (shared && shared->n > 0) {
+    st = fill_experts(shared, dims, false, &L);
+    if (st) return st;
+    ps.shared = true;
+  }
+  if (lora && lora->w.q) {
+    bool ab = false;
+    st = fill_lora(lora, dims->d, &L, &ab);
+    if (st) return st;
+    E0_REQUIRE(lora->out == dims->d, E0_ERR_SHAPE, "in a layer-step the LoRA linear must be d x d");
+    ps.lora = true; ps.lora_ab = ab; ps.lout = lora->out; ps.lr = ab ? lora->r : 0;
+  }
+  if (head && head->lres) {
+    st = fill_head(head, dims, &L);
+    if (st) return st;
+    ps.head = head->H > 0; ps.lres = true; ps.H = head->H;
+    E0_REQUIRE(next_logits || next_ids, E0_ERR_INVALID, "a head needs next_logits or next_ids");
+  }
+  const CachedPlan* cp;
+  st = get_plan(ps, ncta, &cp);
+  if (st) return st;
+  set_inline_plan(P, *cp);
+  P.kinds = 1;
+  const int d = dims->d, E = dims->E, K = dims->K;
+  for (int t = 0; t < T; ++t) {
+    P.h_in = h_in + (size_t)t * d;
+    P.ids_in = ids + (size_t)t * K;
+    P.logits_in = logits + (size_t)t * E;
+    P.ids_prev_in = ids_prev ? ids_prev + (size_t)t * K : nullptr;
+    P.h_out = h_out + (size_t)t * d;
+    P.delta_out = delta_f32 ? delta_f32 + (size_t)t * d : nullptr;
+    P.next_logits = next_logits ? next_logits + (size_t)t * E : nullptr;
+    P.next_ids = next_ids ? next_ids + (size_t)t * K : nullptr;
+    P.next_w = next_weights ? next_weights + (size_t)t * K : nullptr;
+    P.ws = reinterpret_cast<uint8_t*>(workspace);
+    E0_CHECK_CUDA(launch_engine(P, (cudaStream_t)stream));
+  }
+  return E0_OK;
+}
+
+extern "C" e0_status e0_prerouter_forward(const e0_prerouter* head, int32_t d, int32_t E, const uint16_t* h,
+                                          const int32_t* ids_cur, const int32_t* ids_prev, int32_t T, int32_t K,
+                                          const float* logit_bias, float* logits_out, int32_t* ids_out,
+                                          float* weights_out, void* workspace, size_t workspace_bytes,
+                                          e0_stream stream) {
+  e0_dims dm{d, E, 64, K};
+  e0_status st = check_dims(&dm);
+  if (st) return st;
+  E0_REQUIRE(head && h && (logits_out || ids_out), E0_ERR_INVALID, "e0_prerouter_forward: NULL required argument");
+  E0_REQUIRE(T >= 0, E0_ERR_INVALID, "T must be >= 0");
+  if (T == 0) return E0_OK;
+  st = check_ws(&dm, 1, workspace, workspace_bytes);
+  if (st) return st;
+  int ncta;
+  st = device_ctas(d, &ncta);
+  if (st) return st;
+  static thread_local EngineParams P;
+  base_params(P, d, E, 64, K, 1, ncta, MODE_HEAD);
+  st = fill_head(head, &dm, &P.inline_layer);
+  if (st) return st;
+  E0_REQUIRE(head->H == 0 || ids_cur, E0_ERR_INVALID, "a head with an MLP needs ids_cur");
+  PlanSpec ps;
+  ps.d = d; ps.E = E; ps.F = 64; ps.K = K;
+  ps.head = head->H > 0; ps.lres = true; ps.H = head->H;
+  const CachedPlan* cp;
+  st = get_plan(ps, ncta, &cp);
+  if (st) return st;
+  set_inline_plan(P, *cp);
+  P.logit_bias = logit_bias;
+  for (int t = 0; t < T; ++t) {
+    P.h_in = h + (size_t)t * d;
+    P.ids_in = ids_cur ? ids_cur + (size_t)t * K : nullptr;
+    P.ids_prev_in = ids_prev ? ids_prev + (size_t)t * K : nullptr;
+    P.next_logits = logits_out ? logits_out + (size_t)t * E : nullptr;
+    P.next_ids = ids_out ? ids_out + (size_t)t * K : nullptr;
+    P.next_w = weights_out ? weights_out + (size_t)t * K : nullptr;
+    P.ws = reinterpret_cast<uint8_t*>(workspace);
+    E0_CHECK_CUDA(launch_engine(P, (cudaStream_t)stream));
+  }
+  return E0_OK;
+}
+
+extern "C" e0_status e0_qlinear_lora(const e0_qlora* lora, int32_t in, const uint16_t* x, int32_t T,
+                                     int32_t accumulate, uint16_t* y, float* y_f32, void* workspace,
+                                     size_t workspace_bytes, e0_stream stream) {
+  E0_REQUIRE(lora && x && y, E0_ERR_INVALID, "e0_qlinear_lora: NULL required argument");
+  E0_REQUIRE(in == 256 || in == 512 || in == 1024 || in == 2048, E0_ERR_SHAPE, "in must be 256, 512, 1024 or 2048");
+  E0_REQUIRE(T >= 0, E0_ERR_INVALID, "T must be >= 0");
+  if (T == 0) return E0_OK;
+  e0_dims dm{in, 8, 64, 1};
+  e0_status st = check_ws(&dm, 1, workspace, workspace_bytes);
+  if (st) return st;
+  E0_REQUIRE(al16(x) && al16(y) && (!y_f32 || al16(y_f32)), E0_ERR_INVALID, "x, y must be 16-byte aligned");
+  int ncta;
+  st = device_ctas(in, &ncta);
+  if (st) return st;
+  static thread_local EngineParams P;
+  base_params(P, in, 8, 64, 1, 1, ncta, MODE_QLINEAR);
+  bool ab = false;
+  st = fill_lora(lora, in, &P.inline_layer, &ab);
+  if (st) return st;
+  P.norm = 0;
+  P.out_dim = lora->out;
+  P.accumulate = accumulate;
+  PlanSpec ps;
+  ps.d = in; ps.E = 8; ps.F = 64; ps.K = 1;
+  ps.lora = true; ps.lora_ab = ab; ps.lout = lora->out; ps.lr = ab ? lora->r : 0;
+  const CachedPlan* cp;
+  st = get_plan(ps, ncta, &cp);
+  if (st) return st;
+  set_inline_plan(P, *cp);
+  for (int t = 0; t < T; ++t) {
+    P.h_in = x + (size_t)t * in;
+    P.h_out = y + (size_t)t * lora->out;
+    P.delta_out = y_f32 ? y_f32 + (size_t)t * lora->out : nullptr;
+    P.ws = reinterpret_cast<uint8_t*>(workspace);
+    E0_CHECK_CUDA(launch_engine(P, (cudaStream_t)stream));
+  }
+  return E0_OK;
+}
+
+// ------------------------------------------------------------------ stack
+struct e0_stack {
+  e0_dims dims;
+  int L;
+  int ncta;
+  std::vector<int8_t> prerouted;
+  LayerDesc* d_layers = nullptr;
+  Unit* d_plan = nullptr;
+  uint8_t* d_counts = nullptr;
+};
+
+extern "C" e0_status e0_stack_create(e0_stack** out, const e0_dims* dims, const e0_layer* layers, int32_t L,
+                                     const int8_t* prerouted_from) {
+  E0_REQUIRE(out && layers && L >= 1 && L <= 64, E0_ERR_INVALID, "e0_stack_create: need 1..64 layers");
+  *out = nullptr;
+  e0_status st = check_dims(dims);
+  if (st) return st;
+  int ncta;
+  st = device_ctas(dims->d, &ncta);
+  if (st) return st;
+  std::vector<LayerDesc> descs(L);
+  PlanSpec spec[2];
+  bool have_spec[2] = {false, false};
+  for (int l = 0; l < L; ++l) {
+    LayerDesc& D = descs[l];
+    std::memset(&D, 0, sizeof(D));
+    const e0_layer& ly = layers[l];
+    PlanSpec ps;
+    ps.d = dims->d; ps.E = dims->E; ps.F = dims->F; ps.K = dims->K;
+    st = fill_experts(&ly.routed, dims, true, &D);
+    if (st) return st;
+    ps.routed = true;
+    if (ly.shared.n > 0) {
+      st = fill_experts(&ly.shared, dims, false, &D);
+      if (st) return st;
+      ps.shared = true;
+    }
+    if (ly.lora.w.q) {
+      bool ab = false;
+      st = fill_lora(&ly.lora, dims->d, &D, &ab);
+      if (st) return st;
+      E0_REQUIRE(ly.lora.out == dims->d, E0_ERR_SHAPE, "stack LoRA linears must be d x d");
+      ps.lora = true; ps.lora_ab = ab; ps.lout = ly.lora.out; ps.lr = ab ? ly.lora.r : 0;
+    }
+    if (ly.head.lres) {
+      st = fill_head(&ly.head, dims, &D);
+      if (st) return st;
+      ps.head = ly.head.H > 0; ps.lres = true; ps.H = ly.head.H;
+    }
+    E0_REQUIRE(ly.router && al16(ly.router), E0_ERR_INVALID,
+               "every stack layer needs its own gate (used at the first token)");
+    D.router = ly.router;
+    D.prerouted = prerouted_from ? prerouted_from[l] : 0;
+    if (D.prerouted) {
+      E0_REQUIRE(l > 0 && layers[l - 1].head.lres, E0_ERR_INVALID,
+                 "a prerouted layer needs a head on the previous layer");
+    }
+    const int kind = D.has_head ? KIND_MAIN : KIND_MAIN_NOHEAD;
+    if (have_spec[kind]) {
+      E0_REQUIRE(std::memcmp(&spec[kind], &ps, sizeof(ps)) == 0, E0_ERR_UNSUPPORTED,
+                 "stack layers of one kind must share one shape");
+    } else {
+      spec[kind] = ps;
+      have_spec[kind] = true;
+    }
+    D.plan_kind = kind;
+  }
+  PlanSpec rs;
+  rs.d = dims->d; rs.E = dims->E; rs.F = dims->F; rs.K = dims->K; rs.router = true;
+  std::vector<Unit> units((size_t)KINDS_MAX * ncta * MAXU);
+  std::vector<uint8_t> counts((size_t)KINDS_MAX * ncta, 0);
+  for (int k = 0; k < 2; ++k)
+    if (have_spec[k]) {
+      st = build_plan(spec[k], ncta, units.data() + (size_t)k * ncta * MAXU, counts.data() + (size_t)k * ncta);
+      if (st) return st;
+    }
+  st = build_plan(rs, ncta, units.data() + (size_t)KIND_ROUTER * ncta * MAXU,
+                  counts.data() + (size_t)KIND_ROUTER * ncta);
+  if (st) return st;
+
+  e0_stack* s = new e0_stack();
+  s->dims = *dims;
+  s->L = L;
+  s->ncta = ncta;
+  s->prerouted.assign(L, 0);
+  for (int l = 0; l < L; ++l) s->prerouted[l] = descs[l].prerouted ? 1 : 0;
+  cudaError_t e = cudaMalloc(&s->d_layers, sizeof(LayerDesc) * L);
+  if (e == cudaSuccess) e = cudaMalloc(&s->d_plan, sizeof(Unit) * units.size());
+  if (e == cudaSuccess) e = cudaMalloc(&s->d_counts, counts.size());
+  if (e == cudaSuccess) e = cudaMemcpy(s->d_layers, descs.data(), sizeof(LayerDesc) * L, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(s->d_plan, units.data(), sizeof(Unit) * units.size(), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(s->d_counts, counts.data(), counts.size(), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    e0_stack_destroy(s);
+    return e0::cuda_fail(e, "e0_stack_create");
+  }
+  *out = s;
+  return E0_OK;
+}
+
+extern "C" void e0_stack_destroy(e0_stack* s) {
+  if (!s) return;
+  if (s->d_layers) cudaFree(s->d_layers);
+  if (s->d_plan) cudaFree(s->d_plan);
+  if (s->d_counts) cudaFree(s->d_counts);
+  delete s;
+}
+
+extern "C" size_t e0_stack_workspace_size(const e0_stack* s) {
+  if (!s) return 0;
+  return ws_layout(s->dims.E, s->L).total;
+}
+
+extern "C" e0_status e0_stack_step(e0_stack* s, int32_t step, const uint16_t* h0, const uint16_t* incr,
+                                   uint16_t* h_out, int32_t* ids_out, float* weights_out, uint16_t* h_trace,
+                                   void* workspace, size_t workspace_bytes, e0_stream stream) {
+  E0_REQUIRE(s && h0 && h_out, E0_ERR_INVALID, "e0_stack_step: NULL required argument");
+  E0_REQUIRE(step >= 0, E0_ERR_INVALID, "step must be >= 0");
+  e0_status st = check_ws(&s->dims, s->L, workspace, workspace_bytes);
+  if (st) return st;
+  E0_REQUIRE(al16(h0) && al16(h_out) && (!incr || al16(incr)), E0_ERR_INVALID, "hidden buffers must be 16-byte aligned");
+  static thread_local EngineParams P;
+  base_params(P, s->dims.d, s->dims.E, s->dims.F, s->dims.K, s->L, s->ncta, MODE_STACK);
+  P.layers = s->d_layers;
+  P.plan = s->d_plan;
+  P.plan_n = s->d_counts;
+  P.kinds = KINDS_MAX;
+  P.step = step;
+  uint64_t mask = 0;
+  for (int l = 0; l < s->L; ++l)
+    if (step == 0 || !s->prerouted[l]) mask |= 1ull << l;
+  P.router_mask = mask;
+  P.h_in = h0;
+  P.incr = incr;
+  P.h_out = h_out;
+  P.ids_trace = ids_out;
+  P.w_trace = weights_out;
+  P.h_trace = h_trace;
+  P.ws = reinterpret_cast<uint8_t*>(workspace);
+  E0_CHECK_CUDA(launch_engine(P, (cudaStream_t)stream));
+  return E0_OK;
+}

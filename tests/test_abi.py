@@ -1,0 +1,42 @@
+"""The C ABI library builds, loads and exports every function include/e0.h declares (CPU only)."""
+import os
+import re
+
+from routing_predicted_experts_gb300 import _lib
+from routing_predicted_experts_gb300 import build as B
+
+HDR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "e0.h")
+
+
+def declared_functions():
+    text = open(HDR).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(e0_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ["e0_pack_int4", "e0_prerouter_forward", "e0_moe_decode_layer", "e0_qlinear_lora",
+                     "e0_stack_create", "e0_stack_step", "e0_last_error", "e0_get_device_status"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    B.build()
+    lib = _lib.lib()
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(_lib.PROTOTYPES) <= set(declared_functions())
+
+
+def test_host_side_argument_errors_without_gpu():
+    lib = _lib.lib()
+    # NULL arguments are rejected before any CUDA call
+    st = lib.e0_pack_int4(None, 1, 1, 64, 64, 0, None, None, None, None)
+    assert st == -1 and b"null" in lib.e0_last_error().lower()
+    dm = _lib.e0_dims(300, 256, 512, 4)
+    assert lib.e0_workspace_size(None, 1) == 0
+    st = lib.e0_moe_decode_layer(dm, None, None, None, None, None, None, None, None, 1, None, None, None, None,
+                                 None, None, 0, None)
+    assert st == -2  # d = 300 unsupported
