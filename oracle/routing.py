@@ -24,9 +24,15 @@ def topk_desc(scores: np.ndarray, K: int) -> np.ndarray:
 
 
 def softmax_topk(l: np.ndarray, K: int):
-    """Returns (ids int32[K], w float64[K]) exactly as Appendix A writes it."""
+    """Returns (ids int32[K], w float64[K]) as Appendix A writes it.
+
+    softmax is strictly increasing, so top-k of g = softmax(l) is top-k of l in exact
+    arithmetic; the ranking is taken on l itself because in floating point exp()
+    underflows far below the maximum logit and would turn distinct scores into ties.
+    The weights are g[inds] / sum(g[inds]) from the full softmax, as written.
+    """
     g = softmax(l)
-    inds = topk_desc(g, K)
+    inds = topk_desc(l, K)
     sel = g[inds]
     return inds, sel / sel.sum()
 

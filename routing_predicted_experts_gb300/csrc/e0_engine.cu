@@ -434,7 +434,7 @@ __device__ void resolve_route(Prod& pr, const LayerDesc& Ld, int l, bool self_ro
           idx = Ld.slot_of[idx];
           if (idx < 0) { vk = false; raise_error(P, C, E0_DEV_NOT_RESIDENT); }
         }
-        if (vk && idx >= Ld.n_routed) { vk = false; raise_error(P, C, E0_DEV_BAD_ID); }
+        if (vk && Ld.gu_q && idx >= Ld.n_routed) { vk = false; raise_error(P, C, E0_DEV_BAD_ID); }
         C.r_idx[slot][lane] = vk ? idx : 0;
       }
       valid = __ballot_sync(0xffffffffu, vk);

@@ -6,7 +6,7 @@ from oracle import bf16 as OB
 
 def to_dev(a, dtype):
     import torch
-    return torch.from_numpy(np.ascontiguousarray(a)).to(dtype).cuda()
+    return torch.from_numpy(np.array(a, copy=True)).to(dtype).cuda()
 
 
 def bf16_dev(bits):

@@ -34,6 +34,14 @@ def test_topk_ties_go_to_lower_index_and_k1_weight_is_one():
     assert list(ids) == [1] and w[0] == 1.0
 
 
+def test_topk_ranks_logits_that_underflow_in_softmax():
+    # exp(-1e4) underflows to 0 in fp64: the ranking must still follow the logits
+    l = np.array([0.3, -0.2, 0.9, 1e4, 0.1])
+    ids, w = OR.softmax_topk(l, 3)
+    assert list(ids) == [3, 2, 0]
+    assert w[0] == 1.0 and w[1] == 0.0
+
+
 def test_routing_brute_force_tiny():
     rng = np.random.default_rng(5)
     for _ in range(20):
