@@ -1,0 +1,462 @@
+"""Decode benchmark: the 40-layer int4 MoE stack (35B-A3B-class layers), one token per step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--k 4|8] [--impl ours|reference]
+
+A step is one decode token through all 40 layer-steps (prerouter heads on layers 6..38
+committing the routing of layers 7..38 one token ahead; layers 0..6 and 39, and every
+layer at the first token, route with their own gate), i.e. one e0_stack_step launch.
+Weights are synthetic, drawn on the GPU from the seeded generator and packed with
+e0_pack_int4; they occupy ~19 GB of HBM and every step streams 652.8 MB (K=4) of them,
+so the working set is far larger than L2.
+
+Prints ONE JSON line on rank 0.  Under torchrun (N > 1) every rank runs an independent
+replica on its own GPU (the path does not shard); value = tokens of all ranks / the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode tok/s (40-layer int4 MoE stack, K=4) and achieved HBM GB/s vs peak"
+SEED = 0
+
+
+def algorithmic_bytes_per_token(d=2048, E=256, F=512, K=4, H=1024, r=16, L=40, heads=33, routers=8,
+                                shared=True) -> int:
+    """Weight bytes one decode token must read (activations of a few KB ignored).
+
+    Per layer: K routed experts + the shared expert (int4 g64: gate/up/down codes plus
+    bf16 scale and bias per 64 weights) + LoRA (int4 d x d base + bf16 A and B); per
+    head: fc1 hidden block, the 2K one-hot columns it gathers, b1, fc2, b2, Lres; per
+    self-routing layer: its bf16 gate R [E][d]."""
+    def q4(rows, cols):
+        return rows * cols // 2 + rows * (cols // 64) * 4
+    expert = q4(2 * F, d) + q4(d, F)
+    lora = q4(d, d) + 2 * r * d + 2 * d * r
+    head = 2 * H * d + 2 * K * 2 * H + 2 * H + 2 * E * H + 2 * E + 2 * E * d
+    router = 2 * E * d
+    return L * ((K + (1 if shared else 0)) * expert + lora) + heads * head + routers * router
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return float(j["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("e0_engine.cu", "e0_engine.cuh", "e0_common.cuh"):
+        h.update(open(os.path.join(ROOT, "routing_predicted_experts_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_per_launch():
+    """dram bytes per launch from the committed ncu summary, if taken on this kernel source."""
+    p = os.path.join(ROOT, "profiles", "engine_stack_traffic.json")
+    if not os.path.exists(p):
+        return None
+    j = json.load(open(p))
+    if j.get("kernel_src_sha") != _kernel_source_hash():
+        return None
+    return j.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self, t_start: float, t_end: float):
+        rows = []
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5], f[6], f[7], f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[2:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        busy = [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ our arm
+def build_stack(K: int, device):
+    import torch
+    from routing_predicted_experts_gb300 import binding as B, model as M, synth as S
+    sh = S.LAYER35B(K)
+    L = S.STACK_LAYERS
+    layers, structs, pre = [], [], []
+    for l in range(L):
+        ly = M.build_layer(SEED, l, sh, with_head=(l in S.HEAD_OWNERS), device=device)
+        layers.append(ly)
+        structs.append(B.e0_layer_struct(ly["routed"], ly["shared"], ly["lora"], ly["head"], ly["router"]))
+        pre.append(1 if l in S.PREROUTED else 0)
+    torch.cuda.synchronize()
+    return B.Stack(B.dims(sh.d, sh.E, sh.F, sh.K), structs, pre, keepalive=layers), sh, L
+
+
+def run_ours(args, rank: int, world: int, local_rank: int):
+    import torch
+    from routing_predicted_experts_gb300 import binding as B, synth as S
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    t_build = time.time()
+    stack, sh, L = build_stack(args.k, dev)
+    build_s = time.time() - t_build
+    d = sh.d
+    n_steps = args.warmup + args.steps
+    # per-step inputs, resident in HBM before timing: h0 [steps][d], increments [steps][L][d]
+    h0 = torch.empty((n_steps, d), dtype=torch.int16, device=dev)
+    incr = torch.empty((n_steps, L, d), dtype=torch.int16, device=dev)
+    B.e0_synth_normal(h0, SEED, S.stream_id("bench.h0"), 0, 1.0)
+    B.e0_synth_normal(incr, SEED, S.stream_id("bench.incr"), 0, 1.0)
+    h_out = torch.empty((n_steps, d), dtype=torch.int16, device=dev)
+    ws = stack.workspace(dev)
+    stream = torch.cuda.current_stream()
+
+    for t in range(args.warmup):
+        stack.step(t, h0[t], incr[t], h_out[t], ws)
+    torch.cuda.synchronize()
+    if B.e0_get_device_status(ws) != 0:
+        raise RuntimeError("device status after warm-up: %d" % B.e0_get_device_status(ws))
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for t in range(args.warmup, n_steps):
+        stack.step(t, h0[t], incr[t], h_out[t], ws)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    if sampler:
+        sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    st = B.e0_get_device_status(ws)
+    if st != 0:
+        raise RuntimeError("device status after timed steps: %d" % st)
+
+    # end to end through the public API with host buffers: pinned H2D of the step's
+    # inputs, the stack step, D2H of the step's result, every step
+    h0_host = h0.cpu().pin_memory()
+    incr_host = incr.cpu().pin_memory()
+    out_host = torch.empty((n_steps, d), dtype=torch.int16).pin_memory()
+    h0_dev = torch.empty(d, dtype=torch.int16, device=dev)
+    incr_dev = torch.empty((L, d), dtype=torch.int16, device=dev)
+    hout_dev = torch.empty(d, dtype=torch.int16, device=dev)
+    ws2 = stack.workspace(dev)
+    e2e_steps = args.steps
+    for t in range(args.warmup):
+        h0_dev.copy_(h0_host[t], non_blocking=True)
+        incr_dev.copy_(incr_host[t], non_blocking=True)
+        stack.step(t, h0_dev, incr_dev, hout_dev, ws2)
+        out_host[t].copy_(hout_dev, non_blocking=True)
+    torch.cuda.synchronize()
+    e0e, e1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0e.record(stream)
+    for t in range(args.warmup, args.warmup + e2e_steps):
+        h0_dev.copy_(h0_host[t], non_blocking=True)
+        incr_dev.copy_(incr_host[t], non_blocking=True)
+        stack.step(t, h0_dev, incr_dev, hout_dev, ws2)
+        out_host[t].copy_(hout_dev, non_blocking=True)
+    e1e.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0e.elapsed_time(e1e)
+
+    if args.trace:
+        # a few extra steps with %globaltimer stamps per CTA and layer (diagnostics)
+        import ctypes
+        import numpy as np
+        from routing_predicted_experts_gb300 import _lib
+        buf = torch.zeros((160, L, 8), dtype=torch.int64, device=dev)
+        _lib.check(_lib.lib().e0_debug_trace(ctypes.c_void_p(buf.data_ptr()), buf.numel() * 8))
+        stamps = []
+        for t in range(args.warmup + e2e_steps, args.warmup + e2e_steps + 4):
+            stack.step(t, h0_dev, incr_dev, hout_dev, ws2)
+            torch.cuda.synchronize()
+            stamps.append(buf.cpu().numpy().copy())
+        _lib.check(_lib.lib().e0_debug_trace(None, 0))
+        np.save(args.trace, np.stack(stamps))
+
+    times = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    ms, e2e_ms = float(times[0]), float(times[1])
+    stack.close()
+    if rank != 0:
+        return None
+
+    tok_s = world * args.steps / (ms / 1e3)
+    e2e_tok_s = world * e2e_steps / (e2e_ms / 1e3)
+    bpt = algorithmic_bytes_per_token(K=args.k)
+    peak, peak_kind = _peaks()
+    per_launch_s = (ms / 1e3) / args.steps
+    achieved = bpt / per_launch_s / 1e9
+    clocks = sampler.summary(0, 0) if sampler else None
+    line = {
+        "metric": METRIC if args.k == 4 else METRIC.replace("K=4", f"K={args.k}"),
+        "value": round(tok_s, 1),
+        "unit": "tok/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int4 weights x int16-quantised activations -> fp32 accumulate; bf16 in/out",
+        "data": "synthetic (seeded N(0,0.02) weights packed int4 g64; N(0,1) hidden states and per-layer increments)",
+        "config": {
+            "workload": f"40-layer int4 MoE decode stack, 35B-A3B-class layers (d=2048, E=256, F=512, K={args.k}, "
+                        "shared expert F=512, LoRA r=16 alpha=32 on d x d, prerouter heads H=1024 on layers 6-38 "
+                        "routing layers 7-38), 1 token per step, one persistent launch per token",
+            "l2": "inputs larger than L2: every step streams %.1f MB of weights (L2 129 MB)" % (bpt / 1e6),
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+            "bytes_per_token": bpt,
+            "hbm_gbs_achieved": round(achieved, 1),
+            "build_s": round(build_s, 1),
+        },
+        "roofline": {
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+            "frac_of_nominal_8tbs": round(achieved / 8000.0, 4),
+            "kernel": "e0eng::engine_kernel<2048> (stack mode), one launch per token",
+            "traffic": _traffic_per_launch(),
+        },
+        "e2e": {"value": round(e2e_tok_s, 1), "unit": "tok/s",
+                "h2d_bytes_per_step": int(h0_dev.numel() * 2 + incr_dev.numel() * 2),
+                "d2h_bytes_per_step": int(hout_dev.numel() * 2)},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.k, budget_s=args.cpu_budget)
+    return line
+
+
+# ------------------------------------------------------------------ oracle timing
+def _oracle_sample_layers(K: int):
+    """Two sampled layers of the stack for oracle timing: one with a head (33 of 40
+    layers run one), one without."""
+    from oracle import model_inputs as OM
+    from routing_predicted_experts_gb300 import synth as S
+    sh = S.LAYER35B(K)
+    lay_h = OM.layer(SEED, 7, sh, with_head=True)
+    lay_n = OM.layer(SEED, 39, sh, with_head=False)
+    return sh, lay_h, lay_n
+
+
+def oracle_worker(K: int, budget_s: float, steps: int | None = None) -> dict:
+    """Time the oracle (as it stands) on the host: layer-steps of a sampled head layer and
+    a sampled head-less layer; a token is 33 of the former + 7 of the latter + 8 gates."""
+    import numpy as np
+    from oracle import layer as OL, model_inputs as OM, routing as OR
+    t_prep = time.time()
+    sh, lay_h, lay_n = _oracle_sample_layers(K)
+    R = OM.router_weights(SEED, 0, sh)
+    h = OM.hidden(SEED, 0, sh.d)
+    z = OM.supplied_logits(SEED, "cur", sh.E)
+    ids, _ = OR.softmax_topk(z, K)
+    for e in ids:  # draw and dequantise the sampled experts before timing
+        lay_h["expert"](int(e)); lay_n["expert"](int(e))
+    prep_s = time.time() - t_prep
+    th, tn, tr = [], [], []
+    t0 = time.time()
+    n = 0
+    while True:
+        a = time.perf_counter(); OL.layer_step(h, lay_h, ids, z, ids, K); b = time.perf_counter()
+        OL.layer_step(h, lay_n, ids, z, None, K); c = time.perf_counter()
+        OL.router_logits(OL.rmsnorm(np.zeros(sh.d) + 1.0), R); d_ = time.perf_counter()
+        th.append(b - a); tn.append(c - b); tr.append(d_ - c)
+        n += 1
+        if steps is not None:
+            if n >= steps:
+                break
+        elif time.time() - t0 >= budget_s:
+            break
+    per_token = 33 * statistics.median(th) + 7 * statistics.median(tn) + 8 * statistics.median(tr)
+    return {"tok_s": 1.0 / per_token, "per_token_s": per_token, "reps": n, "prep_s": round(prep_s, 1),
+            "layer_head_s": statistics.median(th), "layer_nohead_s": statistics.median(tn)}
+
+
+def cpu_baseline(K: int, budget_s: float = 10.0) -> dict:
+    """Run the oracle timing in a fresh single-threaded interpreter (BLAS pinned to 1 thread)."""
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[v] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-worker", "--k", str(K),
+           "--cpu-budget", str(budget_s)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        return {"value": None, "unit": "tok/s", "cores": 1, "kind": "oracle", "error": r.stderr[-400:]}
+    j = json.loads(r.stdout.strip().splitlines()[-1])
+    cpu = ""
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                cpu = line.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    return {"value": round(j["tok_s"], 4), "unit": "tok/s", "cores": 1, "kind": "oracle",
+            "sample": f"fp64 numpy oracle, 1 thread: {j['reps']} repetitions of one head layer-step (layer 7) "
+                      f"+ one head-less layer-step (layer 39) + one gate GEMV of the 40-layer K={K} workload; "
+                      f"token time = 33 x head layer + 7 x head-less layer + 8 x gate "
+                      f"({j['per_token_s']:.3f} s/token); weights drawn and dequantised before timing "
+                      f"({j['prep_s']} s); host cpu: {cpu or 'unknown'}, nproc {os.cpu_count()}"}
+
+
+def run_reference(args) -> dict:
+    """Reference arm: the CPU oracle as it stands, on the host cores, same metric/config."""
+    env_cores = 1
+    j = None
+    per_step = []
+    import numpy as np  # noqa: F401
+    from oracle import layer as OL, model_inputs as OM, routing as OR
+    sh, lay_h, lay_n = _oracle_sample_layers(args.k)
+    h = OM.hidden(SEED, 0, sh.d)
+    z = OM.supplied_logits(SEED, "cur", sh.E)
+    ids, _ = OR.softmax_topk(z, args.k)
+    for _ in range(args.warmup):
+        OL.layer_step(h, lay_h, ids, z, ids, args.k)
+    for _ in range(args.steps):
+        a = time.perf_counter()
+        OL.layer_step(h, lay_h, ids, z, ids, args.k)
+        b = time.perf_counter()
+        OL.layer_step(h, lay_n, ids, z, None, args.k)
+        c = time.perf_counter()
+        per_step.append(33 * (b - a) + 7 * (c - b))
+    tok_s = args.steps / sum(per_step)
+    line = {
+        "impl": "reference",
+        "metric": METRIC if args.k == 4 else METRIC.replace("K=4", f"K={args.k}"),
+        "value": round(tok_s, 4), "unit": "tok/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * sum(per_step) / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"40-layer int4 MoE decode stack, 35B-A3B-class layers, K={args.k} "
+                               "(CPU oracle, host cores)"},
+        "cpu_baseline": {"value": round(tok_s, 4), "unit": "tok/s", "cores": env_cores, "kind": "oracle",
+                         "sample": "each step: one head layer-step (layer 7) and one head-less layer-step "
+                                   "(layer 39) of the oracle; token time = 33 x + 7 x those"},
+        "e2e": {"value": round(tok_s, 4), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    del j
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4096)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--k", type=int, default=4)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--oracle-worker", action="store_true")
+    ap.add_argument("--trace", default=None, help="write per-CTA per-layer timer stamps of 4 extra steps (.npy)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    if args.oracle_worker:
+        print(json.dumps(oracle_worker(args.k, args.cpu_budget)))
+        return
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            if args.steps > 64:  # each reference step is a bounded oracle sample (~0.1-1 s)
+                args.steps = 64
+            for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS"):
+                os.environ.setdefault(v, "1")
+            print(json.dumps(run_reference(args)))
+        return
+
+    # the oracle subprocess is started before any GPU work in this process
+    pre_cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        pre_cpu = cpu_baseline(args.k, budget_s=args.cpu_budget)
+        args.no_cpu_baseline = True
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if pre_cpu is not None:
+            line["cpu_baseline"] = pre_cpu
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

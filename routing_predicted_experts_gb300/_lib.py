@@ -76,6 +76,7 @@ PROTOTYPES = {
     "e0_stack_step": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
     "e0_synth_normal": (i32, [vp, i64, u64, u32, i64, f64, i32, vp]),
     "e0_debug_inject_stall": (i32, [vp, u64, vp]),
+    "e0_debug_trace": (i32, [vp, sz]),
 }
 
 _lib = None

@@ -35,6 +35,7 @@ extern "C" const char* e0_version(void) { return "libe0 0.1 (sm_103a)"; }
 namespace {
 
 constexpr uint64_t DEFAULT_TIMEOUT_NS = 2000000000ull;  // 2 s per bounded wait
+thread_local uint64_t* g_trace = nullptr;                // diagnostics buffer for the next launches
 
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -257,6 +258,7 @@ void base_params(EngineParams& P, int d, int E, int F, int K, int L, int ncta, i
   P.norm = 1; P.out_dim = d; P.kinds = 1;
   P.timeout_ns = DEFAULT_TIMEOUT_NS;
   P.wl = ws_layout(E, L);
+  P.trace = g_trace;
 }
 
 void set_inline_plan(EngineParams& P, const CachedPlan& cp) {
@@ -284,6 +286,12 @@ extern "C" e0_status e0_get_device_status(const void* ws, uint32_t* status_out, 
   WsHeader h;
   E0_CHECK_CUDA(cudaMemcpy(&h, ws, sizeof(h), cudaMemcpyDeviceToHost));
   *status_out = h.status;
+  return E0_OK;
+}
+
+extern "C" e0_status e0_debug_trace(uint64_t* buf, size_t bytes) {
+  E0_REQUIRE(!buf || bytes >= 8, E0_ERR_INVALID, "e0_debug_trace: buffer too small");
+  g_trace = buf;
   return E0_OK;
 }
 

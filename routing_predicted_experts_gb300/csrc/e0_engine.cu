@@ -111,6 +111,13 @@ __device__ __forceinline__ bool spin_until(const EngineParams& P, Ctl& C, Pred p
 
 __device__ __forceinline__ void cbar() { named_bar_sync(1, NCT); }
 
+// Diagnostics: stamp %globaltimer into trace[cta][l][slot] when a trace buffer is set.
+// Slots: 0 consumer layer start, 1 dependency satisfied, 2 layer input built,
+// 3 units done, 4 producer route published, 5 producer issued the layer's last stage.
+__device__ __forceinline__ void stamp(const EngineParams& P, int l, int slot) {
+  if (P.trace) P.trace[((size_t)blockIdx.x * P.L + l) * 8 + slot] = globaltimer();
+}
+
 __device__ __forceinline__ float bflo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bfhi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 __device__ __forceinline__ float bf(uint16_t u) { return __uint_as_float((uint32_t)u << 16); }
@@ -502,9 +509,11 @@ __device__ void producer(const EngineParams& P, Ctl& C, uint8_t* ring) {
     }
     pr.ok = __shfl_sync(0xffffffffu, pr.ok ? 1 : 0, 0) != 0;
     resolve_route(pr, Ld, l, self_route, par, p3);
+    if (pr.lane == 0) stamp(P, l, 4);
     int nu;
     const Unit* us = units_of(P, P.plan ? Ld.plan_kind : 0, blockIdx.x, nu);
     for (int i = 0; i < nu; ++i) issue_unit(pr, Ld, us[i], l);
+    if (pr.lane == 0) stamp(P, l, 5);
     pr.ok = __shfl_sync(0xffffffffu, pr.ok ? 1 : 0, 0) != 0;
   }
   // Wait for every issued copy to land before the CTA may exit.
@@ -893,12 +902,15 @@ __device__ void consumer(const EngineParams& P, Ctl& C, uint8_t* ring) {
 
   for (int l = 0; l < P.L; ++l) {
     const LayerDesc& Ld = layer_at(P, l);
+    if (tid == 0) stamp(P, l, 0);
     if (l > 0 && P.mode == MODE_STACK) {
       if (tid == 0)
         spin_until(P, C, [&] { return ld_acquire_u32(ctr(P, par, l - 1, 0)) >= (uint32_t)ncta; }, P.timeout_ns);
       cbar();
     }
+    if (tid == 0) stamp(P, l, 1);
     layer_input(cs, l, par);
+    if (tid == 0) stamp(P, l, 2);
     float* acc = acc_ptr(P, par, l);
     float* zh = zhat_ptr(P, pnext3, l);
     float* zr = zr_ptr(P, par, l);
@@ -916,6 +928,7 @@ __device__ void consumer(const EngineParams& P, Ctl& C, uint8_t* ring) {
     int nu;
     const Unit* us = units_of(P, P.plan ? Ld.plan_kind : 0, cta, nu);
     for (int i = 0; i < nu; ++i) consume_unit<D>(cs, Ld, us[i], l, acc, zh, zr);
+    if (tid == 0) stamp(P, l, 3);
 
     if (l == P.L - 1) {
       // Clear the other half of the parity-duplicated buffers for the next launch.

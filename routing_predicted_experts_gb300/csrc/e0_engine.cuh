@@ -168,6 +168,7 @@ struct EngineParams {
   uint16_t* h_trace;
   int32_t accumulate;
   int32_t pad1;
+  uint64_t* trace;             // nullable: [ncta][L][8] %globaltimer stamps (diagnostics)
   uint8_t* ws;
   WsLayout wl;
   LayerDesc inline_layer;
