@@ -205,6 +205,26 @@ e0_status e0_moe_decode_layer(const e0_dims* dims, const e0_experts* routed,
                               size_t workspace_bytes, e0_stream stream);
 
 /* --------------------------------------------------------------------------------
+ * e0_moe_decode_layer_noalloc — the same single-token layer-step (T = 1) as
+ * e0_moe_decode_layer, for callers that cannot allocate device memory (a host
+ * callback or real-time loop that must not enter the allocator, a plugin whose host
+ * framework owns every allocation).  No counterpart in the paper: it is a packaging
+ * of this library.  The workspace lives in a fixed 128 KiB array inside the library's
+ * device memory, reserved on every GPU that loads it until the process exits; dims
+ * whose workspace (e0_workspace_size(dims, 1)) exceeds it return E0_ERR_NOMEM.  The
+ * first call on a device looks the array up (make it before any stream capture).
+ * Each call clears the part it uses on `stream` first; calls that overlap on the GPU
+ * (different streams) share the array and race.  Arguments as e0_moe_decode_layer.
+ * ------------------------------------------------------------------------------ */
+e0_status e0_moe_decode_layer_noalloc(const e0_dims* dims, const e0_experts* routed,
+                                      const e0_experts* shared, const e0_qlora* lora,
+                                      const e0_prerouter* head, const uint16_t* h_in,
+                                      const int32_t* ids, const float* logits,
+                                      const int32_t* ids_prev, uint16_t* h_out,
+                                      float* delta_f32, float* next_logits, int32_t* next_ids,
+                                      float* next_weights, e0_stream stream);
+
+/* --------------------------------------------------------------------------------
  * Decode stack: L layer-steps for one token in ONE launch (§3.2 "Two consumption
  * profiles": routing for layer l at token t is the prediction made by head l-1 at
  * token t-1, on layers whose previous layer owns a head; other layers, and every
