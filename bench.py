@@ -131,17 +131,27 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ our arm
-def build_stack(K: int, device):
+def stack_schedule(L: int):
+    """Head owners and prerouted layers: 6..38 / 7..38 for the 40-layer stack; a shorter
+    stack (profiling) keeps heads on 1..L-2 so it still mixes both kinds of layer."""
+    from routing_predicted_experts_gb300 import synth as S
+    if L == S.STACK_LAYERS:
+        return set(S.HEAD_OWNERS), set(S.PREROUTED)
+    owners = set(range(1, L - 1))
+    return owners, {l + 1 for l in owners}
+
+
+def build_stack(K: int, device, L: int = 40):
     import torch
     from routing_predicted_experts_gb300 import binding as B, model as M, synth as S
     sh = S.LAYER35B(K)
-    L = S.STACK_LAYERS
+    owners, prerouted = stack_schedule(L)
     layers, structs, pre = [], [], []
     for l in range(L):
-        ly = M.build_layer(SEED, l, sh, with_head=(l in S.HEAD_OWNERS), device=device)
+        ly = M.build_layer(SEED, l, sh, with_head=(l in owners), device=device)
         layers.append(ly)
         structs.append(B.e0_layer_struct(ly["routed"], ly["shared"], ly["lora"], ly["head"], ly["router"]))
-        pre.append(1 if l in S.PREROUTED else 0)
+        pre.append(1 if l in prerouted else 0)
     torch.cuda.synchronize()
     return B.Stack(B.dims(sh.d, sh.E, sh.F, sh.K), structs, pre, keepalive=layers), sh, L
 
@@ -152,7 +162,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     t_build = time.time()
-    stack, sh, L = build_stack(args.k, dev)
+    stack, sh, L = build_stack(args.k, dev, args.layers)
     build_s = time.time() - t_build
     d = sh.d
     n_steps = args.warmup + args.steps
@@ -225,10 +235,11 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         import ctypes
         import numpy as np
         from routing_predicted_experts_gb300 import _lib
-        buf = torch.zeros((160, L, 8), dtype=torch.int64, device=dev)
+        buf = torch.zeros((160, L, 16), dtype=torch.int64, device=dev)
         _lib.check(_lib.lib().e0_debug_trace(ctypes.c_void_p(buf.data_ptr()), buf.numel() * 8))
         stamps = []
         for t in range(args.warmup + e2e_steps, args.warmup + e2e_steps + 4):
+            buf.zero_()
             stack.step(t, h0_dev, incr_dev, hout_dev, ws2)
             torch.cuda.synchronize()
             stamps.append(buf.cpu().numpy().copy())
@@ -245,7 +256,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     tok_s = world * args.steps / (ms / 1e3)
     e2e_tok_s = world * e2e_steps / (e2e_ms / 1e3)
-    bpt = algorithmic_bytes_per_token(K=args.k)
+    owners, prerouted = stack_schedule(L)
+    bpt = algorithmic_bytes_per_token(K=args.k, L=L, heads=len(owners), routers=L - len(prerouted))
     peak, peak_kind = _peaks()
     per_launch_s = (ms / 1e3) / args.steps
     achieved = bpt / per_launch_s / 1e9
@@ -412,6 +424,7 @@ def main():
     ap.add_argument("--steps", type=int, default=4096)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--k", type=int, default=4)
+    ap.add_argument("--layers", type=int, default=40, help="stack depth (40 = the benchmark; fewer for profiling)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)

@@ -275,11 +275,12 @@ e0_status e0_synth_normal(void* out, int64_t n, uint64_t seed, uint32_t stream_i
 e0_status e0_debug_inject_stall(void* workspace, uint64_t limit_ns, e0_stream stream);
 
 /* Debug / profiling: when buf != NULL, later engine launches from this thread write
- * %globaltimer stamps to buf[cta][layer][8] (u64, device memory of at least
- * ncta * layers * 64 bytes; ncta <= 160).  Slots: 0 consumer layer start, 1 layer
- * dependency satisfied, 2 layer input built, 3 layer's units done, 4 producer
- * published the layer's routing, 5 producer issued the layer's last copy.
- * buf == NULL switches tracing off. */
+ * %globaltimer stamps to buf[cta][layer][16] (u64, zero-filled device memory of at
+ * least ncta * layers * 128 bytes; ncta <= 160).  Slots: 0 consumer layer start,
+ * 1 layer dependency satisfied, 2 layer input built, 3 layer's units done,
+ * 4 producer published the layer's routing, 5 producer issued the layer's last copy,
+ * 6 ns consumer warp 0 waited for stages, 7 stages it took, 8 + unit type: ns spent
+ * in units of that type (accumulated).  buf == NULL switches tracing off. */
 e0_status e0_debug_trace(uint64_t* buf, size_t bytes);
 
 #ifdef __cplusplus

@@ -107,10 +107,22 @@ e0_status build_plan(const PlanSpec& s, int ncta, Unit* units, uint8_t* counts) 
   }
   // 2. divisible work as granules
   std::vector<Granule> gs;
-  if (s.lora)
-    for (int r = 0; r < s.lout; r += 16) gs.push_back({U_QROWS, r, 16, W_INT4 * 16.0 * q4_row_bytes(d)});
-  if (s.lora_ab)
-    for (int q = 0; q < s.lr; ++q) gs.push_back({U_LORA_AB, q, 1, W_BF16 * (2.0 * d + 2.0 * s.lout)});
+  {
+    // LoRA base rows with the rank slices spread between them, so that the ranks land
+    // on different CTAs rather than piling up on one
+    std::vector<Granule> qr, ab;
+    if (s.lora)
+      for (int r = 0; r < s.lout; r += 16) qr.push_back({U_QROWS, r, 16, W_INT4 * 16.0 * q4_row_bytes(d)});
+    if (s.lora_ab)
+      for (int q = 0; q < s.lr; ++q) ab.push_back({U_LORA_AB, q, 1, W_BF16 * (2.0 * d + 2.0 * s.lout)});
+    const size_t every = ab.empty() ? 0 : std::max<size_t>(1, qr.size() / ab.size());
+    size_t ia = 0;
+    for (size_t i = 0; i < qr.size(); ++i) {
+      gs.push_back(qr[i]);
+      if (every && (i + 1) % every == 0 && ia < ab.size()) gs.push_back(ab[ia++]);
+    }
+    while (ia < ab.size()) gs.push_back(ab[ia++]);
+  }
   if (s.lres)
     for (int e = 0; e < s.E; e += 8) gs.push_back({U_LRES, e, 8, W_BF16 * 8.0 * 2.0 * d});
   if (s.head)
@@ -135,7 +147,8 @@ e0_status build_plan(const PlanSpec& s, int ncta, Unit* units, uint8_t* counts) 
       bool merged = false;
       for (auto& u : L) {
         if (u.type == gr.type && u.r1 == gr.row) {
-          const int limit = gr.type == U_HEAD ? HEAD_ROWS : (gr.type == U_LORA_AB ? RANKS_MAX : 65535);
+          const int limit = (gr.type == U_HEAD || gr.type == U_LRES) ? HEAD_ROWS
+                            : (gr.type == U_LORA_AB ? 4 : 65535);
           if ((int)u.r1 - (int)u.r0 + gr.rows <= limit) {
             u.r1 = (uint16_t)(gr.row + gr.rows);
             merged = true;
@@ -470,7 +483,7 @@ struct e0_stack {
 
 extern "C" e0_status e0_stack_create(e0_stack** out, const e0_dims* dims, const e0_layer* layers, int32_t L,
                                      const int8_t* prerouted_from) {
-  E0_REQUIRE(out && layers && L >= 1 && L <= 64, E0_ERR_INVALID, "e0_stack_create: need 1..64 layers");
+  E0_REQUIRE(out && layers && L >= 1 && L <= LMAX, E0_ERR_INVALID, "e0_stack_create: need 1..64 layers");
   *out = nullptr;
   e0_status st = check_dims(dims);
   if (st) return st;

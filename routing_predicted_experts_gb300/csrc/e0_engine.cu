@@ -20,39 +20,51 @@ struct Ctl {
   float xinv[DMAX / 32];      // per 32-element chunk: dequant step of xq
   float xsum[DMAX / 32];      // per 32-element chunk: sum of x
   float abuf[32];             // SwiGLU activations of the current expert slab
+  uint4 aq[4];                // ... quantised to int16 in the dot32 order
+  float ascale[2];            // ... their dequant step and sum
+  float b2buf[HEAD_ROWS];     // head fc2 bias slice of the current LRES unit
   float ubuf[HEAD_ROWS];      // head fc1 pre-activation, then erf-GELU output
   float vbuf[RANKS_MAX];      // LoRA A x for the current rank slice
   float zbuf[EMAX];           // logits staged for top-K
-  int32_t r_ids[4][KMAX];     // committed expert ids per layer (ring of 4 layers)
-  int32_t r_idx[4][KMAX];     // stored index (slot) of each id
-  float r_w[4][KMAX];         // renormalised combine weights
-  int32_t r_prev[4][KMAX];    // ids this layer used at the previous token
-  uint32_t r_valid[4];
-  uint32_t r_prev_valid[4];
+  // routing of every layer of this launch
+  int16_t rt_ids[LMAX][KMAX];   // committed expert ids
+  int16_t rt_idx[LMAX][KMAX];   // stored index (slot) of each id
+  int16_t rt_prev[LMAX][KMAX];  // ids the layer used at the previous token
+  float rt_w[LMAX][KMAX];       // renormalised combine weights
+  uint32_t rt_valid[LMAX];
+  uint32_t rt_pvalid[LMAX];
+  volatile int32_t rt_ready[LMAX];
   float red[NCW];
   int32_t f_ids[KMAX];        // finisher top-K
   float f_vals[KMAX];
-  volatile int32_t route_seq;
-  volatile int32_t cons_done;
   volatile int32_t abort_flag;
   int32_t is_last;
   uint32_t epoch;
+  Unit su[KINDS_MAX][MAXU];   // this CTA's work units per plan kind
+  int32_t sn[KINDS_MAX];
+  uint32_t rt_tag[LMAX];      // staged: epoch each committed route is for
 };
 
-size_t smem_bytes() { return (size_t)NSTAGES * STAGE_BYTES + sizeof(Ctl); }
+// Dynamic shared memory: the stage ring, the control block, then a copy of the
+// layer descriptors (read on every layer by every warp, so kept on chip).
+constexpr size_t CTL_OFFSET = (size_t)NSTAGES * STAGE_BYTES;
+constexpr size_t LD_OFFSET = (CTL_OFFSET + sizeof(Ctl) + 15) & ~size_t(15);
+size_t smem_bytes() { return LD_OFFSET + sizeof(LayerDesc) * LMAX; }
+
+extern __shared__ __align__(1024) uint8_t e0_smem[];
 
 // ------------------------------------------------------------------ small helpers
 __device__ __forceinline__ const LayerDesc& layer_at(const EngineParams& P, int l) {
-  return P.layers ? P.layers[l] : P.inline_layer;
+  (void)P;
+  return reinterpret_cast<const LayerDesc*>(e0_smem + LD_OFFSET)[l];
 }
 
 __device__ __forceinline__ const Unit* units_of(const EngineParams& P, int kind, int cta, int& n) {
-  if (P.plan) {
-    n = P.plan_n[kind * P.ncta + cta];
-    return P.plan + ((size_t)kind * P.ncta + cta) * MAXU;
-  }
-  n = P.inline_n[cta];
-  return P.inline_plan + (size_t)cta * MAXU;
+  (void)P;
+  (void)cta;
+  const Ctl& C = *reinterpret_cast<const Ctl*>(e0_smem + CTL_OFFSET);
+  n = C.sn[kind];
+  return C.su[kind];
 }
 
 __device__ __forceinline__ WsHeader* hdr(const EngineParams& P) { return reinterpret_cast<WsHeader*>(P.ws); }
@@ -73,6 +85,16 @@ __device__ __forceinline__ int32_t* idsu_ptr(const EngineParams& P, uint32_t par
 }
 __device__ __forceinline__ float* wu_ptr(const EngineParams& P, uint32_t par, int l) {
   return reinterpret_cast<float*>(P.ws + P.wl.wts) + ((size_t)par * P.L + l) * KMAX;
+}
+// routes committed for the next launch: ids [2][L][KMAX], weights, tag [2][L]
+__device__ __forceinline__ int32_t* rg_ids_ptr(const EngineParams& P, uint32_t par, int l) {
+  return reinterpret_cast<int32_t*>(P.ws + P.wl.rg_ids) + ((size_t)par * P.L + l) * KMAX;
+}
+__device__ __forceinline__ float* rg_w_ptr(const EngineParams& P, uint32_t par, int l) {
+  return reinterpret_cast<float*>(P.ws + P.wl.rg_w) + ((size_t)par * P.L + l) * KMAX;
+}
+__device__ __forceinline__ uint32_t* rg_tag_ptr(const EngineParams& P, uint32_t par, int l) {
+  return reinterpret_cast<uint32_t*>(P.ws + P.wl.rg_tag) + (size_t)par * P.L + l;
 }
 
 __device__ __noinline__ void raise_error(const EngineParams& P, Ctl& C, uint32_t bits) {
@@ -109,13 +131,26 @@ __device__ __forceinline__ bool spin_until(const EngineParams& P, Ctl& C, Pred p
   }
 }
 
+// Polling loops (inlined: an out-of-line call needs a stack frame, and local memory
+// is slow here because nearly all of L1 is given to shared memory).
+__device__ __forceinline__ bool wait_mbar(const EngineParams& P, Ctl& C, uint64_t* bar, uint32_t par) {
+  return spin_until(P, C, [&] { return mbar_try_wait(bar, par); }, P.timeout_ns);
+}
+__device__ __forceinline__ bool wait_flag(const EngineParams& P, Ctl& C, volatile int32_t* f) {
+  return spin_until(P, C, [&] { return *f != 0; }, P.timeout_ns);
+}
+__device__ __forceinline__ bool wait_count(const EngineParams& P, Ctl& C, const uint32_t* c, uint32_t target) {
+  return spin_until(P, C, [&] { return ld_acquire_u32(c) >= target; }, P.timeout_ns);
+}
+
 __device__ __forceinline__ void cbar() { named_bar_sync(1, NCT); }
 
 // Diagnostics: stamp %globaltimer into trace[cta][l][slot] when a trace buffer is set.
 // Slots: 0 consumer layer start, 1 dependency satisfied, 2 layer input built,
-// 3 units done, 4 producer route published, 5 producer issued the layer's last stage.
+// 3 units done, 4 producer route published, 5 producer issued the layer's last stage,
+// 6 ns warp 0 waited for stages, 7 stages it took, 8 + unit type: ns in that unit type.
 __device__ __forceinline__ void stamp(const EngineParams& P, int l, int slot) {
-  if (P.trace) P.trace[((size_t)blockIdx.x * P.L + l) * 8 + slot] = globaltimer();
+  if (P.trace) P.trace[((size_t)blockIdx.x * P.L + l) * 16 + slot] = globaltimer();
 }
 
 __device__ __forceinline__ float bflo(uint32_t u) { return __uint_as_float(u << 16); }
@@ -190,7 +225,7 @@ __device__ __forceinline__ uint64_t topk_key(float v, int e) {
 
 // Top-K of z[0..E) (shared memory), descending, ties to the lower index.  Writes
 // ids/vals (lane 0).  All 32 lanes must call.
-__device__ void warp_topk(const float* z, int E, int K, int lane, int32_t* ids, float* vals) {
+__device__ __noinline__ void warp_topk(const float* z, int E, int K, int lane, int32_t* ids, float* vals) {
   uint32_t taken = 0;
   uint64_t best = 0;
   for (int e = lane, m = 0; e < E; e += 32, ++m) best = max(best, topk_key(z[e], e));
@@ -214,6 +249,8 @@ __device__ void warp_topk(const float* z, int E, int K, int lane, int32_t* ids, 
 }
 
 // ------------------------------------------------------------------ producer
+// The whole producer warp runs this code in lock step; lane 0 issues the copies and
+// all lanes take part in routing (loads of logits and ids, warp top-K).
 struct Prod {
   const EngineParams& P;
   Ctl& C;
@@ -221,98 +258,302 @@ struct Prod {
   uint32_t n;      // stages issued
   bool ok;
   int lane;
-
-  // lane 0: wait until stage n's slot is free, return its base (nullptr on failure)
-  __device__ uint8_t* begin(uint32_t& slot) {
-    slot = n % NSTAGES;
-    const uint32_t round = n / NSTAGES;
-    if (round > 0) {
-      uint64_t* bar = &C.empty[slot];
-      const uint32_t par = (round - 1) & 1u;
-      if (!spin_until(P, C, [&] { return mbar_try_wait(bar, par); }, P.timeout_ns)) return nullptr;
-    }
-    return ring + (size_t)slot * STAGE_BYTES;
-  }
-  __device__ void commit() { ++n; }
+  uint32_t par, p3, epoch;
 };
 
-// Issue one stage worth of int4 rows [row0, row0+nr) of a row-layout matrix (in = D).
-__device__ __forceinline__ bool issue_q4_rows(Prod& pr, const uint32_t* q, const uint16_t* s, const uint16_t* b,
-                                              int in, int row0, int nr) {
-  if (pr.lane == 0 && pr.ok) {
-    uint32_t slot;
-    uint8_t* st = pr.begin(slot);
-    if (!st) {
-      pr.ok = false;
-    } else {
-      const uint32_t qb = (uint32_t)nr * in / 2, sb = (uint32_t)nr * in / 32;
-      mbar_arrive_expect_tx(&pr.C.full[slot], qb + 2 * sb);
-      tma_bulk_g2s(st, q + (size_t)row0 * (in / 8), qb, &pr.C.full[slot]);
-      tma_bulk_g2s(st + qb, s + (size_t)row0 * (in / 64), sb, &pr.C.full[slot]);
-      tma_bulk_g2s(st + qb + sb, b + (size_t)row0 * (in / 64), sb, &pr.C.full[slot]);
-      pr.commit();
+__device__ __forceinline__ bool self_routes(const EngineParams& P, int l) {
+  return P.mode == MODE_STACK && ((P.router_mask >> l) & 1ull);
+}
+
+// Publish the routing of layer l in the route table.  Lane k (< K) brings id k
+// (-1 = none) and its unnormalised combine weight; ids are checked (range,
+// duplicates, slot table) and the weights renormalised over the ids that survive.
+__device__ __noinline__ void publish_route(Prod& pr, int l, int id, float w) {
+  const EngineParams& P = pr.P;
+  Ctl& C = pr.C;
+  const LayerDesc& Ld = layer_at(P, l);
+  const int lane = pr.lane, K = P.K;
+  if (lane < K) C.rt_ids[l][lane] = (int16_t)id;
+  __syncwarp();
+  bool v = lane < K && id >= 0 && id < P.E;
+  if (lane < K)
+    for (int j = 0; j < lane; ++j)
+      if (C.rt_ids[l][j] == id) v = false;
+  if (lane < K && id != -1 && !v) raise_error(P, C, E0_DEV_BAD_ID);
+  int idx = v ? id : 0;
+  if (v && Ld.slot_of) {
+    idx = Ld.slot_of[id];
+    if (idx < 0) {
+      v = false;
+      raise_error(P, C, E0_DEV_NOT_RESIDENT);
     }
   }
-  return true;
+  if (v && Ld.gu_q && idx >= Ld.n_routed) {
+    v = false;
+    raise_error(P, C, E0_DEV_BAD_ID);
+  }
+  const uint32_t valid = __ballot_sync(0xffffffffu, v);
+  const float wv = v ? w : 0.f;
+  float tot = wv;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  if (lane < K) {
+    C.rt_idx[l][lane] = (int16_t)idx;
+    C.rt_w[l][lane] = (v && tot > 0.f) ? wv / tot : 0.f;
+  }
+  if (lane == 0) C.rt_valid[l] = valid;
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence_block();
+    C.rt_ready[l] = 1;
+    stamp(P, l, 4);
+  }
+  __syncwarp();
+}
+
+// Top-K of C.zbuf[0..E) (descending, ties to the lower id); lane k < K gets id k and
+// exp(z_k - z_max), the unnormalised softmax weight.
+__device__ __forceinline__ void topk_lane(Prod& pr, int& id, float& w) {
+  const EngineParams& P = pr.P;
+  Ctl& C = pr.C;
+  warp_topk(C.zbuf, P.E, P.K, pr.lane, C.f_ids, C.f_vals);  // lane 0 writes
+  __syncwarp();
+  id = -1;
+  w = 0.f;
+  if (pr.lane < P.K) {
+    id = C.f_ids[pr.lane];
+    w = expf(C.f_vals[pr.lane] - C.f_vals[0]);
+  }
+  __syncwarp();
+}
+
+// Kernel start: routing known at launch time (given ids, or the routes the previous
+// launch committed for this token) and the previous-token ids the heads one-hot.
+__device__ __noinline__ void load_routes(Prod& pr) {
+  const EngineParams& P = pr.P;
+  Ctl& C = pr.C;
+  const int lane = pr.lane, K = P.K;
+  if (P.mode == MODE_LAYER || P.mode == MODE_HEAD) {
+    int id = -1, pid = -1;
+    float z = 0.f;
+    if (P.ids_in && lane < K) id = P.ids_in[lane];
+    if (P.ids_prev_in && lane < K) pid = P.ids_prev_in[lane];
+    const bool inr = id >= 0 && id < P.E;
+    if (P.logits_in && inr) z = P.logits_in[id];
+    float mx = inr ? z : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float w = (P.logits_in && inr) ? expf(z - mx) : 0.f;
+    if (lane < K) C.rt_prev[0][lane] = (int16_t)pid;
+    __syncwarp();
+    bool pv = lane < K && pid >= 0 && pid < P.E;
+    if (lane < K)
+      for (int j = 0; j < lane; ++j)
+        if (C.rt_prev[0][j] == pid) pv = false;
+    if (lane < K && pid != -1 && !pv) raise_error(P, C, E0_DEV_BAD_ID);
+    const uint32_t pvalid = __ballot_sync(0xffffffffu, pv);
+    if (lane == 0) C.rt_pvalid[0] = pvalid;
+    __syncwarp();
+    if (P.ids_in) {
+      publish_route(pr, 0, id, w);
+    } else if (lane == 0) {
+      C.rt_valid[0] = 0u;
+      __threadfence_block();
+      C.rt_ready[0] = 1;
+    }
+    __syncwarp();
+    return;
+  }
+  if (P.mode != MODE_STACK) return;
+  // Stage, with independent loads issued back to back: the previous-token ids of every
+  // layer (recorded by the previous launch) and the routes it committed for this token.
+  const int L = P.L;
+  for (int j = lane; j < L * K; j += 32) {
+    const int l = j / K, k = j % K;
+    const int pid = P.step > 0 ? __ldcg(idsu_ptr(P, pr.par ^ 1u, l) + k) : -1;
+    const int id = __ldcg(rg_ids_ptr(P, pr.par, l) + k);
+    const float w = __ldcg(rg_w_ptr(P, pr.par, l) + k);
+    C.rt_prev[l][k] = (int16_t)pid;
+    C.rt_ids[l][k] = (int16_t)id;
+    C.rt_w[l][k] = w;
+  }
+  for (int l = lane; l < L; l += 32) C.rt_tag[l] = __ldcg(rg_tag_ptr(P, pr.par, l));
+  __syncwarp();
+  for (int l = 0; l < L; ++l) {
+    bool pv = false;
+    if (lane < K) {
+      const int pid = C.rt_prev[l][lane];
+      pv = pid >= 0 && pid < P.E;
+      for (int j = 0; j < lane; ++j)
+        if (C.rt_prev[l][j] == pid) pv = false;
+    }
+    const uint32_t pvalid = __ballot_sync(0xffffffffu, pv);
+    if (lane == 0) C.rt_pvalid[l] = pvalid;
+  }
+  __syncwarp();
+}
+
+// Publish the staged route of a prerouted layer (committed by the previous launch).
+__device__ __noinline__ void publish_staged_route(Prod& pr, int l) {
+  Ctl& C = pr.C;
+  const bool fresh = C.rt_tag[l] == pr.epoch;
+  int id = -1;
+  float w = 0.f;
+  if (pr.lane < pr.P.K && fresh) {
+    id = C.rt_ids[l][pr.lane];
+    w = C.rt_w[l][pr.lane];
+  }
+  __syncwarp();
+  if (!fresh && pr.lane == 0) raise_error(pr.P, C, E0_DEV_BAD_ID);  // not the step after the last one
+  publish_route(pr, l, id, w);
+}
+
+// Bounded wait helper for the producer warp: true while we may keep waiting.
+__device__ __forceinline__ bool prod_keep_waiting(Prod& pr, uint64_t t0, uint32_t it) {
+  if ((it & 15u) != 0) return true;
+  bool go = true;
+  if (pr.lane == 0) {
+    if (aborted(pr.P, pr.C)) {
+      go = false;
+    } else if (globaltimer() - t0 > pr.P.timeout_ns) {
+      raise_error(pr.P, pr.C, E0_DEV_TIMEOUT);
+      go = false;
+    }
+  }
+  return __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
+}
+
+// Wait (bounded) until counter `which` of layer l has every CTA's arrival.
+__device__ __forceinline__ bool prod_wait_counter(Prod& pr, int l, int which) {
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    bool r = false;
+    if (pr.lane == 0) r = ld_acquire_u32(ctr(pr.P, pr.par, l, which)) >= (uint32_t)pr.P.ncta;
+    if (__shfl_sync(0xffffffffu, r ? 1 : 0, 0)) return true;
+    if (!prod_keep_waiting(pr, t0, it)) return false;
+  }
+}
+
+// A layer that routes with its own gate: wait until every CTA wrote its gate rows,
+// then publish the top-K of the gate logits (routing warp).
+__device__ __noinline__ void compute_self_route(Prod& pr, int l) {
+  if (!pr.ok || pr.C.rt_ready[l]) return;
+  if (!prod_wait_counter(pr, l, 1)) {
+    pr.ok = false;
+    return;
+  }
+  const float* z = zr_ptr(pr.P, pr.par, l);
+#pragma unroll 8
+  for (int e = pr.lane; e < pr.P.E; e += 32) pr.C.zbuf[e] = __ldcg(z + e);
+  __syncwarp();
+  int id;
+  float w;
+  topk_lane(pr, id, w);
+  publish_route(pr, l, id, w);
+}
+
+// Producer: wait (bounded) until the routing warp has published layer l's route.
+__device__ __forceinline__ void need_route(Prod& pr, int l) {
+  if (!pr.ok || pr.C.rt_ready[l]) return;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1; !pr.C.rt_ready[l]; ++it) {
+    if (!prod_keep_waiting(pr, t0, it)) {
+      pr.ok = false;
+      return;
+    }
+  }
+}
+
+// Wait until stage n's slot is free; returns its base (nullptr after an abort).
+__device__ __forceinline__ uint8_t* prod_begin(Prod& pr, uint32_t& slot) {
+  slot = pr.n % NSTAGES;
+  const uint32_t round = pr.n / NSTAGES;
+  if (round > 0) {
+    uint64_t* bar = &pr.C.empty[slot];
+    const uint32_t par = (round - 1) & 1u;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+      bool fr = false;
+      if (pr.lane == 0) fr = mbar_try_wait(bar, par);
+      if (__shfl_sync(0xffffffffu, fr ? 1 : 0, 0)) break;
+      if (!prod_keep_waiting(pr, t0, it)) {
+        pr.ok = false;
+        return nullptr;
+      }
+    }
+  }
+  return pr.ring + (size_t)slot * STAGE_BYTES;
+}
+
+// Issue one stage of int4 rows [row0, row0+nr) of a row-layout matrix (in columns).
+__device__ __forceinline__ void issue_q4_rows(Prod& pr, const uint32_t* q, const uint16_t* s, const uint16_t* b, int in, int row0,
+                              int nr) {
+  if (!pr.ok) return;
+  uint32_t slot;
+  uint8_t* st = prod_begin(pr, slot);
+  if (!st) return;
+  if (pr.lane == 0) {
+    const uint32_t qb = (uint32_t)nr * in / 2, sb = (uint32_t)nr * in / 32;
+    mbar_arrive_expect_tx(&pr.C.full[slot], qb + 2 * sb);
+    tma_bulk_g2s(st, q + (size_t)row0 * (in / 8), qb, &pr.C.full[slot]);
+    tma_bulk_g2s(st + qb, s + (size_t)row0 * (in / 64), sb, &pr.C.full[slot]);
+    tma_bulk_g2s(st + qb + sb, b + (size_t)row0 * (in / 64), sb, &pr.C.full[slot]);
+  }
+  ++pr.n;
 }
 
 __device__ __forceinline__ void issue_bytes(Prod& pr, const void* src, uint32_t bytes) {
-  if (pr.lane == 0 && pr.ok) {
-    uint32_t slot;
-    uint8_t* st = pr.begin(slot);
-    if (!st) {
-      pr.ok = false;
-    } else {
-      mbar_arrive_expect_tx(&pr.C.full[slot], bytes);
-      tma_bulk_g2s(st, src, bytes, &pr.C.full[slot]);
-      pr.commit();
-    }
+  if (!pr.ok) return;
+  uint32_t slot;
+  uint8_t* st = prod_begin(pr, slot);
+  if (!st) return;
+  if (pr.lane == 0) {
+    mbar_arrive_expect_tx(&pr.C.full[slot], bytes);
+    tma_bulk_g2s(st, src, bytes, &pr.C.full[slot]);
   }
+  ++pr.n;
 }
 
 // Issue bf16 rows [row0, row1) of a [rows][in] matrix, in stage-sized chunks.
-__device__ void issue_bf_rows(Prod& pr, const uint16_t* m, int in, int row0, int row1) {
+__device__ __forceinline__ void issue_bf_rows(Prod& pr, const uint16_t* m, int in, int row0, int row1) {
   const int per = bf_rows_per_stage(in);
-  for (int r = row0; r < row1; r += per) {
-    const int nr = min(per, row1 - r);
-    issue_bytes(pr, m + (size_t)r * in, (uint32_t)nr * in * 2);
-  }
+  for (int r = row0; r < row1; r += per) issue_bytes(pr, m + (size_t)r * in, (uint32_t)min(per, row1 - r) * in * 2);
 }
 
-__device__ void issue_unit(Prod& pr, const LayerDesc& Ld, const Unit& u, int l) {
+__device__ __forceinline__ void issue_unit(Prod& pr, const LayerDesc& Ld, const Unit& u, int l) {
   const EngineParams& P = pr.P;
   Ctl& C = pr.C;
   const int d = P.d;
-  const int slot4 = l & 3;
   switch (u.type) {
     case U_EXPERT: {
       const bool shared = u.k >= P.K;
-      if (shared ? !Ld.has_shared : !((C.r_valid[slot4] >> u.k) & 1u)) return;
-      const int idx = shared ? 0 : C.r_idx[slot4][u.k];
+      if (!shared) need_route(pr, l);
+      if (!pr.ok) return;
+      if (shared ? !Ld.has_shared : !((C.rt_valid[l] >> u.k) & 1u)) return;
+      const int idx = shared ? 0 : C.rt_idx[l][u.k];
       const uint32_t* guq = (shared ? Ld.sgu_q : Ld.gu_q) + (size_t)idx * (2 * P.F) * (d / 8);
       const uint16_t* gus = (shared ? Ld.sgu_s : Ld.gu_s) + (size_t)idx * (2 * P.F) * (d / 64);
       const uint16_t* gub = (shared ? Ld.sgu_b : Ld.gu_b) + (size_t)idx * (2 * P.F) * (d / 64);
       const int per = q4_rows_per_stage(d);
-      for (int r = 64 * u.r0; r < 64 * u.r0 + 64; r += per) issue_q4_rows(pr, guq, gus, gub, d, r, min(per, 64 * u.r0 + 64 - r));
+      for (int r = 64 * u.r0; r < 64 * u.r0 + 64; r += per)
+        issue_q4_rows(pr, guq, gus, gub, d, r, min(per, 64 * u.r0 + 64 - r));
       const uint32_t* dq = (shared ? Ld.sdn_q : Ld.dn_q) + (size_t)idx * (P.F / 32) * d * 4 + (size_t)u.r0 * d * 4;
       const uint16_t* ds = (shared ? Ld.sdn_s : Ld.dn_s) + (size_t)idx * (P.F / 64) * d + (size_t)(u.r0 >> 1) * d;
       const uint16_t* db = (shared ? Ld.sdn_b : Ld.dn_b) + (size_t)idx * (P.F / 64) * d + (size_t)(u.r0 >> 1) * d;
       const int pd = dn_rows_per_stage(d);
       for (int i0 = 0; i0 < d; i0 += pd) {
         const int nr = min(pd, d - i0);
-        if (pr.lane == 0 && pr.ok) {
-          uint32_t slot;
-          uint8_t* st = pr.begin(slot);
-          if (!st) {
-            pr.ok = false;
-          } else {
-            mbar_arrive_expect_tx(&C.full[slot], (uint32_t)nr * 20);
-            tma_bulk_g2s(st, dq + (size_t)i0 * 4, nr * 16, &C.full[slot]);
-            tma_bulk_g2s(st + nr * 16, ds + i0, nr * 2, &C.full[slot]);
-            tma_bulk_g2s(st + nr * 18, db + i0, nr * 2, &C.full[slot]);
-            pr.commit();
-          }
+        if (!pr.ok) return;
+        uint32_t slot;
+        uint8_t* st = prod_begin(pr, slot);
+        if (!st) return;
+        if (pr.lane == 0) {
+          mbar_arrive_expect_tx(&C.full[slot], (uint32_t)nr * 20);
+          tma_bulk_g2s(st, dq + (size_t)i0 * 4, nr * 16, &C.full[slot]);
+          tma_bulk_g2s(st + nr * 16, ds + i0, nr * 2, &C.full[slot]);
+          tma_bulk_g2s(st + nr * 18, db + i0, nr * 2, &C.full[slot]);
         }
+        ++pr.n;
       }
       break;
     }
@@ -330,33 +571,33 @@ __device__ void issue_unit(Prod& pr, const LayerDesc& Ld, const Unit& u, int l) 
     }
     case U_HEAD: {
       issue_bf_rows(pr, Ld.w1h, d, u.r0, u.r1);
+      need_route(pr, l);
+      if (!pr.ok) return;
       const int nr = u.r1 - u.r0;
       const uint32_t slotb = (uint32_t)nr * 2;
-      if (pr.lane == 0 && pr.ok) {
-        uint32_t slot;
-        uint8_t* st = pr.begin(slot);
-        if (!st) {
-          pr.ok = false;
-        } else {
-          uint32_t bytes = 0;
-          if (Ld.b1) bytes += slotb;
-          for (int k = 0; k < P.K; ++k) {
-            if ((C.r_valid[slot4] >> k) & 1u) bytes += slotb;
-            if ((C.r_prev_valid[slot4] >> k) & 1u) bytes += slotb;
-          }
-          mbar_arrive_expect_tx(&C.full[slot], bytes);
-          if (Ld.b1) tma_bulk_g2s(st, Ld.b1 + u.r0, slotb, &C.full[slot]);
-          for (int k = 0; k < P.K; ++k) {
-            if ((C.r_valid[slot4] >> k) & 1u)
-              tma_bulk_g2s(st + (1 + k) * slotb, Ld.w1c_t + (size_t)C.r_ids[slot4][k] * Ld.H + u.r0, slotb,
-                           &C.full[slot]);
-            if ((C.r_prev_valid[slot4] >> k) & 1u)
-              tma_bulk_g2s(st + (1 + P.K + k) * slotb, Ld.w1p_t + (size_t)C.r_prev[slot4][k] * Ld.H + u.r0, slotb,
-                           &C.full[slot]);
-          }
-          pr.commit();
+      uint32_t slot;
+      uint8_t* st = prod_begin(pr, slot);
+      if (!st) return;
+      if (pr.lane == 0) {
+        const uint32_t cv = C.rt_valid[l], pv = C.rt_pvalid[l];
+        uint32_t bytes = 0;
+        if (Ld.b1) bytes += slotb;
+        for (int k = 0; k < P.K; ++k) {
+          if ((cv >> k) & 1u) bytes += slotb;
+          if ((pv >> k) & 1u) bytes += slotb;
+        }
+        mbar_arrive_expect_tx(&C.full[slot], bytes);
+        if (Ld.b1) tma_bulk_g2s(st, Ld.b1 + u.r0, slotb, &C.full[slot]);
+        for (int k = 0; k < P.K; ++k) {
+          if ((cv >> k) & 1u)
+            tma_bulk_g2s(st + (1 + k) * slotb, Ld.w1c_t + (size_t)C.rt_ids[l][k] * Ld.H + u.r0, slotb,
+                         &C.full[slot]);
+          if ((pv >> k) & 1u)
+            tma_bulk_g2s(st + (1 + P.K + k) * slotb, Ld.w1p_t + (size_t)C.rt_prev[l][k] * Ld.H + u.r0, slotb,
+                         &C.full[slot]);
         }
       }
+      ++pr.n;
       const int per = max(1, STAGE_BYTES / (2 * P.E));
       for (int i = u.r0; i < u.r1; i += per)
         issue_bytes(pr, Ld.w2t + (size_t)i * P.E, (uint32_t)min(per, u.r1 - i) * P.E * 2);
@@ -373,148 +614,19 @@ __device__ void issue_unit(Prod& pr, const LayerDesc& Ld, const Unit& u, int l) 
   }
 }
 
-// Resolve the routing of layer l and publish it in route slot l & 3.
-__device__ void resolve_route(Prod& pr, const LayerDesc& Ld, int l, bool self_route, uint32_t par, uint32_t p3) {
-  const EngineParams& P = pr.P;
-  Ctl& C = pr.C;
-  const int lane = pr.lane;
-  const int slot = l & 3;
-  const int K = P.K, E = P.E;
-  bool ok = pr.ok;
-  if (ok && lane == 0) ok = spin_until(P, C, [&] { return C.cons_done >= l - 3; }, P.timeout_ns);
-  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-  pr.ok = ok;
-  if (ok && P.mode != MODE_QLINEAR) {
-    const int32_t* given = nullptr;
-    const float* z = nullptr;
-    const int32_t* prev = nullptr;
-    bool z_remote = false;
-    if (P.mode == MODE_LAYER) {
-      given = P.ids_in; z = P.logits_in; prev = P.ids_prev_in;
-    } else if (P.mode == MODE_HEAD) {
-      given = P.ids_in; prev = P.ids_prev_in;
-    } else {  // stack
-      if (self_route) {
-        bool w = true;
-        if (lane == 0)
-          w = spin_until(P, C, [&] { return ld_acquire_u32(ctr(P, par, l, 1)) >= (uint32_t)P.ncta; }, P.timeout_ns);
-        w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
-        pr.ok = w;
-        z = zr_ptr(P, par, l);
-      } else {
-        z = zhat_ptr(P, p3, l - 1);
-      }
-      z_remote = true;
-      if (P.step > 0) prev = idsu_ptr(P, par ^ 1u, l);
-    }
-    if (pr.ok) {
-      if (z) {
-        for (int e = lane; e < E; e += 32) C.zbuf[e] = z_remote ? ld_cg_f32(z + e) : z[e];
-        __syncwarp();
-      }
-      uint32_t valid = 0;
-      if (given) {
-        int id = -1;
-        if (lane < K) {
-          id = given[lane];
-          C.r_ids[slot][lane] = id;
-        }
-        __syncwarp();
-        bool v = lane < K && id >= 0 && id < E;
-        if (lane < K)
-          for (int j = 0; j < lane; ++j)
-            if (C.r_ids[slot][j] == id) v = false;
-        if (lane < K && !v) raise_error(P, C, E0_DEV_BAD_ID);
-        valid = __ballot_sync(0xffffffffu, v);
-      } else if (z) {
-        warp_topk(C.zbuf, E, K, lane, C.r_ids[slot], C.r_w[slot]);  // r_w holds the logits for now
-        valid = (K >= 32) ? 0xffffffffu : ((1u << K) - 1u);
-      } else {
-        valid = 0u;  // no current routing (head without one-hot input)
-      }
-      __syncwarp();
-      // stored index through the slot table
-      bool vk = lane < K && ((valid >> lane) & 1u);
-      if (lane < K) {
-        int idx = C.r_ids[slot][lane];
-        if (vk && Ld.slot_of) {
-          idx = Ld.slot_of[idx];
-          if (idx < 0) { vk = false; raise_error(P, C, E0_DEV_NOT_RESIDENT); }
-        }
-        if (vk && Ld.gu_q && idx >= Ld.n_routed) { vk = false; raise_error(P, C, E0_DEV_BAD_ID); }
-        C.r_idx[slot][lane] = vk ? idx : 0;
-      }
-      valid = __ballot_sync(0xffffffffu, vk);
-      // combine weights: softmax over the selected logits
-      if (z && lane == 0) {
-        float mx = -INFINITY;
-        for (int k = 0; k < K; ++k)
-          if ((valid >> k) & 1u) mx = fmaxf(mx, C.zbuf[C.r_ids[slot][k]]);
-        float s = 0.f;
-        for (int k = 0; k < K; ++k)
-          if ((valid >> k) & 1u) s += expf(C.zbuf[C.r_ids[slot][k]] - mx);
-        for (int k = 0; k < K; ++k)
-          C.r_w[slot][k] = ((valid >> k) & 1u) ? expf(C.zbuf[C.r_ids[slot][k]] - mx) / s : 0.f;
-      } else if (!z && lane < K) {
-        C.r_w[slot][lane] = 0.f;
-      }
-      // previous-token ids (one-hot of the previous step)
-      uint32_t pvalid = 0;
-      if (prev) {
-        int pid = -1;
-        if (lane < K) {
-          pid = P.mode == MODE_STACK ? ld_cg_s32(prev + lane) : prev[lane];
-          C.r_prev[slot][lane] = pid;
-        }
-        __syncwarp();
-        bool v = lane < K && pid >= 0 && pid < E;
-        if (lane < K)
-          for (int j = 0; j < lane; ++j)
-            if (C.r_prev[slot][j] == pid) v = false;
-        if (lane < K && pid != -1 && !v && P.mode != MODE_STACK) raise_error(P, C, E0_DEV_BAD_ID);
-        pvalid = __ballot_sync(0xffffffffu, v);
-      }
-      if (lane == 0) {
-        C.r_valid[slot] = valid;
-        C.r_prev_valid[slot] = pvalid;
-      }
-      __syncwarp();
-      if (P.mode == MODE_STACK && blockIdx.x == 0 && lane < K) {
-        const int id = ((valid >> lane) & 1u) ? C.r_ids[slot][lane] : -1;
-        idsu_ptr(P, par, l)[lane] = id;
-        wu_ptr(P, par, l)[lane] = C.r_w[slot][lane];
-        if (P.ids_trace) P.ids_trace[l * K + lane] = id;
-        if (P.w_trace) P.w_trace[l * K + lane] = C.r_w[slot][lane];
-      }
-    }
-  }
-  __syncwarp();
-  if (lane == 0) {
-    __threadfence_block();
-    C.route_seq = l + 1;
-  }
-  __syncwarp();
-}
-
 __device__ void producer(const EngineParams& P, Ctl& C, uint8_t* ring) {
-  Prod pr{P, C, ring, 0u, true, (int)(threadIdx.x & 31)};
-  const uint32_t par = C.epoch & 1u, p3 = C.epoch % 3u;
-  for (int l = 0; l < P.L; ++l) {
+  Prod pr{P, C, ring, 0u, true, (int)(threadIdx.x & 31), C.epoch & 1u, C.epoch % 3u, C.epoch};
+  for (int l = 0; l < P.L && pr.ok; ++l) {
     const LayerDesc& Ld = layer_at(P, l);
-    const bool self_route = P.mode == MODE_STACK && ((P.router_mask >> l) & 1ull);
-    if (self_route) {
+    if (self_routes(P, l)) {
       int nu;
       const Unit* us = units_of(P, KIND_ROUTER, blockIdx.x, nu);
       for (int i = 0; i < nu; ++i) issue_bf_rows(pr, Ld.router, P.d, us[i].r0, us[i].r1);
     }
-    pr.ok = __shfl_sync(0xffffffffu, pr.ok ? 1 : 0, 0) != 0;
-    resolve_route(pr, Ld, l, self_route, par, p3);
-    if (pr.lane == 0) stamp(P, l, 4);
     int nu;
     const Unit* us = units_of(P, P.plan ? Ld.plan_kind : 0, blockIdx.x, nu);
     for (int i = 0; i < nu; ++i) issue_unit(pr, Ld, us[i], l);
     if (pr.lane == 0) stamp(P, l, 5);
-    pr.ok = __shfl_sync(0xffffffffu, pr.ok ? 1 : 0, 0) != 0;
   }
   // Wait for every issued copy to land before the CTA may exit.
   if (pr.lane == 0) {
@@ -533,33 +645,112 @@ __device__ void producer(const EngineParams& P, Ctl& C, uint8_t* ring) {
   }
 }
 
+// Routing warp: publishes every layer's route in the route table (routes known at
+// launch, then the layers that route with their own gate as their gate logits
+// complete) and, in the stack, the bookkeeping for the next token.
+__device__ void router_warp(const EngineParams& P, Ctl& C) {
+  Prod pr{P, C, nullptr, 0u, true, (int)(threadIdx.x & 31), C.epoch & 1u, C.epoch % 3u, C.epoch};
+  load_routes(pr);
+  if (P.mode == MODE_STACK)
+    for (int l = 0; l < P.L && pr.ok; ++l) {
+      if (self_routes(P, l))
+        compute_self_route(pr, l);
+      else
+        publish_staged_route(pr, l);
+    }
+  // Stack bookkeeping, one CTA per layer: record the ids each layer used (the heads'
+  // previous-token one-hot at the next step) and commit the next token's routing of
+  // every prerouted layer: the top-K of the logits the previous layer's head produced.
+  if (P.mode == MODE_STACK) {
+    const uint32_t pnext3 = (pr.epoch + 1) % 3u;
+    for (int l = blockIdx.x; l < P.L && pr.ok; l += P.ncta) {
+      compute_self_route(pr, l);
+      if (!pr.ok) break;
+      if (pr.lane < P.K) {
+        const bool v = (C.rt_valid[l] >> pr.lane) & 1u;
+        const int id = v ? C.rt_ids[l][pr.lane] : -1;
+        idsu_ptr(P, pr.par, l)[pr.lane] = id;
+        wu_ptr(P, pr.par, l)[pr.lane] = C.rt_w[l][pr.lane];
+        if (P.ids_trace) P.ids_trace[l * P.K + pr.lane] = id;
+        if (P.w_trace) P.w_trace[l * P.K + pr.lane] = C.rt_w[l][pr.lane];
+      }
+      if (layer_at(P, l).prerouted && l > 0) {
+        if (!prod_wait_counter(pr, l - 1, 0)) {
+          pr.ok = false;
+          break;
+        }
+        const float* z = zhat_ptr(P, pnext3, l - 1);
+#pragma unroll 8
+        for (int e = pr.lane; e < P.E; e += 32) C.zbuf[e] = __ldcg(z + e);
+        __syncwarp();
+        int id;
+        float w;
+        topk_lane(pr, id, w);
+        float tot = w;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        if (pr.lane < P.K) {
+          rg_ids_ptr(P, pr.par ^ 1u, l)[pr.lane] = id;
+          rg_w_ptr(P, pr.par ^ 1u, l)[pr.lane] = w / tot;
+        }
+        __syncwarp();
+        if (pr.lane == 0) *rg_tag_ptr(P, pr.par ^ 1u, l) = pr.epoch + 1u;
+      }
+    }
+  }
+  // After an abort, mark every route published so that no consumer waits on one.
+  if (pr.lane == 0 && !pr.ok)
+    for (int l = 0; l < P.L; ++l) C.rt_ready[l] = 1;
+  if (pr.lane == 0 && !pr.ok)
+    for (int l = 0; l < P.L; ++l) C.rt_ready[l] = 1;
+}
+
 // ------------------------------------------------------------------ consumers
+constexpr int GMAX = 4;  // stages a consumer holds at once (the ring has NSTAGES)
+
 struct Cons {
   const EngineParams& P;
   Ctl& C;
   uint8_t* ring;
   uint32_t n;  // stages consumed
   int cw, lane, tid;
+  uint64_t t_acq = 0;   // diagnostics (warp 0, lane 0): time waiting for stages
+  uint64_t n_acq = 0;   // stages acquired in the current layer
 
-  // wait for the next stage; returns its base or nullptr (abort)
-  __device__ const uint8_t* acquire(uint32_t& slot) {
-    slot = n % NSTAGES;
-    const uint32_t par = (n / NSTAGES) & 1u;
-    uint64_t* bar = &C.full[slot];
-    bool ok = spin_until(P, C, [&] { return mbar_try_wait(bar, par); }, P.timeout_ns);
-    return ok ? ring + (size_t)slot * STAGE_BYTES : nullptr;
+  __device__ __forceinline__ const uint8_t* stage(int i) const {
+    return ring + (size_t)((n + i) % NSTAGES) * STAGE_BYTES;
   }
-  __device__ void release(uint32_t slot) {
+  // Wait until the next cnt stages (cnt <= GMAX) have landed.  False on abort.
+  __device__ __forceinline__ bool acquire(int cnt) {
+    const bool timed = P.trace && tid == 0;
+    const uint64_t t0 = timed ? globaltimer() : 0;
+    bool ok = true;
+    for (int i = 0; i < cnt && ok; ++i) {
+      const uint32_t m = n + i;
+      uint64_t* bar = &C.full[m % NSTAGES];
+      const uint32_t par = (m / NSTAGES) & 1u;
+      ok = wait_mbar(P, C, bar, par);
+    }
+    if (timed) {
+      t_acq += globaltimer() - t0;
+      n_acq += cnt;
+    }
+    return ok;
+  }
+  // This warp is done reading the next cnt stages.
+  __device__ void release(int cnt) {
     __syncwarp();
-    if (lane == 0) mbar_arrive(&C.empty[slot]);
-    ++n;
+    if (lane == 0)
+      for (int i = 0; i < cnt; ++i) mbar_arrive(&C.empty[(n + i) % NSTAGES]);
+    n += cnt;
   }
 };
 
 template <int D>
 struct Q4Frag {
-  static constexpr int LPR = (D / 32) < 32 ? (D / 32) : 32;
-  static constexpr int CPL = (D / 32) / LPR;
+  static constexpr int LPR = (D / 32) < 32 ? (D / 32) : 32;   // lanes per row
+  static constexpr int RPW = 32 / LPR;                         // rows per warp pass
+  static constexpr int CPL = (D / 32) / LPR;                   // 32-element chunks per lane
   uint32_t xp[CPL][16];
   float inv[CPL], sum[CPL];
   __device__ __forceinline__ void load(const Ctl& C, int lane) {
@@ -577,49 +768,95 @@ struct Q4Frag {
   }
 };
 
-// int4 rows of one stage: GU = gate/up pairs -> abuf; else rows -> red.add(out + row)
-template <int D, bool GU>
-__device__ __forceinline__ void q4_stage(const uint8_t* st, int nr, int rho0, const Q4Frag<D>& f, int cw, int lane,
-                                         float* abuf, float* out) {
-  constexpr int LPR = Q4Frag<D>::LPR, RPW = 32 / LPR, CPL = Q4Frag<D>::CPL;
-  constexpr int IR = RPW > 2 ? RPW : 2;
-  constexpr int NP = IR / RPW;
+// Lane partial of row `lr` of an int4 stage holding `nr` rows (row layout, in = D).
+template <int D>
+__device__ __forceinline__ float q4_partial(const uint8_t* st, int nr, int lr, int lane, const Q4Frag<D>& f) {
+  constexpr int LPR = Q4Frag<D>::LPR, CPL = Q4Frag<D>::CPL;
   const uint4* q = reinterpret_cast<const uint4*>(st);
   const uint16_t* s = reinterpret_cast<const uint16_t*>(st + (size_t)nr * D / 2);
   const uint16_t* b = s + nr * (D / 64);
-  for (int it = 0; it < nr / IR; ++it) {
-    if (((rho0 / IR) + it) % NCW != cw) continue;
-    float vals[NP];
+  float v = 0.f;
 #pragma unroll
-    for (int p = 0; p < NP; ++p) {
-      const int r = it * IR + p * RPW + lane / LPR;
-      float v = 0.f;
+  for (int j = 0; j < CPL; ++j) {
+    const int c = lane % LPR + LPR * j;
+    const int a = dot32(q[lr * (D / 32) + c], f.xp[j]);
+    const float sf = bf(s[lr * (D / 64) + (c >> 1)]);
+    const float bb = bf(b[lr * (D / 64) + (c >> 1)]);
+    v += sf * ((float)a * f.inv[j]) + bb * f.sum[j];
+  }
+  return v;
+}
+
+template <int LPR>
+__device__ __forceinline__ float reduce_lpr(float v) {
 #pragma unroll
-      for (int j = 0; j < CPL; ++j) {
-        const int c = lane % LPR + LPR * j;
-        const uint4 qq = q[r * (D / 32) + c];
-        const int a = dot32(qq, f.xp[j]);
-        const float sf = bf(s[r * (D / 64) + (c >> 1)]);
-        const float bb = bf(b[r * (D / 64) + (c >> 1)]);
-        v += sf * ((float)a * f.inv[j]) + bb * f.sum[j];
+  for (int o = LPR / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// A group of int4 stages holding rows [g0, g0 + R) of a part cut into stages of `per`
+// rows (part_rows rows in total).  Items of IR rows go to warps round robin, two items
+// per pass for instruction-level parallelism.  GU: rows 2j/2j+1 are gate/up of pair j
+// -> abuf[j] = silu(g) * u.  Otherwise each row value is added to out[row0 + row].
+template <int D, bool GU>
+__device__ __forceinline__ void q4_group(const Cons& cs, int g0, int R, int per, int part_rows,
+                                         const Q4Frag<D>& f, float* abuf, float* out, int row0) {
+  constexpr int LPR = Q4Frag<D>::LPR, RPW = Q4Frag<D>::RPW;
+  constexpr int IR = RPW > 2 ? RPW : 2;
+  constexpr int NP = IR / RPW;
+  const int lane = cs.lane;
+  const int items = R / IR;
+  for (int it = cs.cw; it < items; it += 2 * NCW) {
+    const bool two = it + NCW < items;
+    float v[2][NP];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+#pragma unroll
+      for (int p = 0; p < NP; ++p) {
+        v[u][p] = 0.f;
+        if (u == 0 || two) {
+          const int rho = g0 + (it + u * NCW) * IR + p * RPW + lane / LPR;  // row within the part
+          const int si = rho / per - g0 / per;
+          const int nr = min(per, part_rows - (rho / per) * per);
+          v[u][p] = q4_partial<D>(cs.stage(si), nr, rho % per, lane, f);
+        }
       }
-#pragma unroll
-      for (int o = LPR / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      vals[p] = v;
     }
-    if (GU) {
-      if (RPW == 1) {
-        if (lane == 0) abuf[(rho0 + it * IR) / 2] = silu_f(vals[0]) * vals[NP - 1];
-      } else {
-        const float up = __shfl_down_sync(0xffffffffu, vals[0], LPR);
-        if (lane % (2 * LPR) == 0) abuf[(rho0 + it * IR + lane / LPR) / 2] = silu_f(vals[0]) * up;
-      }
-    } else {
-      if (lane % LPR == 0) {
 #pragma unroll
-        for (int p = 0; p < NP; ++p) red_add_f32(out + rho0 + it * IR + p * RPW + lane / LPR, vals[p]);
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int p = 0; p < NP; ++p) v[u][p] = reduce_lpr<LPR>(v[u][p]);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (u == 1 && !two) break;
+      const int rbase = g0 + (it + u * NCW) * IR;
+      if (GU) {
+        if (RPW == 1) {
+          if (lane == 0) abuf[rbase / 2] = silu_f(v[u][0]) * v[u][NP - 1];
+        } else {
+          const float up = __shfl_down_sync(0xffffffffu, v[u][0], LPR);
+          if (lane % (2 * LPR) == 0) abuf[(rbase + lane / LPR) / 2] = silu_f(v[u][0]) * up;
+        }
+      } else if (lane % LPR == 0) {
+#pragma unroll
+        for (int p = 0; p < NP; ++p) red_add_f32(out + row0 + rbase + p * RPW + lane / LPR, v[u][p]);
       }
     }
+  }
+}
+
+// Consume the int4 rows [0, rows) of a part in groups of at most GMAX stages.
+template <int D, bool GU>
+__device__ __forceinline__ void consume_q4_part(Cons& cs, int rows, float* abuf, float* out, int row0) {
+  Q4Frag<D> f;
+  f.load(cs.C, cs.lane);
+  const int per = q4_rows_per_stage(D);
+  const int nst = (rows + per - 1) / per;
+  for (int s0 = 0; s0 < nst; s0 += GMAX) {
+    const int cnt = min(GMAX, nst - s0);
+    const int g0 = s0 * per, R = min(rows, (s0 + cnt) * per) - g0;
+    if (cs.acquire(cnt)) q4_group<D, GU>(cs, g0, R, per, rows, f, abuf, out, row0);
+    cs.release(cnt);
   }
 }
 
@@ -638,120 +875,147 @@ struct BfFrag {
   }
 };
 
-// bf16 rows (in = D) of one stage, one warp per row; out(row_in_part, value) on lane 0.
-template <int D, class Out>
-__device__ __forceinline__ void bf_stage(const uint8_t* st, int nr, int rho0, const BfFrag<D>& f, int cw, int lane,
-                                         Out out) {
-  const uint4* w = reinterpret_cast<const uint4*>(st);
-  for (int r = 0; r < nr; ++r) {
-    if ((rho0 + r) % NCW != cw) continue;
-    float v0 = 0.f, v1 = 0.f;
+template <int D>
+__device__ __forceinline__ float bf_partial(const uint8_t* row, int lane, const BfFrag<D>& f) {
+  const uint4* w = reinterpret_cast<const uint4*>(row);
+  float v0 = 0.f, v1 = 0.f;
 #pragma unroll
-    for (int j = 0; j < BfFrag<D>::CPL; ++j) {
-      const uint4 u = w[r * (D / 8) + lane + 32 * j];
-      v0 = fmaf(bflo(u.x), f.x[j][0], v0); v1 = fmaf(bfhi(u.x), f.x[j][1], v1);
-      v0 = fmaf(bflo(u.y), f.x[j][2], v0); v1 = fmaf(bfhi(u.y), f.x[j][3], v1);
-      v0 = fmaf(bflo(u.z), f.x[j][4], v0); v1 = fmaf(bfhi(u.z), f.x[j][5], v1);
-      v0 = fmaf(bflo(u.w), f.x[j][6], v0); v1 = fmaf(bfhi(u.w), f.x[j][7], v1);
-    }
-    const float v = warp_sum(v0 + v1);
-    if (lane == 0) out(rho0 + r, v);
+  for (int j = 0; j < BfFrag<D>::CPL; ++j) {
+    const uint4 u = w[lane + 32 * j];
+    v0 = fmaf(bflo(u.x), f.x[j][0], v0); v1 = fmaf(bfhi(u.x), f.x[j][1], v1);
+    v0 = fmaf(bflo(u.y), f.x[j][2], v0); v1 = fmaf(bfhi(u.y), f.x[j][3], v1);
+    v0 = fmaf(bflo(u.z), f.x[j][4], v0); v1 = fmaf(bfhi(u.z), f.x[j][5], v1);
+    v0 = fmaf(bflo(u.w), f.x[j][6], v0); v1 = fmaf(bfhi(u.w), f.x[j][7], v1);
   }
+  return v0 + v1;
 }
 
-template <int D, class Out>
-__device__ void consume_bf_rows(Cons& cs, int rows, Out out) {
+// Where consume_bf_rows puts a row value: a shared buffer (dst[row] = v), the head
+// logits accumulator (dst[row] += v + bias[row]), or a layer's gate logits (dst[row] = v).
+enum BfOut : int { BF_SMEM = 0, BF_ADD_BIAS = 1, BF_STORE = 2 };
+
+// bf16 rows [0, rows) of a part (in = D), stages of bf_rows_per_stage(D) rows, in
+// groups of at most GMAX stages; one warp per row, two rows per pass.
+template <int D>
+__device__ __forceinline__ void consume_bf_rows(Cons& cs, int rows, int mode, float* dst, const float* bias) {
   BfFrag<D> f;
   f.load(cs.C, cs.lane);
   const int per = bf_rows_per_stage(D);
-  for (int r = 0; r < rows; r += per) {
-    uint32_t slot;
-    const uint8_t* st = cs.acquire(slot);
-    if (st) bf_stage<D>(st, min(per, rows - r), r, f, cs.cw, cs.lane, out);
-    cs.release(slot);
+  const int nst = (rows + per - 1) / per;
+  for (int s0 = 0; s0 < nst; s0 += GMAX) {
+    const int cnt = min(GMAX, nst - s0);
+    const int g0 = s0 * per, R = min(rows, (s0 + cnt) * per) - g0;
+    if (cs.acquire(cnt)) {
+      for (int r = cs.cw; r < R; r += 2 * NCW) {
+        const bool two = r + NCW < R;
+        const int ra = g0 + r, rb = g0 + r + NCW;
+        float va = bf_partial<D>(cs.stage(ra / per - s0) + (size_t)(ra % per) * 2 * D, cs.lane, f);
+        float vb = two ? bf_partial<D>(cs.stage(rb / per - s0) + (size_t)(rb % per) * 2 * D, cs.lane, f) : 0.f;
+        va = warp_sum(va);
+        vb = warp_sum(vb);
+        if (cs.lane == 0) {
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            if (u == 1 && !two) break;
+            const int row = u ? rb : ra;
+            const float v = u ? vb : va;
+            if (mode == BF_ADD_BIAS)
+              red_add_f32(dst + row, v + (bias ? bias[row] : 0.f));
+            else
+              dst[row] = v;
+          }
+        }
+      }
+    }
+    cs.release(cnt);
   }
 }
 
 template <int D>
-__device__ void consume_unit(Cons& cs, const LayerDesc& Ld, const Unit& u, int l, float* acc, float* zhat,
+__device__ __forceinline__ void consume_unit(Cons& cs, const LayerDesc& Ld, const Unit& u, int l, float* acc, float* zhat,
                              float* zr) {
   const EngineParams& P = cs.P;
   Ctl& C = cs.C;
-  const int slot4 = l & 3;
-  const int cw = cs.cw, lane = cs.lane, tid = cs.tid;
+  const int tid = cs.tid;
   switch (u.type) {
     case U_EXPERT: {
       const bool shared = u.k >= P.K;
-      cbar();  // abuf reuse
-      if (!shared) spin_until(P, C, [&] { return C.route_seq > l; }, P.timeout_ns);
+      if (!shared) wait_flag(P, C, &C.rt_ready[l]);
+      cbar();  // abuf / aq reuse
       // The named barriers below are executed unconditionally so that every warp
       // reaches the same barriers even if the route table were read inconsistently.
-      const bool valid = shared ? Ld.has_shared != 0 : ((C.r_valid[slot4] >> u.k) & 1u) != 0;
-      if (valid) {
-        Q4Frag<D> f;
-        f.load(C, lane);
-        const int per = q4_rows_per_stage(D);
-        for (int r = 0; r < 64; r += per) {
-          uint32_t slot;
-          const uint8_t* st = cs.acquire(slot);
-          if (st) q4_stage<D, true>(st, min(per, 64 - r), r, f, cw, lane, C.abuf, nullptr);
-          cs.release(slot);
+      const bool valid = shared ? Ld.has_shared != 0 : ((C.rt_valid[l] >> u.k) & 1u) != 0;
+      if (valid) consume_q4_part<D, true>(cs, 64, C.abuf, nullptr, 0);
+      cbar();  // all 32 activations ready
+      if (cs.cw == 0) {
+        // quantise the 32 activations once for all warps (lane j holds a_j)
+        const float a = C.abuf[cs.lane];
+        float m = fabsf(a), s = a;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+          s += __shfl_xor_sync(0xffffffffu, s, o);
+        }
+        const float r = m > 0.f ? 32767.0f / m : 0.f;
+        int q = __float2int_rn(a * r);
+        q = q > 32767 ? 32767 : (q < -32767 ? -32767 : q);
+        const int j = cs.lane, idx = j & 7;
+        reinterpret_cast<int16_t*>(C.aq)[8 * (j >> 3) + ((idx & 1) ? 4 + (idx >> 1) : (idx >> 1))] = (int16_t)q;
+        if (cs.lane == 0) {
+          C.ascale[0] = m > 0.f ? m / 32767.0f : 0.f;
+          C.ascale[1] = s;
         }
       }
-      cbar();  // all 32 activations ready
+      cbar();
       if (valid) {
-        float av[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) av[i] = C.abuf[i];
         uint32_t ap[16];
-        float asum;
-        const float ainv = quant_chunk32(av, ap, &asum);
-        const float wk = shared ? 1.0f : C.r_w[slot4][u.k];
-        const int pd = dn_rows_per_stage(P.d);
-        for (int i0 = 0; i0 < P.d; i0 += pd) {
-          const int nr = min(pd, P.d - i0);
-          uint32_t slot;
-          const uint8_t* st = cs.acquire(slot);
-          if (st) {
-            const uint4* q = reinterpret_cast<const uint4*>(st);
-            const uint16_t* s = reinterpret_cast<const uint16_t*>(st + nr * 16);
-            const uint16_t* b = s + nr;
-            for (int r = cw * 32 + lane; r < nr; r += NCT) {
-              const int a = dot32(q[r], ap);
-              const float v = bf(s[r]) * ((float)a * ainv) + bf(b[r]) * asum;
-              red_add_f32(acc + i0 + r, wk * v);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const uint4 v = C.aq[t];
+          ap[4 * t] = v.x; ap[4 * t + 1] = v.y; ap[4 * t + 2] = v.z; ap[4 * t + 3] = v.w;
+        }
+        const float ainv = C.ascale[0], asum = C.ascale[1];
+        const float wk = shared ? 1.0f : C.rt_w[l][u.k];
+        const int pd = dn_rows_per_stage(D);
+        constexpr int NDS = (D + 1023) / 1024;   // down-projection stages (<= 2)
+        constexpr int RPT = (D + NCT - 1) / NCT;  // rows per thread (<= 4)
+        if (cs.acquire(NDS)) {
+          float v[RPT];
+#pragma unroll
+          for (int m = 0; m < RPT; ++m) {
+            const int rho = tid + NCT * m;
+            v[m] = 0.f;
+            if (rho < D) {
+              const int si = rho / pd, lr = rho % pd, nr = min(pd, D - si * pd);
+              const uint8_t* st = cs.stage(si);
+              const uint4 qq = reinterpret_cast<const uint4*>(st)[lr];
+              const uint16_t* sc = reinterpret_cast<const uint16_t*>(st + nr * 16);
+              const int a = dot32(qq, ap);
+              v[m] = bf(sc[lr]) * ((float)a * ainv) + bf(sc[nr + lr]) * asum;
             }
           }
-          cs.release(slot);
+#pragma unroll
+          for (int m = 0; m < RPT; ++m)
+            if (tid + NCT * m < D) red_add_f32(acc + tid + NCT * m, wk * v[m]);
         }
+        cs.release(NDS);
       }
       break;
     }
-    case U_QROWS: {
-      Q4Frag<D> f;
-      f.load(C, lane);
-      const int per = q4_rows_per_stage(D);
-      for (int r = u.r0; r < u.r1; r += per) {
-        uint32_t slot;
-        const uint8_t* st = cs.acquire(slot);
-        if (st) q4_stage<D, false>(st, min(per, u.r1 - r), r, f, cw, lane, nullptr, acc);
-        cs.release(slot);
-      }
+    case U_QROWS:
+      consume_q4_part<D, false>(cs, u.r1 - u.r0, nullptr, acc, u.r0);
       break;
-    }
     case U_LORA_AB: {
       cbar();  // vbuf reuse
       float* vb = C.vbuf;
-      consume_bf_rows<D>(cs, u.r1 - u.r0, [&](int r, float v) { vb[r] = v; });
+      consume_bf_rows<D>(cs, u.r1 - u.r0, BF_SMEM, vb, nullptr);
       cbar();
       const int out = Ld.lout;
       const int per = max(1, STAGE_BYTES / (2 * out));
       for (int q0 = 0; q0 < u.r1 - u.r0; q0 += per) {
         const int nr = min(per, u.r1 - u.r0 - q0);
-        uint32_t slot;
-        const uint8_t* st = cs.acquire(slot);
-        if (st) {
-          const uint32_t* w = reinterpret_cast<const uint32_t*>(st);
+        if (cs.acquire(1)) {
+          const uint32_t* w = reinterpret_cast<const uint32_t*>(cs.stage(0));
           for (int i2 = tid; i2 < out / 2; i2 += NCT) {
             float s0 = 0.f, s1 = 0.f;
             for (int r = 0; r < nr; ++r) {
@@ -764,42 +1028,36 @@ __device__ void consume_unit(Cons& cs, const LayerDesc& Ld, const Unit& u, int l
             red_add_f32(acc + 2 * i2 + 1, Ld.lscale * s1);
           }
         }
-        cs.release(slot);
+        cs.release(1);
       }
       break;
     }
     case U_HEAD: {
       cbar();  // ubuf reuse
       float* ub = C.ubuf;
-      consume_bf_rows<D>(cs, u.r1 - u.r0, [&](int r, float v) { ub[r] = v; });
-      spin_until(P, C, [&] { return C.route_seq > l; }, P.timeout_ns);
+      consume_bf_rows<D>(cs, u.r1 - u.r0, BF_SMEM, ub, nullptr);
+      wait_flag(P, C, &C.rt_ready[l]);
       cbar();
       const int nr = u.r1 - u.r0;
-      {
-        uint32_t slot;
-        const uint8_t* st = cs.acquire(slot);
-        if (st && tid < nr) {
-          const uint16_t* g = reinterpret_cast<const uint16_t*>(st);
-          float v = ub[tid];
-          if (Ld.b1) v += bf(g[tid]);
-          const uint32_t cv = C.r_valid[slot4], pv = C.r_prev_valid[slot4];
-          for (int k = 0; k < P.K; ++k) {
-            if ((cv >> k) & 1u) v += bf(g[(1 + k) * nr + tid]);
-            if ((pv >> k) & 1u) v += bf(g[(1 + P.K + k) * nr + tid]);
-          }
-          ub[tid] = gelu_f(v);
+      if (cs.acquire(1) && tid < nr) {
+        const uint16_t* g = reinterpret_cast<const uint16_t*>(cs.stage(0));
+        float v = ub[tid];
+        if (Ld.b1) v += bf(g[tid]);
+        const uint32_t cv = C.rt_valid[l], pv = C.rt_pvalid[l];
+        for (int k = 0; k < P.K; ++k) {
+          if ((cv >> k) & 1u) v += bf(g[(1 + k) * nr + tid]);
+          if ((pv >> k) & 1u) v += bf(g[(1 + P.K + k) * nr + tid]);
         }
-        cs.release(slot);
+        ub[tid] = gelu_f(v);
       }
+      cs.release(1);
       cbar();
       const int E = P.E;
       const int per = max(1, STAGE_BYTES / (2 * E));
       for (int i0 = 0; i0 < nr; i0 += per) {
         const int ni = min(per, nr - i0);
-        uint32_t slot;
-        const uint8_t* st = cs.acquire(slot);
-        if (st) {
-          const uint32_t* w = reinterpret_cast<const uint32_t*>(st);
+        if (cs.acquire(1)) {
+          const uint32_t* w = reinterpret_cast<const uint32_t*>(cs.stage(0));
           for (int e2 = tid; e2 < E / 2; e2 += NCT) {
             float s0 = 0.f, s1 = 0.f;
             for (int r = 0; r < ni; ++r) {
@@ -812,21 +1070,24 @@ __device__ void consume_unit(Cons& cs, const LayerDesc& Ld, const Unit& u, int l
             red_add_f32(zhat + 2 * e2 + 1, s1);
           }
         }
-        cs.release(slot);
+        cs.release(1);
       }
       break;
     }
     case U_LRES: {
       const uint16_t* b2 = Ld.b2;
       const int e0 = u.r0;
-      consume_bf_rows<D>(cs, u.r1 - u.r0, [&](int r, float v) {
-        red_add_f32(zhat + e0 + r, v + (b2 ? bf(b2[e0 + r]) : 0.f));
-      });
+      float* bb = C.b2buf;
+      cbar();  // b2buf reuse
+      if (b2)  // stage the bias slice in shared memory (read-only input)
+        for (int e = tid; e < u.r1 - u.r0; e += NCT) bb[e] = bf(b2[e0 + e]);
+      cbar();
+      consume_bf_rows<D>(cs, u.r1 - u.r0, BF_ADD_BIAS, zhat + e0, b2 ? bb : nullptr);
       break;
     }
     case U_ROUTER: {
       const int e0 = u.r0;
-      consume_bf_rows<D>(cs, u.r1 - u.r0, [&](int r, float v) { zr[e0 + r] = v; });
+      consume_bf_rows<D>(cs, u.r1 - u.r0, BF_STORE, zr + e0, nullptr);
       break;
     }
     default:
@@ -834,28 +1095,41 @@ __device__ void consume_unit(Cons& cs, const LayerDesc& Ld, const Unit& u, int l
   }
 }
 
-// Build the layer input: residual h (fp32 of bf16 values) and normed x, plus the
-// int16 copy of x used by the int4 rows.  All consumer threads.
-__device__ void layer_input(Cons& cs, int l, uint32_t par) {
+// Build the layer input: residual h (fp32 of bf16 values), normed x, and the int16
+// copy of x used by the int4 rows.  Thread t owns elements t + NCT*k, so warp w owns
+// the whole 32-element chunks w + 16k and quantises them with shuffles.  inc[] holds
+// this thread's residual increments, loaded before the dependency wait.
+template <int D>
+__device__ __forceinline__ void layer_input(Cons& cs, int l, uint32_t par, const float* inc) {
   const EngineParams& P = cs.P;
   Ctl& C = cs.C;
-  const int d = P.d, tid = cs.tid;
+  const int tid = cs.tid;
+  constexpr int PER = (D + NCT - 1) / NCT;
+  float h[PER];
   float ss = 0.f;
-  for (int i = tid; i < d; i += NCT) {
-    float h;
-    if (P.mode == MODE_STACK) {
-      uint16_t hb;
-      if (l == 0) {
-        hb = P.h_in[i];
+  const float* accp = (P.mode == MODE_STACK && l > 0) ? acc_ptr(P, par, l - 1) : nullptr;
+  float a[PER];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int i = tid + NCT * k;
+    a[k] = (accp && i < D) ? __ldcg(accp + i) : 0.f;
+  }
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int i = tid + NCT * k;
+    h[k] = 0.f;
+    if (i < D) {
+      float v;
+      if (P.mode == MODE_STACK) {
+        const uint16_t hb = l == 0 ? P.h_in[i] : f32_to_bf16_bits(C.res[i] + a[k]);
+        v = P.incr ? bf(f32_to_bf16_bits(bf(hb) + inc[k])) : bf(hb);
       } else {
-        hb = f32_to_bf16_bits(C.res[i] + ld_cg_f32(acc_ptr(P, par, l - 1) + i));
+        v = bf(P.h_in[i]);
       }
-      h = P.incr ? bf(f32_to_bf16_bits(bf(hb) + bf(P.incr[(size_t)l * d + i]))) : bf(hb);
-    } else {
-      h = bf(P.h_in[i]);
+      h[k] = v;
+      C.res[i] = v;
+      ss += v * v;
     }
-    C.res[i] = h;
-    ss += h * h;
   }
   ss = warp_sum(ss);
   if (cs.lane == 0) C.red[cs.cw] = ss;
@@ -863,23 +1137,33 @@ __device__ void layer_input(Cons& cs, int l, uint32_t par) {
   float tot = 0.f;
 #pragma unroll
   for (int w = 0; w < NCW; ++w) tot += C.red[w];
-  const float scale = P.norm ? rsqrtf(tot / (float)d + RMS_EPS) : 1.0f;
-  for (int i = tid; i < d; i += NCT) C.x[i] = C.res[i] * scale;
-  cbar();
-  for (int c = tid; c < d / 32; c += NCT) {
-    uint32_t xp[16];
-    float s;
-    const float inv = quant_chunk32(C.x + 32 * c, xp, &s);
-    uint4* dst = C.xq + 4 * c;
-    dst[0] = make_uint4(xp[0], xp[1], xp[2], xp[3]);
-    dst[1] = make_uint4(xp[4], xp[5], xp[6], xp[7]);
-    dst[2] = make_uint4(xp[8], xp[9], xp[10], xp[11]);
-    dst[3] = make_uint4(xp[12], xp[13], xp[14], xp[15]);
-    C.xinv[c] = inv;
-    C.xsum[c] = s;
+  const float scale = P.norm ? rsqrtf(tot / (float)D + RMS_EPS) : 1.0f;
+  int16_t* xq16 = reinterpret_cast<int16_t*>(C.xq);
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int i = tid + NCT * k;
+    if (i < D) {  // warp-uniform: chunks are warp-aligned
+      const float x = h[k] * scale;
+      C.x[i] = x;
+      float m = fabsf(x), s = x;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        s += __shfl_xor_sync(0xffffffffu, s, o);
+      }
+      const float r = m > 0.f ? 32767.0f / m : 0.f;
+      int q = __float2int_rn(x * r);
+      q = q > 32767 ? 32767 : (q < -32767 ? -32767 : q);
+      const int c = i >> 5, j = cs.lane, idx = j & 7;
+      xq16[32 * c + 8 * (j >> 3) + ((idx & 1) ? 4 + (idx >> 1) : (idx >> 1))] = (int16_t)q;
+      if (cs.lane == 0) {
+        C.xinv[c] = m > 0.f ? m / 32767.0f : 0.f;
+        C.xsum[c] = s;
+      }
+      if (P.mode == MODE_STACK && P.h_trace && blockIdx.x == 0)
+        P.h_trace[(size_t)l * D + i] = f32_to_bf16_bits(h[k]);
+    }
   }
-  if (P.mode == MODE_STACK && P.h_trace && blockIdx.x == 0)
-    for (int i = tid; i < d; i += NCT) P.h_trace[(size_t)l * d + i] = f32_to_bf16_bits(C.res[i]);
   cbar();
 }
 
@@ -887,7 +1171,7 @@ template <int D>
 __device__ void consumer(const EngineParams& P, Ctl& C, uint8_t* ring) {
   Cons cs{P, C, ring, 0u, (int)(threadIdx.x >> 5), (int)(threadIdx.x & 31), (int)threadIdx.x};
   const int tid = cs.tid;
-  const uint32_t par = C.epoch & 1u, p3 = C.epoch % 3u;
+  const uint32_t par = C.epoch & 1u;
   const uint32_t pnext3 = (C.epoch + 1) % 3u, pclr3 = (C.epoch + 2) % 3u;
   const int ncta = P.ncta, cta = blockIdx.x;
 
@@ -903,13 +1187,20 @@ __device__ void consumer(const EngineParams& P, Ctl& C, uint8_t* ring) {
   for (int l = 0; l < P.L; ++l) {
     const LayerDesc& Ld = layer_at(P, l);
     if (tid == 0) stamp(P, l, 0);
+    // residual increments of this layer are inputs: load them before the dependency wait
+    float inc[(D + NCT - 1) / NCT];
+#pragma unroll
+    for (int k = 0; k < (D + NCT - 1) / NCT; ++k) {
+      const int i = tid + NCT * k;
+      inc[k] = (P.mode == MODE_STACK && P.incr && i < D) ? bf(P.incr[(size_t)l * D + i]) : 0.f;
+    }
     if (l > 0 && P.mode == MODE_STACK) {
       if (tid == 0)
-        spin_until(P, C, [&] { return ld_acquire_u32(ctr(P, par, l - 1, 0)) >= (uint32_t)ncta; }, P.timeout_ns);
+        wait_count(P, C, ctr(P, par, l - 1, 0), (uint32_t)ncta);
       cbar();
     }
     if (tid == 0) stamp(P, l, 1);
-    layer_input(cs, l, par);
+    layer_input<D>(cs, l, par, inc);
     if (tid == 0) stamp(P, l, 2);
     float* acc = acc_ptr(P, par, l);
     float* zh = zhat_ptr(P, pnext3, l);
@@ -920,15 +1211,24 @@ __device__ void consumer(const EngineParams& P, Ctl& C, uint8_t* ring) {
       const Unit* us = units_of(P, KIND_ROUTER, cta, nu);
       for (int i = 0; i < nu; ++i) consume_unit<D>(cs, Ld, us[i], l, acc, zh, zr);
       cbar();
-      if (tid == 0) {
-        __threadfence();
-        red_release_add_u32(ctr(P, par, l, 1), 1u);
-      }
+      if (tid == 0) red_release_add_u32(ctr(P, par, l, 1), 1u);
     }
     int nu;
     const Unit* us = units_of(P, P.plan ? Ld.plan_kind : 0, cta, nu);
-    for (int i = 0; i < nu; ++i) consume_unit<D>(cs, Ld, us[i], l, acc, zh, zr);
-    if (tid == 0) stamp(P, l, 3);
+    for (int i = 0; i < nu; ++i) {
+      const uint64_t tu = (P.trace && tid == 0) ? globaltimer() : 0;
+      consume_unit<D>(cs, Ld, us[i], l, acc, zh, zr);
+      if (P.trace && tid == 0) P.trace[((size_t)cta * P.L + l) * 16 + 8 + us[i].type] += globaltimer() - tu;
+    }
+    if (tid == 0) {
+      stamp(P, l, 3);
+      if (P.trace) {
+        P.trace[((size_t)cta * P.L + l) * 16 + 6] = cs.t_acq;
+        P.trace[((size_t)cta * P.L + l) * 16 + 7] = cs.n_acq;
+      }
+      cs.t_acq = 0;
+      cs.n_acq = 0;
+    }
 
     if (l == P.L - 1) {
       // Clear the other half of the parity-duplicated buffers for the next launch.
@@ -951,14 +1251,13 @@ __device__ void consumer(const EngineParams& P, Ctl& C, uint8_t* ring) {
     }
     cbar();
     if (tid == 0) {
-      __threadfence();
+      // the bar.sync above orders every consumer thread's reductions before this release
       if (l == P.L - 1) {
         const uint32_t old = atom_acq_rel_add_u32(ctr(P, par, l, 0), 1u);
         C.is_last = (old == (uint32_t)ncta - 1u);
       } else {
         red_release_add_u32(ctr(P, par, l, 0), 1u);
       }
-      C.cons_done = l + 1;
     }
   }
   cbar();
@@ -1016,23 +1315,43 @@ __device__ void consumer(const EngineParams& P, Ctl& C, uint8_t* ring) {
 
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1) engine_kernel(const __grid_constant__ EngineParams P) {
-  extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* ring = smem;
-  Ctl& C = *reinterpret_cast<Ctl*>(smem + (size_t)NSTAGES * STAGE_BYTES);
+  uint8_t* ring = e0_smem;
+  Ctl& C = *reinterpret_cast<Ctl*>(e0_smem + CTL_OFFSET);
+  {
+    // layer descriptors and this CTA's work units, copied on chip once
+    const int nl = P.layers ? P.L : 1;
+    const uint64_t* src = reinterpret_cast<const uint64_t*>(P.layers ? P.layers : &P.inline_layer);
+    uint64_t* dst = reinterpret_cast<uint64_t*>(e0_smem + LD_OFFSET);
+    const int nw = nl * (int)(sizeof(LayerDesc) / 8);
+    for (int i = threadIdx.x; i < nw; i += NTHREADS) dst[i] = src[i];
+    for (int i = threadIdx.x; i < KINDS_MAX * MAXU; i += NTHREADS) {
+      const int kind = i / MAXU, u = i % MAXU;
+      if (P.plan) {
+        if (kind < P.kinds) {
+          C.su[kind][u] = P.plan[((size_t)kind * P.ncta + blockIdx.x) * MAXU + u];
+          if (u == 0) C.sn[kind] = P.plan_n[kind * P.ncta + blockIdx.x];
+        }
+      } else if (kind == 0) {
+        C.su[0][u] = P.inline_plan[(size_t)blockIdx.x * MAXU + u];
+        if (u == 0) C.sn[0] = P.inline_n[blockIdx.x];
+      }
+    }
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGES; ++s) {
       mbar_init(&C.full[s], 1);
       mbar_init(&C.empty[s], NCW);
     }
     fence_mbar_init();
-    C.route_seq = 0;
-    C.cons_done = 0;
+    for (int l = 0; l < LMAX; ++l) C.rt_ready[l] = 0;
     C.abort_flag = 0;
     C.is_last = 0;
     C.epoch = *reinterpret_cast<volatile uint32_t*>(&hdr(P)->epoch);
   }
   __syncthreads();
-  if (threadIdx.x >= NCT)
+  if (threadIdx.x >= NCT + 32)
+    router_warp(P, C);
+  else if (threadIdx.x >= NCT)
     producer(P, C, ring);
   else
     consumer<D>(P, C, ring);

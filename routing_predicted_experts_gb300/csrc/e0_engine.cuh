@@ -29,11 +29,11 @@
 
 namespace e0eng {
 
-constexpr int NCW = 16;                       // consumer warps
-constexpr int NTHREADS = (NCW + 1) * 32;      // + one producer warp
+constexpr int NCW = 14;                       // consumer warps (16 warps in all: 4 per SM sub-partition)
+constexpr int NTHREADS = (NCW + 2) * 32;      // + producer warp + routing warp
 constexpr int NCT = NCW * 32;                 // consumer threads
 constexpr int STAGE_BYTES = 20480;
-constexpr int NSTAGES = 9;
+constexpr int NSTAGES = 8;
 constexpr int KMAX = 16;
 constexpr int EMAX = 1024;
 constexpr int DMAX = 2048;
@@ -43,6 +43,7 @@ constexpr int MAX_CTAS = 160;
 constexpr int HEAD_ROWS = 64;                 // max fc1 rows per U_HEAD unit
 constexpr int RANKS_MAX = 64;                 // max LoRA rank
 constexpr int KINDS_MAX = 3;
+constexpr int LMAX = 64;                      // layers per launch
 constexpr float RMS_EPS = 1e-6f;
 
 enum UnitType : uint8_t { U_NONE = 0, U_EXPERT, U_QROWS, U_LORA_AB, U_HEAD, U_LRES, U_ROUTER };
@@ -124,6 +125,9 @@ struct WsLayout {
   size_t zr;         // f32 [2][L][E]
   size_t ids;        // i32 [2][L][KMAX]
   size_t wts;        // f32 [2][L][KMAX]
+  size_t rg_ids;     // i32 [2][L][KMAX] routes committed for the next launch
+  size_t rg_w;       // f32 [2][L][KMAX]
+  size_t rg_tag;     // u32 [2][L]  epoch the route is for
   size_t total;
 };
 
@@ -138,6 +142,9 @@ __host__ __device__ inline WsLayout ws_layout(int E, int L) {
   w.zr = o;       o = ws_align(o + sizeof(float) * 2 * (size_t)L * E);
   w.ids = o;      o = ws_align(o + sizeof(int32_t) * 2 * (size_t)L * KMAX);
   w.wts = o;      o = ws_align(o + sizeof(float) * 2 * (size_t)L * KMAX);
+  w.rg_ids = o;   o = ws_align(o + sizeof(int32_t) * 2 * (size_t)L * KMAX);
+  w.rg_w = o;     o = ws_align(o + sizeof(float) * 2 * (size_t)L * KMAX);
+  w.rg_tag = o;   o = ws_align(o + sizeof(uint32_t) * 2 * (size_t)L);
   w.total = o;
   return w;
 }
