@@ -130,15 +130,30 @@ e0_status build_plan(const PlanSpec& s, int ncta, Unit* units, uint8_t* counts) 
       gs.push_back({U_HEAD, i, 8, W_BF16 * 8.0 * (2.0 * d + 2.0 * s.E + 2.0 * (1 + 2 * s.K))});
   if (s.router)
     for (int e = 0; e < s.E; e += 8) gs.push_back({U_ROUTER, e, 8, W_BF16 * 8.0 * 2.0 * d});
-  double total = 0.0;
-  for (double v : load) total += v;
-  for (auto& g : gs) total += g.cost;
-  const double target = total / ncta;
-  // 3. water-fill granules over CTAs with cumulative capacity (rounding spreads evenly)
+  double gtotal = 0.0;
+  for (auto& g : gs) gtotal += g.cost;
+  // 3. water-fill: the level T at which the CTAs below it take exactly the granules,
+  //    sum_c max(0, T - load[c]) = gtotal (CTAs already above T, e.g. ones with an
+  //    expert slab heavier than the mean, get nothing more)
+  double level = 0.0;
+  {
+    std::vector<double> sorted(load);
+    std::sort(sorted.begin(), sorted.end());
+    double below = 0.0;  // sum of the loads of the CTAs under the level
+    for (int c = 0; c < ncta; ++c) {
+      below += sorted[c];
+      const double t = (gtotal + below) / (c + 1);  // level if CTAs 0..c take everything
+      if (c + 1 == ncta || t <= sorted[c + 1]) {
+        level = t;
+        break;
+      }
+    }
+  }
+  // assign granules in order with cumulative capacity (rounding spreads evenly)
   double cum_cap = 0.0, cum_assigned = 0.0;
   size_t g = 0;
   for (int c = 0; c < ncta && g < gs.size(); ++c) {
-    cum_cap += std::max(0.0, target - load[c]);
+    cum_cap += std::max(0.0, level - load[c]);
     const bool last = (c == ncta - 1);
     while (g < gs.size() && (last || cum_assigned + 0.5 * gs[g].cost <= cum_cap)) {
       const Granule& gr = gs[g];

@@ -14,14 +14,13 @@ namespace e0eng {
 struct Ctl {
   uint64_t full[NSTAGES];
   uint64_t empty[NSTAGES];
-  float x[DMAX];              // layer input x (normed), fp32
-  float res[DMAX];            // residual h of the layer, fp32 (exact bf16 values)
-  uint4 xq[DMAX / 8];         // x as int16, 8-element groups stored [0,2,4,6,1,3,5,7]
-  float xinv[DMAX / 32];      // per 32-element chunk: dequant step of xq
-  float xsum[DMAX / 32];      // per 32-element chunk: sum of x
-  float abuf[32];             // SwiGLU activations of the current expert slab
-  uint4 aq[4];                // ... quantised to int16 in the dot32 order
-  float ascale[2];            // ... their dequant step and sum
+  float res[DMAX];            // residual h of the layer, fp32 (exact bf16 values); x = res * xscale
+  uint4 xq[4][DMAX / 32];     // x as int16: xq[t][c] = group t (of 4) of chunk c, stored [0,2,4,6,1,3,5,7]
+                              // (group-major, so that lanes reading consecutive chunks hit distinct banks)
+  float xinv[DMAX / 32];      // per 32-element chunk: dequant step of xq (one step for all of x)
+  float xsum[DMAX / 32];      // per 32-element chunk: sum of the dequantised chunk
+  float abuf[2][32];          // SwiGLU activations of the last two expert slabs
+  uint4 aqw[NCW][4];          // per warp: the activations quantised to int16 in the dot32 order
   float b2buf[HEAD_ROWS];     // head fc2 bias slice of the current LRES unit
   float ubuf[HEAD_ROWS];      // head fc1 pre-activation, then erf-GELU output
   float vbuf[RANKS_MAX];      // LoRA A x for the current rank slice
@@ -35,6 +34,8 @@ struct Ctl {
   uint32_t rt_pvalid[LMAX];
   volatile int32_t rt_ready[LMAX];
   float red[NCW];
+  uint32_t redm[NCW];
+  float xscale;               // RMSNorm factor of the current layer input
   int32_t f_ids[KMAX];        // finisher top-K
   float f_vals[KMAX];
   volatile int32_t abort_flag;
@@ -50,6 +51,7 @@ struct Ctl {
 constexpr size_t CTL_OFFSET = (size_t)NSTAGES * STAGE_BYTES;
 constexpr size_t LD_OFFSET = (CTL_OFFSET + sizeof(Ctl) + 15) & ~size_t(15);
 size_t smem_bytes() { return LD_OFFSET + sizeof(LayerDesc) * LMAX; }
+static_assert(LD_OFFSET + sizeof(LayerDesc) * LMAX <= 227 * 1024, "shared memory per CTA is 227 KB at most");
 
 extern __shared__ __align__(1024) uint8_t e0_smem[];
 
@@ -716,6 +718,7 @@ struct Cons {
   int cw, lane, tid;
   uint64_t t_acq = 0;   // diagnostics (warp 0, lane 0): time waiting for stages
   uint64_t n_acq = 0;   // stages acquired in the current layer
+  uint32_t nx = 0;      // expert slabs consumed (selects the activation buffer)
 
   __device__ __forceinline__ const uint8_t* stage(int i) const {
     return ring + (size_t)((n + i) % NSTAGES) * STAGE_BYTES;
@@ -727,16 +730,19 @@ struct Cons {
     bool ok = true;
     for (int i = 0; i < cnt && ok; ++i) {
       const uint32_t m = n + i;
-      uint64_t* bar = &C.full[m % NSTAGES];
-      const uint32_t par = (m / NSTAGES) & 1u;
-      ok = wait_mbar(P, C, bar, par);
+      ok = wait_mbar(P, C, &C.full[m % NSTAGES], (m / NSTAGES) & 1u);
     }
     if (timed) {
       t_acq += globaltimer() - t0;
       n_acq += cnt;
     }
-    return ok;
+    // warp-uniform, so that the shuffles that follow a successful acquire see every lane
+    return __all_sync(0xffffffffu, ok);
   }
+  // Wait until the routing warp has published layer l's route.  Every lane polls: a
+  // single polling lane followed by a warp barrier measured several times slower in
+  // the code that follows.
+  __device__ __forceinline__ void wait_route(int l) { wait_flag(P, C, &C.rt_ready[l]); }
   // This warp is done reading the next cnt stages.
   __device__ void release(int cnt) {
     __syncwarp();
@@ -759,7 +765,7 @@ struct Q4Frag {
       const int c = lane % LPR + LPR * j;
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
-        const uint4 v = C.xq[4 * c + t];
+        const uint4 v = C.xq[t][c];
         xp[j][4 * t] = v.x; xp[j][4 * t + 1] = v.y; xp[j][4 * t + 2] = v.z; xp[j][4 * t + 3] = v.w;
       }
       inv[j] = C.xinv[c];
@@ -795,26 +801,28 @@ __device__ __forceinline__ float reduce_lpr(float v) {
 }
 
 // A group of int4 stages holding rows [g0, g0 + R) of a part cut into stages of `per`
-// rows (part_rows rows in total).  Items of IR rows go to warps round robin, two items
-// per pass for instruction-level parallelism.  GU: rows 2j/2j+1 are gate/up of pair j
-// -> abuf[j] = silu(g) * u.  Otherwise each row value is added to out[row0 + row].
+// rows (part_rows rows in total).  Items of IR rows go to warps round robin, up to NI
+// items per warp and pass, so that a full group (64 rows) takes a single pass with
+// every warp busy and several independent rows in flight per lane.  GU: rows 2j/2j+1
+// are gate/up of pair j -> abuf[j] = silu(g) * u.  Otherwise each row value is added
+// to out[row0 + row].
 template <int D, bool GU>
 __device__ __forceinline__ void q4_group(const Cons& cs, int g0, int R, int per, int part_rows,
                                          const Q4Frag<D>& f, float* abuf, float* out, int row0) {
   constexpr int LPR = Q4Frag<D>::LPR, RPW = Q4Frag<D>::RPW;
   constexpr int IR = RPW > 2 ? RPW : 2;
   constexpr int NP = IR / RPW;
+  constexpr int NI = 3;
   const int lane = cs.lane;
   const int items = R / IR;
-  for (int it = cs.cw; it < items; it += 2 * NCW) {
-    const bool two = it + NCW < items;
-    float v[2][NP];
+  for (int it = cs.cw; it < items; it += NI * NCW) {
+    float v[NI][NP];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < NI; ++u) {
 #pragma unroll
       for (int p = 0; p < NP; ++p) {
         v[u][p] = 0.f;
-        if (u == 0 || two) {
+        if (it + u * NCW < items) {
           const int rho = g0 + (it + u * NCW) * IR + p * RPW + lane / LPR;  // row within the part
           const int si = rho / per - g0 / per;
           const int nr = min(per, part_rows - (rho / per) * per);
@@ -823,12 +831,12 @@ __device__ __forceinline__ void q4_group(const Cons& cs, int g0, int R, int per,
       }
     }
 #pragma unroll
-    for (int u = 0; u < 2; ++u)
+    for (int u = 0; u < NI; ++u)
 #pragma unroll
       for (int p = 0; p < NP; ++p) v[u][p] = reduce_lpr<LPR>(v[u][p]);
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      if (u == 1 && !two) break;
+    for (int u = 0; u < NI; ++u) {
+      if (it + u * NCW >= items) break;
       const int rbase = g0 + (it + u * NCW) * IR;
       if (GU) {
         if (RPW == 1) {
@@ -862,32 +870,33 @@ __device__ __forceinline__ void consume_q4_part(Cons& cs, int rows, float* abuf,
 
 template <int D>
 struct BfFrag {
-  static constexpr int CPL = D / 256;  // chunks of 8 per lane
-  float x[CPL][8];
+  static constexpr int NV = D / 128;  // float4 groups per lane: lane owns elements 4 (lane + 32 j) .. + 3
+  float x[NV][4];                     // residual h; the row dot is scaled by sc afterwards
+  float sc;                           // RMSNorm factor: x = h * sc
   __device__ __forceinline__ void load(const Ctl& C, int lane) {
+    sc = C.xscale;
+    const float4* p = reinterpret_cast<const float4*>(C.res);
 #pragma unroll
-    for (int j = 0; j < CPL; ++j) {
-      const float4* p = reinterpret_cast<const float4*>(C.x + 8 * (lane + 32 * j));
-      const float4 a = p[0], c = p[1];
+    for (int j = 0; j < NV; ++j) {
+      const float4 a = p[lane + 32 * j];  // consecutive lanes, consecutive 16 bytes
       x[j][0] = a.x; x[j][1] = a.y; x[j][2] = a.z; x[j][3] = a.w;
-      x[j][4] = c.x; x[j][5] = c.y; x[j][6] = c.z; x[j][7] = c.w;
     }
   }
 };
 
+// Lane partial of w . x for one bf16 row (x = h * sc); the lane reads 4 bf16 (8 bytes)
+// per group, so a warp reads 256 contiguous bytes per load.
 template <int D>
 __device__ __forceinline__ float bf_partial(const uint8_t* row, int lane, const BfFrag<D>& f) {
-  const uint4* w = reinterpret_cast<const uint4*>(row);
+  const uint2* w = reinterpret_cast<const uint2*>(row);
   float v0 = 0.f, v1 = 0.f;
 #pragma unroll
-  for (int j = 0; j < BfFrag<D>::CPL; ++j) {
-    const uint4 u = w[lane + 32 * j];
+  for (int j = 0; j < BfFrag<D>::NV; ++j) {
+    const uint2 u = w[lane + 32 * j];
     v0 = fmaf(bflo(u.x), f.x[j][0], v0); v1 = fmaf(bfhi(u.x), f.x[j][1], v1);
     v0 = fmaf(bflo(u.y), f.x[j][2], v0); v1 = fmaf(bfhi(u.y), f.x[j][3], v1);
-    v0 = fmaf(bflo(u.z), f.x[j][4], v0); v1 = fmaf(bfhi(u.z), f.x[j][5], v1);
-    v0 = fmaf(bflo(u.w), f.x[j][6], v0); v1 = fmaf(bfhi(u.w), f.x[j][7], v1);
   }
-  return v0 + v1;
+  return (v0 + v1) * f.sc;
 }
 
 // Where consume_bf_rows puts a row value: a shared buffer (dst[row] = v), the head
@@ -931,6 +940,30 @@ __device__ __forceinline__ void consume_bf_rows(Cons& cs, int rows, int mode, fl
   }
 }
 
+// dst[0, n) += scale * sum_r v[r] * W[r][0, n) over the nr bf16 rows W of one stage
+// (n a multiple of 4, dst 16-byte aligned).  A thread owns 4 adjacent outputs; when
+// there are fewer 4-output groups than threads, the rows are split between
+// NCT / (n / 4) thread groups, each adding its partial sums with vector reductions.
+__device__ __forceinline__ void bf_axpy_rows(const uint8_t* st, int nr, int n, const float* v, float scale,
+                                             float* dst, int tid) {
+  const int n4 = n >> 2;
+  const int G = n4 >= NCT ? 1 : NCT / n4;
+  const int rg = tid / n4;
+  if (rg >= G) return;
+  for (int c = tid % n4; c < n4; c += NCT) {
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    for (int r = rg; r < nr; r += G) {
+      const uint2 w = reinterpret_cast<const uint2*>(st + (size_t)r * 2 * n)[c];
+      const float x = v[r];
+      s0 = fmaf(bflo(w.x), x, s0);
+      s1 = fmaf(bfhi(w.x), x, s1);
+      s2 = fmaf(bflo(w.y), x, s2);
+      s3 = fmaf(bfhi(w.y), x, s3);
+    }
+    red_add_v4_f32(dst + 4 * c, scale * s0, scale * s1, scale * s2, scale * s3);
+  }
+}
+
 template <int D>
 __device__ __forceinline__ void consume_unit(Cons& cs, const LayerDesc& Ld, const Unit& u, int l, float* acc, float* zhat,
                              float* zr) {
@@ -940,63 +973,65 @@ __device__ __forceinline__ void consume_unit(Cons& cs, const LayerDesc& Ld, cons
   switch (u.type) {
     case U_EXPERT: {
       const bool shared = u.k >= P.K;
-      if (!shared) wait_flag(P, C, &C.rt_ready[l]);
-      cbar();  // abuf / aq reuse
-      // The named barriers below are executed unconditionally so that every warp
-      // reaches the same barriers even if the route table were read inconsistently.
+      if (!shared) cs.wait_route(l);
+      // The named barrier below is executed unconditionally so that every warp
+      // reaches it even if the route table were read inconsistently.
       const bool valid = shared ? Ld.has_shared != 0 : ((C.rt_valid[l] >> u.k) & 1u) != 0;
-      if (valid) consume_q4_part<D, true>(cs, 64, C.abuf, nullptr, 0);
+      // Two activation buffers: a warp writes buffer (n & 1) of unit n only after the
+      // barrier of unit n - 1, which every warp passes after reading buffer (n & 1) of
+      // unit n - 2.
+      float* ab = C.abuf[cs.nx & 1u];
+      ++cs.nx;
+      if (valid) consume_q4_part<D, true>(cs, 64, ab, nullptr, 0);
       cbar();  // all 32 activations ready
-      if (cs.cw == 0) {
-        // quantise the 32 activations once for all warps (lane j holds a_j)
-        const float a = C.abuf[cs.lane];
-        float m = fabsf(a), s = a;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-          s += __shfl_xor_sync(0xffffffffu, s, o);
-        }
+      if (valid) {
+        // Every warp quantises the 32 activations itself (lane j holds a_j): one step
+        // m / 32767 for the slab, m = max |a_j| (the bit patterns of non-negative
+        // floats order like their values, so an unsigned max reduction finds it).
+        const float a = ab[cs.lane];
+        const float m = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(a))));
         const float r = m > 0.f ? 32767.0f / m : 0.f;
+        const float ainv = m > 0.f ? m / 32767.0f : 0.f;
         int q = __float2int_rn(a * r);
         q = q > 32767 ? 32767 : (q < -32767 ? -32767 : q);
+        const float asum = (float)__reduce_add_sync(0xffffffffu, q) * ainv;
         const int j = cs.lane, idx = j & 7;
-        reinterpret_cast<int16_t*>(C.aq)[8 * (j >> 3) + ((idx & 1) ? 4 + (idx >> 1) : (idx >> 1))] = (int16_t)q;
-        if (cs.lane == 0) {
-          C.ascale[0] = m > 0.f ? m / 32767.0f : 0.f;
-          C.ascale[1] = s;
-        }
-      }
-      cbar();
-      if (valid) {
+        __syncwarp();  // the previous slab's reads of aqw are done
+        reinterpret_cast<int16_t*>(C.aqw[cs.cw])[8 * (j >> 3) + ((idx & 1) ? 4 + (idx >> 1) : (idx >> 1))] =
+            (int16_t)q;
+        __syncwarp();
         uint32_t ap[16];
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-          const uint4 v = C.aq[t];
+          const uint4 v = C.aqw[cs.cw][t];
           ap[4 * t] = v.x; ap[4 * t + 1] = v.y; ap[4 * t + 2] = v.z; ap[4 * t + 3] = v.w;
         }
-        const float ainv = C.ascale[0], asum = C.ascale[1];
         const float wk = shared ? 1.0f : C.rt_w[l][u.k];
         const int pd = dn_rows_per_stage(D);
         constexpr int NDS = (D + 1023) / 1024;   // down-projection stages (<= 2)
-        constexpr int RPT = (D + NCT - 1) / NCT;  // rows per thread (<= 4)
+        constexpr int RPT = (D + NCT - 1) / NCT;  // rows per thread (<= 5)
+        static_assert(D % 32 == 0 && NCT % 32 == 0, "a warp owns whole 32-row blocks");
         if (cs.acquire(NDS)) {
-          float v[RPT];
 #pragma unroll
           for (int m = 0; m < RPT; ++m) {
-            const int rho = tid + NCT * m;
-            v[m] = 0.f;
-            if (rho < D) {
+            const int base = 32 * cs.cw + NCT * m;  // this warp's 32 rows
+            if (base < D) {                          // warp-uniform
+              const int rho = base + cs.lane;
               const int si = rho / pd, lr = rho % pd, nr = min(pd, D - si * pd);
               const uint8_t* st = cs.stage(si);
               const uint4 qq = reinterpret_cast<const uint4*>(st)[lr];
               const uint16_t* sc = reinterpret_cast<const uint16_t*>(st + nr * 16);
               const int a = dot32(qq, ap);
-              v[m] = bf(sc[lr]) * ((float)a * ainv) + bf(sc[nr + lr]) * asum;
+              const float v = wk * (bf(sc[lr]) * ((float)a * ainv) + bf(sc[nr + lr]) * asum);
+              // lanes 0..7 add 4 consecutive rows each with one vector reduction
+              const int src = 4 * (cs.lane & 7);
+              const float t0 = __shfl_sync(0xffffffffu, v, src);
+              const float t1 = __shfl_sync(0xffffffffu, v, src + 1);
+              const float t2 = __shfl_sync(0xffffffffu, v, src + 2);
+              const float t3 = __shfl_sync(0xffffffffu, v, src + 3);
+              if (cs.lane < 8) red_add_v4_f32(acc + base + src, t0, t1, t2, t3);
             }
           }
-#pragma unroll
-          for (int m = 0; m < RPT; ++m)
-            if (tid + NCT * m < D) red_add_f32(acc + tid + NCT * m, wk * v[m]);
         }
         cs.release(NDS);
       }
@@ -1014,20 +1049,7 @@ __device__ __forceinline__ void consume_unit(Cons& cs, const LayerDesc& Ld, cons
       const int per = max(1, STAGE_BYTES / (2 * out));
       for (int q0 = 0; q0 < u.r1 - u.r0; q0 += per) {
         const int nr = min(per, u.r1 - u.r0 - q0);
-        if (cs.acquire(1)) {
-          const uint32_t* w = reinterpret_cast<const uint32_t*>(cs.stage(0));
-          for (int i2 = tid; i2 < out / 2; i2 += NCT) {
-            float s0 = 0.f, s1 = 0.f;
-            for (int r = 0; r < nr; ++r) {
-              const uint32_t ww = w[r * (out / 2) + i2];
-              const float v = vb[q0 + r];
-              s0 = fmaf(bflo(ww), v, s0);
-              s1 = fmaf(bfhi(ww), v, s1);
-            }
-            red_add_f32(acc + 2 * i2, Ld.lscale * s0);
-            red_add_f32(acc + 2 * i2 + 1, Ld.lscale * s1);
-          }
-        }
+        if (cs.acquire(1)) bf_axpy_rows(cs.stage(0), nr, out, vb + q0, Ld.lscale, acc, tid);
         cs.release(1);
       }
       break;
@@ -1036,7 +1058,7 @@ __device__ __forceinline__ void consume_unit(Cons& cs, const LayerDesc& Ld, cons
       cbar();  // ubuf reuse
       float* ub = C.ubuf;
       consume_bf_rows<D>(cs, u.r1 - u.r0, BF_SMEM, ub, nullptr);
-      wait_flag(P, C, &C.rt_ready[l]);
+      cs.wait_route(l);
       cbar();
       const int nr = u.r1 - u.r0;
       if (cs.acquire(1) && tid < nr) {
@@ -1056,20 +1078,7 @@ __device__ __forceinline__ void consume_unit(Cons& cs, const LayerDesc& Ld, cons
       const int per = max(1, STAGE_BYTES / (2 * E));
       for (int i0 = 0; i0 < nr; i0 += per) {
         const int ni = min(per, nr - i0);
-        if (cs.acquire(1)) {
-          const uint32_t* w = reinterpret_cast<const uint32_t*>(cs.stage(0));
-          for (int e2 = tid; e2 < E / 2; e2 += NCT) {
-            float s0 = 0.f, s1 = 0.f;
-            for (int r = 0; r < ni; ++r) {
-              const uint32_t ww = w[r * (E / 2) + e2];
-              const float p = ub[i0 + r];
-              s0 = fmaf(bflo(ww), p, s0);
-              s1 = fmaf(bfhi(ww), p, s1);
-            }
-            red_add_f32(zhat + 2 * e2, s0);
-            red_add_f32(zhat + 2 * e2 + 1, s1);
-          }
-        }
+        if (cs.acquire(1)) bf_axpy_rows(cs.stage(0), ni, E, ub + i0, 1.0f, zhat, tid);
         cs.release(1);
       }
       break;
@@ -1095,10 +1104,13 @@ __device__ __forceinline__ void consume_unit(Cons& cs, const LayerDesc& Ld, cons
   }
 }
 
-// Build the layer input: residual h (fp32 of bf16 values), normed x, and the int16
-// copy of x used by the int4 rows.  Thread t owns elements t + NCT*k, so warp w owns
-// the whole 32-element chunks w + 16k and quantises them with shuffles.  inc[] holds
-// this thread's residual increments, loaded before the dependency wait.
+// Build the layer input: residual h (fp32 of bf16 values), the RMSNorm factor, and
+// the int16 copy of x = h * factor used by the int4 rows.  One quantisation step,
+// max|x| / 32767, serves the whole vector, so the only block-wide reduction is the
+// one that the norm needs anyway (sum of squares and max |h| together).  Thread t
+// owns elements t + NCT*k: warp w owns the whole 32-element chunks w + NCW*k, whose
+// sums come from one integer warp reduction.  inc[] holds this thread's residual
+// increments, loaded before the dependency wait.
 template <int D>
 __device__ __forceinline__ void layer_input(Cons& cs, int l, uint32_t par, const float* inc) {
   const EngineParams& P = cs.P;
@@ -1106,7 +1118,7 @@ __device__ __forceinline__ void layer_input(Cons& cs, int l, uint32_t par, const
   const int tid = cs.tid;
   constexpr int PER = (D + NCT - 1) / NCT;
   float h[PER];
-  float ss = 0.f;
+  float ss = 0.f, mx = 0.f;
   const float* accp = (P.mode == MODE_STACK && l > 0) ? acc_ptr(P, par, l - 1) : nullptr;
   float a[PER];
 #pragma unroll
@@ -1129,41 +1141,46 @@ __device__ __forceinline__ void layer_input(Cons& cs, int l, uint32_t par, const
       h[k] = v;
       C.res[i] = v;
       ss += v * v;
+      mx = fmaxf(mx, fabsf(v));
     }
   }
   ss = warp_sum(ss);
-  if (cs.lane == 0) C.red[cs.cw] = ss;
+  const uint32_t mb = __reduce_max_sync(0xffffffffu, __float_as_uint(mx));
+  if (cs.lane == 0) {
+    C.red[cs.cw] = ss;
+    C.redm[cs.cw] = mb;
+  }
   cbar();
   float tot = 0.f;
+  uint32_t mxb = 0u;
 #pragma unroll
-  for (int w = 0; w < NCW; ++w) tot += C.red[w];
+  for (int w = 0; w < NCW; ++w) {
+    tot += C.red[w];
+    mxb = max(mxb, C.redm[w]);
+  }
   const float scale = P.norm ? rsqrtf(tot / (float)D + RMS_EPS) : 1.0f;
+  const float xmax = __uint_as_float(mxb) * scale;
+  const float r = xmax > 0.f ? 32767.0f / xmax : 0.f;
+  const float inv = xmax > 0.f ? xmax / 32767.0f : 0.f;
   int16_t* xq16 = reinterpret_cast<int16_t*>(C.xq);
 #pragma unroll
   for (int k = 0; k < PER; ++k) {
     const int i = tid + NCT * k;
     if (i < D) {  // warp-uniform: chunks are warp-aligned
-      const float x = h[k] * scale;
-      C.x[i] = x;
-      float m = fabsf(x), s = x;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        s += __shfl_xor_sync(0xffffffffu, s, o);
-      }
-      const float r = m > 0.f ? 32767.0f / m : 0.f;
-      int q = __float2int_rn(x * r);
+      int q = __float2int_rn(h[k] * scale * r);
       q = q > 32767 ? 32767 : (q < -32767 ? -32767 : q);
       const int c = i >> 5, j = cs.lane, idx = j & 7;
-      xq16[32 * c + 8 * (j >> 3) + ((idx & 1) ? 4 + (idx >> 1) : (idx >> 1))] = (int16_t)q;
+      xq16[((j >> 3) * (DMAX / 32) + c) * 8 + ((idx & 1) ? 4 + (idx >> 1) : (idx >> 1))] = (int16_t)q;
+      const int sq = __reduce_add_sync(0xffffffffu, q);
       if (cs.lane == 0) {
-        C.xinv[c] = m > 0.f ? m / 32767.0f : 0.f;
-        C.xsum[c] = s;
+        C.xinv[c] = inv;
+        C.xsum[c] = (float)sq * inv;
       }
       if (P.mode == MODE_STACK && P.h_trace && blockIdx.x == 0)
         P.h_trace[(size_t)l * D + i] = f32_to_bf16_bits(h[k]);
     }
   }
+  if (tid == 0) C.xscale = scale;
   cbar();
 }
 

@@ -33,7 +33,7 @@ constexpr int NCW = 14;                       // consumer warps (16 warps in all
 constexpr int NTHREADS = (NCW + 2) * 32;      // + producer warp + routing warp
 constexpr int NCT = NCW * 32;                 // consumer threads
 constexpr int STAGE_BYTES = 20480;
-constexpr int NSTAGES = 8;
+constexpr int NSTAGES = 9;
 constexpr int KMAX = 16;
 constexpr int EMAX = 1024;
 constexpr int DMAX = 2048;
