@@ -84,6 +84,10 @@ struct Granule {
 // byte of bf16 rows.
 constexpr double W_INT4 = 1.25;
 constexpr double W_BF16 = 1.0;
+// Fixed cost of one unit on a CTA, in the same units (bf16 bytes): the fragment load
+// of x, the first stage's wait and the barriers between phases take about as long as
+// streaming 32 KB.  It steers the planner away from giving one CTA several small units.
+constexpr double UNIT_COST = 32768.0;
 
 e0_status build_plan(const PlanSpec& s, int ncta, Unit* units, uint8_t* counts) {
   std::vector<std::vector<Unit>> lists(ncta);
@@ -91,7 +95,7 @@ e0_status build_plan(const PlanSpec& s, int ncta, Unit* units, uint8_t* counts) 
   const int d = s.d;
   // 1. expert slabs, round robin
   if (s.routed || s.shared) {
-    const double c_exp = W_INT4 * (64.0 * q4_row_bytes(d) + 20.0 * d);
+    const double c_exp = W_INT4 * (64.0 * q4_row_bytes(d) + 20.0 * d) + UNIT_COST;
     int idx = 0;
     const int kmax = s.routed ? s.K : 0;
     for (int k = 0; k <= kmax; ++k) {
@@ -107,22 +111,11 @@ e0_status build_plan(const PlanSpec& s, int ncta, Unit* units, uint8_t* counts) 
   }
   // 2. divisible work as granules
   std::vector<Granule> gs;
-  {
-    // LoRA base rows with the rank slices spread between them, so that the ranks land
-    // on different CTAs rather than piling up on one
-    std::vector<Granule> qr, ab;
-    if (s.lora)
-      for (int r = 0; r < s.lout; r += 16) qr.push_back({U_QROWS, r, 16, W_INT4 * 16.0 * q4_row_bytes(d)});
-    if (s.lora_ab)
-      for (int q = 0; q < s.lr; ++q) ab.push_back({U_LORA_AB, q, 1, W_BF16 * (2.0 * d + 2.0 * s.lout)});
-    const size_t every = ab.empty() ? 0 : std::max<size_t>(1, qr.size() / ab.size());
-    size_t ia = 0;
-    for (size_t i = 0; i < qr.size(); ++i) {
-      gs.push_back(qr[i]);
-      if (every && (i + 1) % every == 0 && ia < ab.size()) gs.push_back(ab[ia++]);
-    }
-    while (ia < ab.size()) gs.push_back(ab[ia++]);
-  }
+  // the LoRA down projection first: the CTAs that own LoRA base rows wait for its v
+  if (s.lora_ab) gs.push_back({U_LORA_A, 0, s.lr, W_BF16 * 2.0 * d * s.lr});
+  if (s.lora)
+    for (int r = 0; r < s.lout; r += 16)
+      gs.push_back({U_QROWS, r, 16, W_INT4 * 16.0 * q4_row_bytes(d) + W_BF16 * 16.0 * 2.0 * s.lr});
   if (s.lres)
     for (int e = 0; e < s.E; e += 8) gs.push_back({U_LRES, e, 8, W_BF16 * 8.0 * 2.0 * d});
   if (s.head)
@@ -132,9 +125,10 @@ e0_status build_plan(const PlanSpec& s, int ncta, Unit* units, uint8_t* counts) 
     for (int e = 0; e < s.E; e += 8) gs.push_back({U_ROUTER, e, 8, W_BF16 * 8.0 * 2.0 * d});
   double gtotal = 0.0;
   for (auto& g : gs) gtotal += g.cost;
-  // 3. water-fill: the level T at which the CTAs below it take exactly the granules,
-  //    sum_c max(0, T - load[c]) = gtotal (CTAs already above T, e.g. ones with an
-  //    expert slab heavier than the mean, get nothing more)
+  // 3. water-fill: the level T at which the CTAs below it take exactly the granules
+  //    and one unit cost each, sum_c max(0, T - load[c]) = gtotal + UNIT_COST * n_below
+  //    (CTAs already above T, e.g. ones with an expert slab heavier than the mean, get
+  //    nothing more)
   double level = 0.0;
   {
     std::vector<double> sorted(load);
@@ -142,7 +136,7 @@ e0_status build_plan(const PlanSpec& s, int ncta, Unit* units, uint8_t* counts) 
     double below = 0.0;  // sum of the loads of the CTAs under the level
     for (int c = 0; c < ncta; ++c) {
       below += sorted[c];
-      const double t = (gtotal + below) / (c + 1);  // level if CTAs 0..c take everything
+      const double t = (gtotal + below) / (c + 1) + UNIT_COST;  // level if CTAs 0..c take everything
       if (c + 1 == ncta || t <= sorted[c + 1]) {
         level = t;
         break;
@@ -155,37 +149,55 @@ e0_status build_plan(const PlanSpec& s, int ncta, Unit* units, uint8_t* counts) 
   for (int c = 0; c < ncta && g < gs.size(); ++c) {
     cum_cap += std::max(0.0, level - load[c]);
     const bool last = (c == ncta - 1);
-    while (g < gs.size() && (last || cum_assigned + 0.5 * gs[g].cost <= cum_cap)) {
+    while (g < gs.size()) {
       const Granule& gr = gs[g];
       auto& L = lists[c];
       // merge with the previous unit when contiguous and of the same type
-      bool merged = false;
+      Unit* into = nullptr;
       for (auto& u : L) {
         if (u.type == gr.type && u.r1 == gr.row) {
+          // unit size limits: head buffers; the B slice of a LoRA row unit fits one stage
           const int limit = (gr.type == U_HEAD || gr.type == U_LRES) ? HEAD_ROWS
-                            : (gr.type == U_LORA_AB ? 4 : 65535);
-          if ((int)u.r1 - (int)u.r0 + gr.rows <= limit) {
-            u.r1 = (uint16_t)(gr.row + gr.rows);
-            merged = true;
-          }
+                            : gr.type == U_QROWS && s.lr > 0 ? (STAGE_BYTES / (2 * s.lr)) / 16 * 16
+                                                             : 65535;
+          if ((int)u.r1 - (int)u.r0 + gr.rows <= limit) into = &u;
           break;
         }
       }
-      if (!merged) lists[c].push_back(Unit{gr.type, 0, (uint16_t)gr.row, (uint16_t)(gr.row + gr.rows), 0});
-      load[c] += gr.cost;
-      cum_assigned += gr.cost;
+      const double cost = gr.cost + (into ? 0.0 : UNIT_COST);
+      if (!last && cum_assigned + 0.5 * cost > cum_cap) break;
+      if (into)
+        into->r1 = (uint16_t)(gr.row + gr.rows);
+      else
+        L.push_back(Unit{gr.type, 0, (uint16_t)gr.row, (uint16_t)(gr.row + gr.rows), 0});
+      if (gr.type == U_QROWS && s.lr > 0) {
+        // the B rows of the same LoRA rows go with them, as a unit of their own
+        bool merged_b = false;
+        for (auto& u : L)
+          if (u.type == U_LORA_B && u.r1 == gr.row && (int)u.r1 - (int)u.r0 + gr.rows <= (STAGE_BYTES / (2 * s.lr)) / 16 * 16) {
+            u.r1 = (uint16_t)(gr.row + gr.rows);
+            merged_b = true;
+            break;
+          }
+        if (!merged_b) L.push_back(Unit{U_LORA_B, 0, (uint16_t)gr.row, (uint16_t)(gr.row + gr.rows), 0});
+      }
+      load[c] += cost;
+      cum_assigned += cost;
       ++g;
     }
   }
-  // 4. order: id-independent work first, experts last
+  // 4. order: id-independent work first, experts last.  U_LORA_A must precede U_LORA_B
+  //    on a CTA that has both (B waits for the v that A publishes); B goes late so that
+  //    v is normally there by the time it is needed.
   auto rank = [](uint8_t t) {
     switch (t) {
       case U_ROUTER: return 0;
-      case U_QROWS: return 1;
-      case U_LORA_AB: return 2;
+      case U_LORA_A: return 1;
+      case U_QROWS: return 2;
       case U_LRES: return 3;
       case U_HEAD: return 4;
-      default: return 5;
+      case U_LORA_B: return 5;
+      default: return 6;
     }
   };
   for (int c = 0; c < ncta; ++c) {

@@ -24,6 +24,7 @@ struct Ctl {
   float b2buf[HEAD_ROWS];     // head fc2 bias slice of the current LRES unit
   float ubuf[HEAD_ROWS];      // head fc1 pre-activation, then erf-GELU output
   float vbuf[RANKS_MAX];      // LoRA A x for the current rank slice
+  float lvs[RANKS_MAX];       // LoRA v = A x of the layer (all ranks), for the B rows
   float zbuf[EMAX];           // logits staged for top-K
   // routing of every layer of this launch
   int16_t rt_ids[LMAX][KMAX];   // committed expert ids
@@ -71,7 +72,10 @@ __device__ __forceinline__ const Unit* units_of(const EngineParams& P, int kind,
 
 __device__ __forceinline__ WsHeader* hdr(const EngineParams& P) { return reinterpret_cast<WsHeader*>(P.ws); }
 __device__ __forceinline__ uint32_t* ctr(const EngineParams& P, uint32_t par, int l, int which) {
-  return reinterpret_cast<uint32_t*>(P.ws + P.wl.counters) + ((size_t)par * P.L + l) * 2 + which;
+  return reinterpret_cast<uint32_t*>(P.ws + P.wl.counters) + ((size_t)par * P.L + l) * 4 + which;
+}
+__device__ __forceinline__ float* lv_ptr(const EngineParams& P, uint32_t par, int l) {
+  return reinterpret_cast<float*>(P.ws + P.wl.lv) + ((size_t)par * P.L + l) * RANKS_MAX;
 }
 __device__ __forceinline__ float* acc_ptr(const EngineParams& P, uint32_t par, int l) {
   return reinterpret_cast<float*>(P.ws + P.wl.acc) + ((size_t)par * P.L + l) * OUTMAX;
@@ -564,11 +568,23 @@ __device__ __forceinline__ void issue_unit(Prod& pr, const LayerDesc& Ld, const 
       for (int r = u.r0; r < u.r1; r += per) issue_q4_rows(pr, Ld.lw_q, Ld.lw_s, Ld.lw_b, d, r, min(per, u.r1 - r));
       break;
     }
-    case U_LORA_AB: {
+    case U_LORA_B: {
+      // one stage: Bt[q][r0, r1) for every rank q, stored [q][row]
+      const int nr = u.r1 - u.r0;
+      uint32_t slot;
+      uint8_t* st = prod_begin(pr, slot);
+      if (!st) return;
+      if (pr.lane == 0) {
+        mbar_arrive_expect_tx(&C.full[slot], (uint32_t)(Ld.lr * nr * 2));
+        for (int q = 0; q < Ld.lr; ++q)
+          tma_bulk_g2s(st + (size_t)q * nr * 2, Ld.lbt + (size_t)q * Ld.lout + u.r0, (uint32_t)nr * 2,
+                       &C.full[slot]);
+      }
+      ++pr.n;
+      break;
+    }
+    case U_LORA_A: {
       issue_bf_rows(pr, Ld.la, d, u.r0, u.r1);
-      const int per = max(1, STAGE_BYTES / (2 * Ld.lout));
-      for (int q = u.r0; q < u.r1; q += per)
-        issue_bytes(pr, Ld.lbt + (size_t)q * Ld.lout, (uint32_t)min(per, u.r1 - q) * Ld.lout * 2);
       break;
     }
     case U_HEAD: {
@@ -1040,18 +1056,40 @@ __device__ __forceinline__ void consume_unit(Cons& cs, const LayerDesc& Ld, cons
     case U_QROWS:
       consume_q4_part<D, false>(cs, u.r1 - u.r0, nullptr, acc, u.r0);
       break;
-    case U_LORA_AB: {
-      cbar();  // vbuf reuse
-      float* vb = C.vbuf;
-      consume_bf_rows<D>(cs, u.r1 - u.r0, BF_SMEM, vb, nullptr);
+    case U_LORA_B: {
+      // (alpha/r) B v for rows [r0, r1), once every rank of v is published
+      const uint32_t par = C.epoch & 1u;
+      if (tid == 0) wait_count(P, C, ctr(P, par, l, 2), (uint32_t)Ld.lr);
       cbar();
-      const int out = Ld.lout;
-      const int per = max(1, STAGE_BYTES / (2 * out));
-      for (int q0 = 0; q0 < u.r1 - u.r0; q0 += per) {
-        const int nr = min(per, u.r1 - u.r0 - q0);
-        if (cs.acquire(1)) bf_axpy_rows(cs.stage(0), nr, out, vb + q0, Ld.lscale, acc, tid);
-        cs.release(1);
+      if (tid < Ld.lr) C.lvs[tid] = __ldcg(lv_ptr(P, par, l) + tid);
+      cbar();
+      const int nr = u.r1 - u.r0;
+      if (cs.acquire(1)) {
+        const uint16_t* bt = reinterpret_cast<const uint16_t*>(cs.stage(0));
+        for (int rho = tid; rho < nr; rho += NCT) {
+          float s0 = 0.f, s1 = 0.f;
+          int q = 0;
+          for (; q + 1 < Ld.lr; q += 2) {
+            s0 = fmaf(bf(bt[q * nr + rho]), C.lvs[q], s0);
+            s1 = fmaf(bf(bt[(q + 1) * nr + rho]), C.lvs[q + 1], s1);
+          }
+          if (q < Ld.lr) s0 = fmaf(bf(bt[q * nr + rho]), C.lvs[q], s0);
+          red_add_f32(acc + u.r0 + rho, Ld.lscale * (s0 + s1));
+        }
       }
+      cs.release(1);
+      break;
+    }
+    case U_LORA_A: {
+      // v = A x for ranks [r0, r1), published for the CTAs that own the B rows
+      const uint32_t par = C.epoch & 1u;
+      const int n = u.r1 - u.r0;
+      cbar();  // vbuf reuse
+      consume_bf_rows<D>(cs, n, BF_SMEM, C.vbuf, nullptr);
+      cbar();
+      if (tid < n) lv_ptr(P, par, l)[u.r0 + tid] = C.vbuf[tid];
+      cbar();  // orders every thread's store before the release below
+      if (tid == 0) red_release_add_u32(ctr(P, par, l, 2), (uint32_t)n);
       break;
     }
     case U_HEAD: {
@@ -1249,7 +1287,7 @@ __device__ void consumer(const EngineParams& P, Ctl& C, uint8_t* ring) {
 
     if (l == P.L - 1) {
       // Clear the other half of the parity-duplicated buffers for the next launch.
-      const size_t n_ctr = (size_t)P.L * 2, n_acc = (size_t)P.L * P.out_dim, n_z = (size_t)P.L * P.E;
+      const size_t n_ctr = (size_t)P.L * 4, n_acc = (size_t)P.L * P.out_dim, n_z = (size_t)P.L * P.E;
       const size_t total = n_ctr + n_acc + n_z;
       const size_t per = (total + ncta - 1) / ncta;
       const size_t b0 = (size_t)cta * per, b1 = min(total, b0 + per);

@@ -15,8 +15,9 @@
 //             to 32 columns of its SwiGLU width: 32 gate rows + 32 up rows give 32
 //             activations a = silu(g) * u, which the matching 32-column slab of the
 //             down projection turns into a contribution to all d outputs;
-//   U_QROWS   rows of the LoRA base W;  U_LORA_AB  a slice of ranks: v = A x, then
-//             (alpha/r) Bt^T v;  U_HEAD  rows of prerouter fc1 (plus the one-hot
+//   U_QROWS   rows of the LoRA base W;  U_LORA_A  a slice of ranks of the LoRA down
+//             projection, v = A x, published to the other CTAs;  U_LORA_B  (alpha/r) B v
+//             for LoRA rows once v is published (last on its CTA, so v is rarely waited for);  U_HEAD  rows of prerouter fc1 (plus the one-hot
 //             columns picked by the committed ids), erf-GELU, then the matching rows
 //             of fc2^T;  U_LRES  rows of the head's linear residual;  U_ROUTER  rows
 //             of a layer's own gate.
@@ -46,7 +47,7 @@ constexpr int KINDS_MAX = 3;
 constexpr int LMAX = 64;                      // layers per launch
 constexpr float RMS_EPS = 1e-6f;
 
-enum UnitType : uint8_t { U_NONE = 0, U_EXPERT, U_QROWS, U_LORA_AB, U_HEAD, U_LRES, U_ROUTER };
+enum UnitType : uint8_t { U_NONE = 0, U_EXPERT, U_QROWS, U_LORA_A, U_HEAD, U_LRES, U_ROUTER, U_LORA_B };
 
 struct Unit {
   uint8_t type;
@@ -119,7 +120,7 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 64, "header size");
 
 struct WsLayout {
-  size_t counters;   // u32 [2][L][2]
+  size_t counters;   // u32 [2][L][4]: layer done, own gate done, LoRA v published
   size_t acc;        // f32 [2][L][OUTMAX]
   size_t zhat;       // f32 [3][L][E]
   size_t zr;         // f32 [2][L][E]
@@ -128,6 +129,7 @@ struct WsLayout {
   size_t rg_ids;     // i32 [2][L][KMAX] routes committed for the next launch
   size_t rg_w;       // f32 [2][L][KMAX]
   size_t rg_tag;     // u32 [2][L]  epoch the route is for
+  size_t lv;         // f32 [2][L][RANKS_MAX]  LoRA v = A x
   size_t total;
 };
 
@@ -136,7 +138,7 @@ __host__ __device__ inline size_t ws_align(size_t x) { return (x + 255) & ~size_
 __host__ __device__ inline WsLayout ws_layout(int E, int L) {
   WsLayout w;
   size_t o = 256;
-  w.counters = o; o = ws_align(o + sizeof(uint32_t) * 2 * L * 2);
+  w.counters = o; o = ws_align(o + sizeof(uint32_t) * 2 * L * 4);
   w.acc = o;      o = ws_align(o + sizeof(float) * 2 * (size_t)L * OUTMAX);
   w.zhat = o;     o = ws_align(o + sizeof(float) * 3 * (size_t)L * E);
   w.zr = o;       o = ws_align(o + sizeof(float) * 2 * (size_t)L * E);
@@ -145,6 +147,7 @@ __host__ __device__ inline WsLayout ws_layout(int E, int L) {
   w.rg_ids = o;   o = ws_align(o + sizeof(int32_t) * 2 * (size_t)L * KMAX);
   w.rg_w = o;     o = ws_align(o + sizeof(float) * 2 * (size_t)L * KMAX);
   w.rg_tag = o;   o = ws_align(o + sizeof(uint32_t) * 2 * (size_t)L);
+  w.lv = o;       o = ws_align(o + sizeof(float) * 2 * (size_t)L * RANKS_MAX);
   w.total = o;
   return w;
 }
