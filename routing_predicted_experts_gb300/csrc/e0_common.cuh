@@ -108,6 +108,19 @@ __device__ __forceinline__ void red_add_v4_f32(float* p, float a, float b, float
                : "memory");
 }
 
+// A value published with its tag in one 64-bit word: a reader that sees the tag it
+// expects also sees the value written with it (single-copy atomic 64-bit access), so
+// no counter or fence is needed between writer and reader.
+__device__ __forceinline__ void st_tagged(uint64_t* p, uint32_t tag, float v) {
+  const uint64_t w = ((uint64_t)tag << 32) | __float_as_uint(v);
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // L2-coherent loads for data written by other CTAs during the same launch.
 __device__ __forceinline__ float ld_cg_f32(const float* p) {
   float v;

@@ -83,8 +83,8 @@ __device__ __forceinline__ float* acc_ptr(const EngineParams& P, uint32_t par, i
 __device__ __forceinline__ float* zhat_ptr(const EngineParams& P, uint32_t p3, int l) {
   return reinterpret_cast<float*>(P.ws + P.wl.zhat) + ((size_t)p3 * P.L + l) * P.E;
 }
-__device__ __forceinline__ float* zr_ptr(const EngineParams& P, uint32_t par, int l) {
-  return reinterpret_cast<float*>(P.ws + P.wl.zr) + ((size_t)par * P.L + l) * P.E;
+__device__ __forceinline__ uint64_t* zr_ptr(const EngineParams& P, uint32_t par, int l) {
+  return reinterpret_cast<uint64_t*>(P.ws + P.wl.zr) + ((size_t)par * P.L + l) * P.E;
 }
 __device__ __forceinline__ int32_t* idsu_ptr(const EngineParams& P, uint32_t par, int l) {
   return reinterpret_cast<int32_t*>(P.ws + P.wl.ids) + ((size_t)par * P.L + l) * KMAX;
@@ -254,6 +254,39 @@ __device__ __noinline__ void warp_topk(const float* z, int E, int K, int lane, i
   __syncwarp();
 }
 
+// Top-K of logits held in registers (lane holds z[lane + 32 j], j < NPL), descending,
+// ties to the lower index, with the same key order as warp_topk.  Each round takes the
+// warp maximum of the keys below the previous pick with two integer reductions (high
+// then low word).  Lane k < K receives the k-th id (-1 if none) and its logit.
+__device__ __forceinline__ float topk_key_value(uint32_t hi) {
+  return __uint_as_float((hi & 0x80000000u) ? (hi & 0x7FFFFFFFu) : ~hi);
+}
+template <int NPL>
+__device__ __forceinline__ void warp_topk_regs(const float (&z)[NPL], int E, int K, int lane, int& id, float& val) {
+  uint64_t key[NPL];
+#pragma unroll
+  for (int j = 0; j < NPL; ++j) {
+    const int e = lane + 32 * j;
+    key[j] = e < E ? topk_key(z[j], e) : 0ull;
+  }
+  uint64_t prev = ~0ull;
+  id = -1;
+  val = 0.f;
+  for (int k = 0; k < K; ++k) {
+    uint64_t m = 0ull;
+#pragma unroll
+    for (int j = 0; j < NPL; ++j)
+      if (key[j] < prev && key[j] > m) m = key[j];
+    const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(m >> 32));
+    const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(m >> 32) == hi ? (uint32_t)m : 0u);
+    prev = ((uint64_t)hi << 32) | lo;
+    if (lane == k && prev != 0ull) {
+      id = (int)(0xFFFFFFFFu - lo);
+      val = topk_key_value(hi);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ producer
 // The whole producer warp runs this code in lock step; lane 0 issues the copies and
 // all lanes take part in routing (loads of logits and ids, warp top-K).
@@ -374,16 +407,41 @@ __device__ __noinline__ void load_routes(Prod& pr) {
   // Stage, with independent loads issued back to back: the previous-token ids of every
   // layer (recorded by the previous launch) and the routes it committed for this token.
   const int L = P.L;
-  for (int j = lane; j < L * K; j += 32) {
-    const int l = j / K, k = j % K;
-    const int pid = P.step > 0 ? __ldcg(idsu_ptr(P, pr.par ^ 1u, l) + k) : -1;
-    const int id = __ldcg(rg_ids_ptr(P, pr.par, l) + k);
-    const float w = __ldcg(rg_w_ptr(P, pr.par, l) + k);
-    C.rt_prev[l][k] = (int16_t)pid;
-    C.rt_ids[l][k] = (int16_t)id;
-    C.rt_w[l][k] = w;
+  for (int j0 = 0; j0 < L * K; j0 += 32 * 8) {
+    int pid[8], id[8];
+    float w[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {  // loads first, all in flight together
+      const int j = j0 + 32 * u + lane, l = j / K, k = j % K;
+      pid[u] = -1;
+      id[u] = -1;
+      w[u] = 0.f;
+      if (j < L * K) {
+        if (P.step > 0) pid[u] = __ldcg(idsu_ptr(P, pr.par ^ 1u, l) + k);
+        if (!self_routes(P, l)) {
+          id[u] = __ldcg(rg_ids_ptr(P, pr.par, l) + k);
+          w[u] = __ldcg(rg_w_ptr(P, pr.par, l) + k);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int j = j0 + 32 * u + lane, l = j / K, k = j % K;
+      if (j < L * K) {
+        C.rt_prev[l][k] = (int16_t)pid[u];
+        if (!self_routes(P, l)) {  // a self-routed layer may already have its route published
+          C.rt_ids[l][k] = (int16_t)id[u];
+          C.rt_w[l][k] = w[u];
+        }
+      }
+    }
   }
-  for (int l = lane; l < L; l += 32) C.rt_tag[l] = __ldcg(rg_tag_ptr(P, pr.par, l));
+  {
+    const uint32_t t0 = lane < L ? __ldcg(rg_tag_ptr(P, pr.par, lane)) : 0u;
+    const uint32_t t1 = lane + 32 < L ? __ldcg(rg_tag_ptr(P, pr.par, lane + 32)) : 0u;
+    if (lane < L) C.rt_tag[lane] = t0;
+    if (lane + 32 < L) C.rt_tag[lane + 32] = t1;
+  }
   __syncwarp();
   for (int l = 0; l < L; ++l) {
     bool pv = false;
@@ -442,20 +500,48 @@ __device__ __forceinline__ bool prod_wait_counter(Prod& pr, int l, int which) {
 
 // A layer that routes with its own gate: wait until every CTA wrote its gate rows,
 // then publish the top-K of the gate logits (routing warp).
+template <int NPL>
+__device__ __forceinline__ void self_route_regs(Prod& pr, int l) {
+  const EngineParams& P = pr.P;
+  const uint64_t* z = zr_ptr(P, pr.par, l);
+  const uint32_t tag = pr.epoch + 1u;
+  float zv[NPL];
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    bool have = true;
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+      const int e = pr.lane + 32 * j;
+      zv[j] = 0.f;
+      if (e < P.E) {
+        const uint64_t w = ld_relaxed_u64(z + e);
+        have = have && (uint32_t)(w >> 32) == tag;
+        zv[j] = __uint_as_float((uint32_t)w);
+      }
+    }
+    if (__all_sync(0xffffffffu, have)) break;
+    if (!prod_keep_waiting(pr, t0, it)) {
+      pr.ok = false;
+      return;
+    }
+  }
+  int id;
+  float val;
+  warp_topk_regs<NPL>(zv, P.E, P.K, pr.lane, id, val);
+  const float v0 = __shfl_sync(0xffffffffu, val, 0);
+  publish_route(pr, l, pr.lane < P.K ? id : -1, pr.lane < P.K && id >= 0 ? expf(val - v0) : 0.f);
+}
+
+// A layer that routes with its own gate: wait until every gate logit of this launch
+// is published (tagged words, see st_tagged), then publish their top-K (routing warp).
 __device__ __noinline__ void compute_self_route(Prod& pr, int l) {
   if (!pr.ok || pr.C.rt_ready[l]) return;
-  if (!prod_wait_counter(pr, l, 1)) {
-    pr.ok = false;
-    return;
-  }
-  const float* z = zr_ptr(pr.P, pr.par, l);
-#pragma unroll 8
-  for (int e = pr.lane; e < pr.P.E; e += 32) pr.C.zbuf[e] = __ldcg(z + e);
-  __syncwarp();
-  int id;
-  float w;
-  topk_lane(pr, id, w);
-  publish_route(pr, l, id, w);
+  if (pr.P.E <= 256)
+    self_route_regs<8>(pr, l);
+  else if (pr.P.E <= 512)
+    self_route_regs<16>(pr, l);
+  else
+    self_route_regs<32>(pr, l);
 }
 
 // Producer: wait (bounded) until the routing warp has published layer l's route.
@@ -668,6 +754,9 @@ __device__ void producer(const EngineParams& P, Ctl& C, uint8_t* ring) {
 // complete) and, in the stack, the bookkeeping for the next token.
 __device__ void router_warp(const EngineParams& P, Ctl& C) {
   Prod pr{P, C, nullptr, 0u, true, (int)(threadIdx.x & 31), C.epoch & 1u, C.epoch % 3u, C.epoch};
+  // The first layer's own route is needed first: compute it before staging the rest
+  // (a layer with a head also needs its previous-token ids, staged below).
+  if (P.mode == MODE_STACK && self_routes(P, 0) && !layer_at(P, 0).has_head) compute_self_route(pr, 0);
   load_routes(pr);
   if (P.mode == MODE_STACK)
     for (int l = 0; l < P.L && pr.ok; ++l) {
@@ -717,8 +806,6 @@ __device__ void router_warp(const EngineParams& P, Ctl& C) {
     }
   }
   // After an abort, mark every route published so that no consumer waits on one.
-  if (pr.lane == 0 && !pr.ok)
-    for (int l = 0; l < P.L; ++l) C.rt_ready[l] = 1;
   if (pr.lane == 0 && !pr.ok)
     for (int l = 0; l < P.L; ++l) C.rt_ready[l] = 1;
 }
@@ -917,7 +1004,7 @@ __device__ __forceinline__ float bf_partial(const uint8_t* row, int lane, const 
 
 // Where consume_bf_rows puts a row value: a shared buffer (dst[row] = v), the head
 // logits accumulator (dst[row] += v + bias[row]), or a layer's gate logits (dst[row] = v).
-enum BfOut : int { BF_SMEM = 0, BF_ADD_BIAS = 1, BF_STORE = 2 };
+enum BfOut : int { BF_SMEM = 0, BF_ADD_BIAS = 1, BF_TAGGED = 2 };
 
 // bf16 rows [0, rows) of a part (in = D), stages of bf_rows_per_stage(D) rows, in
 // groups of at most GMAX stages; one warp per row, two rows per pass.
@@ -946,6 +1033,8 @@ __device__ __forceinline__ void consume_bf_rows(Cons& cs, int rows, int mode, fl
             const float v = u ? vb : va;
             if (mode == BF_ADD_BIAS)
               red_add_f32(dst + row, v + (bias ? bias[row] : 0.f));
+            else if (mode == BF_TAGGED)
+              st_tagged(reinterpret_cast<uint64_t*>(dst) + row, cs.C.epoch + 1u, v);
             else
               dst[row] = v;
           }
@@ -1134,7 +1223,8 @@ __device__ __forceinline__ void consume_unit(Cons& cs, const LayerDesc& Ld, cons
     }
     case U_ROUTER: {
       const int e0 = u.r0;
-      consume_bf_rows<D>(cs, u.r1 - u.r0, BF_STORE, zr + e0, nullptr);
+      consume_bf_rows<D>(cs, u.r1 - u.r0, BF_TAGGED, reinterpret_cast<float*>(reinterpret_cast<uint64_t*>(zr) + e0),
+                         nullptr);
       break;
     }
     default:
@@ -1259,14 +1349,13 @@ __device__ void consumer(const EngineParams& P, Ctl& C, uint8_t* ring) {
     if (tid == 0) stamp(P, l, 2);
     float* acc = acc_ptr(P, par, l);
     float* zh = zhat_ptr(P, pnext3, l);
-    float* zr = zr_ptr(P, par, l);
+    float* zr = reinterpret_cast<float*>(zr_ptr(P, par, l));  // tagged u64 words
     const bool self_route = P.mode == MODE_STACK && ((P.router_mask >> l) & 1ull);
     if (self_route) {
+      // gate rows first: the routing warps pick this layer's experts from them
       int nu;
       const Unit* us = units_of(P, KIND_ROUTER, cta, nu);
       for (int i = 0; i < nu; ++i) consume_unit<D>(cs, Ld, us[i], l, acc, zh, zr);
-      cbar();
-      if (tid == 0) red_release_add_u32(ctr(P, par, l, 1), 1u);
     }
     int nu;
     const Unit* us = units_of(P, P.plan ? Ld.plan_kind : 0, cta, nu);

@@ -123,7 +123,7 @@ struct WsLayout {
   size_t counters;   // u32 [2][L][4]: layer done, own gate done, LoRA v published
   size_t acc;        // f32 [2][L][OUTMAX]
   size_t zhat;       // f32 [3][L][E]
-  size_t zr;         // f32 [2][L][E]
+  size_t zr;         // u64 [2][L][E]  own-gate logits, tagged with the launch (see st_tagged)
   size_t ids;        // i32 [2][L][KMAX]
   size_t wts;        // f32 [2][L][KMAX]
   size_t rg_ids;     // i32 [2][L][KMAX] routes committed for the next launch
@@ -141,7 +141,7 @@ __host__ __device__ inline WsLayout ws_layout(int E, int L) {
   w.counters = o; o = ws_align(o + sizeof(uint32_t) * 2 * L * 4);
   w.acc = o;      o = ws_align(o + sizeof(float) * 2 * (size_t)L * OUTMAX);
   w.zhat = o;     o = ws_align(o + sizeof(float) * 3 * (size_t)L * E);
-  w.zr = o;       o = ws_align(o + sizeof(float) * 2 * (size_t)L * E);
+  w.zr = o;       o = ws_align(o + sizeof(uint64_t) * 2 * (size_t)L * E);
   w.ids = o;      o = ws_align(o + sizeof(int32_t) * 2 * (size_t)L * KMAX);
   w.wts = o;      o = ws_align(o + sizeof(float) * 2 * (size_t)L * KMAX);
   w.rg_ids = o;   o = ws_align(o + sizeof(int32_t) * 2 * (size_t)L * KMAX);
