@@ -307,7 +307,7 @@ __device__ __forceinline__ bool self_routes(const EngineParams& P, int l) {
 // Publish the routing of layer l in the route table.  Lane k (< K) brings id k
 // (-1 = none) and its unnormalised combine weight; ids are checked (range,
 // duplicates, slot table) and the weights renormalised over the ids that survive.
-__device__ __noinline__ void publish_route(Prod& pr, int l, int id, float w) {
+__device__ __forceinline__ void publish_route(Prod& pr, int l, int id, float w) {
   const EngineParams& P = pr.P;
   Ctl& C = pr.C;
   const LayerDesc& Ld = layer_at(P, l);
@@ -368,7 +368,7 @@ __device__ __forceinline__ void topk_lane(Prod& pr, int& id, float& w) {
 
 // Kernel start: routing known at launch time (given ids, or the routes the previous
 // launch committed for this token) and the previous-token ids the heads one-hot.
-__device__ __noinline__ void load_routes(Prod& pr) {
+__device__ __forceinline__ void load_routes(Prod& pr) {
   const EngineParams& P = pr.P;
   Ctl& C = pr.C;
   const int lane = pr.lane, K = P.K;
@@ -458,7 +458,7 @@ __device__ __noinline__ void load_routes(Prod& pr) {
 }
 
 // Publish the staged route of a prerouted layer (committed by the previous launch).
-__device__ __noinline__ void publish_staged_route(Prod& pr, int l) {
+__device__ __forceinline__ void publish_staged_route(Prod& pr, int l) {
   Ctl& C = pr.C;
   const bool fresh = C.rt_tag[l] == pr.epoch;
   int id = -1;
@@ -534,7 +534,7 @@ __device__ __forceinline__ void self_route_regs(Prod& pr, int l) {
 
 // A layer that routes with its own gate: wait until every gate logit of this launch
 // is published (tagged words, see st_tagged), then publish their top-K (routing warp).
-__device__ __noinline__ void compute_self_route(Prod& pr, int l) {
+__device__ __forceinline__ void compute_self_route(Prod& pr, int l) {
   if (!pr.ok || pr.C.rt_ready[l]) return;
   if (pr.P.E <= 256)
     self_route_regs<8>(pr, l);
