@@ -66,13 +66,18 @@ def _kernel_source_hash() -> str:
 
 def _traffic_per_launch():
     """dram bytes per launch from the committed ncu summary, if taken on this kernel source."""
-    p = os.path.join(ROOT, "profiles", "engine_stack_traffic.json")
+    p = os.path.join(ROOT, "profiles", "engine_stack_traffic.txt")
     if not os.path.exists(p):
         return None
-    j = json.load(open(p))
-    if j.get("kernel_src_sha") != _kernel_source_hash():
+    kv = {}
+    for line in open(p):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("kernel_src_sha") != _kernel_source_hash():
         return None
-    return j.get("dram_bytes_per_launch")
+    v = kv.get("dram_bytes_per_launch_40_layers")
+    return int(v) if v else None
 
 
 class ClockSampler:
@@ -154,6 +159,18 @@ def build_stack(K: int, device, L: int = 40):
         pre.append(1 if l in prerouted else 0)
     torch.cuda.synchronize()
     return B.Stack(B.dims(sh.d, sh.E, sh.F, sh.K), structs, pre, keepalive=layers), sh, L
+
+
+def combine_ranks(ms: float, e2e_ms: float, steps: int, e2e_steps: int, world: int, device=None):
+    """Replicas: every rank ran the same number of steps on its own GPU.  The job's time is
+    the slowest rank's (max over ranks); the job's throughput counts every rank's tokens."""
+    import torch
+    times = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    ms, e2e_ms = float(times[0]), float(times[1])
+    return ms, e2e_ms, world * steps / (ms / 1e3), world * e2e_steps / (e2e_ms / 1e3)
 
 
 def run_ours(args, rank: int, world: int, local_rank: int):
@@ -246,16 +263,11 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         _lib.check(_lib.lib().e0_debug_trace(None, 0))
         np.save(args.trace, np.stack(stamps))
 
-    times = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    ms, e2e_ms = float(times[0]), float(times[1])
+    ms, e2e_ms, tok_s, e2e_tok_s = combine_ranks(ms, e2e_ms, args.steps, e2e_steps, world, dev)
     stack.close()
     if rank != 0:
         return None
 
-    tok_s = world * args.steps / (ms / 1e3)
-    e2e_tok_s = world * e2e_steps / (e2e_ms / 1e3)
     owners, prerouted = stack_schedule(L)
     bpt = algorithmic_bytes_per_token(K=args.k, L=L, heads=len(owners), routers=L - len(prerouted))
     peak, peak_kind = _peaks()
