@@ -205,6 +205,33 @@ e0_status e0_moe_decode_layer(const e0_dims* dims, const e0_experts* routed,
                               size_t workspace_bytes, e0_stream stream);
 
 /* --------------------------------------------------------------------------------
+ * e0_moe_prefill_layer — a chunk of T tokens through one MoE layer (prefill), on the
+ * tcgen05 tensor cores.  "The Other Half of the Memory Wall", §3.1 "Executor paths"
+ * (same expert math as decode), Appendix A "Softmax-topk" (routing), §3.3 (LoRA); the
+ * pages run no prerouter in prefill, so there is no head here.
+ *   Per token t: x = RMSNorm(h_in[t]); ids = top-K of logits[t] (descending, ties to
+ *   the lower id), w = softmax over the selected logits; delta = sum_k w_k E_{ids_k}(x)
+ *   + E_shared(x) + LoRA(x); h_out[t] = bf16(h_in[t] + delta).
+ *   h_in, h_out: bf16 bits [T][d] (16-byte aligned); logits fp32 [T][E].
+ *   delta_f32 fp32 [T][d], ids_out int32 [T][K], weights_out fp32 [T][K]: nullable.
+ *   routed: all E experts resident (slot_of must be NULL); shared, lora nullable; the
+ *   LoRA linear must be d x d.  Shapes: d and 2F multiples of 256, F of 64, E <= 1024,
+ *   K <= 16, T*K <= 65536.
+ *   workspace: caller-owned device memory of e0_prefill_workspace_size(dims, T,
+ *   lora_out) bytes (lora_out = the LoRA output width, 0 without LoRA); its first 256
+ *   bytes carry a device status word readable with e0_get_device_status.
+ *   The products run in fp16 (x and the dequantised weights each rounded once) with
+ *   fp32 accumulation; the routing and the combine run in fp32.
+ * ------------------------------------------------------------------------------ */
+size_t e0_prefill_workspace_size(const e0_dims* dims, int32_t T, int32_t lora_out);
+e0_status e0_moe_prefill_layer(const e0_dims* dims, const e0_experts* routed,
+                               const e0_experts* shared, const e0_qlora* lora,
+                               const uint16_t* h_in, const float* logits, int32_t T,
+                               uint16_t* h_out, float* delta_f32, int32_t* ids_out,
+                               float* weights_out, void* workspace, size_t workspace_bytes,
+                               e0_stream stream);
+
+/* --------------------------------------------------------------------------------
  * e0_moe_decode_layer_noalloc — the same single-token layer-step (T = 1) as
  * e0_moe_decode_layer, for callers that cannot allocate device memory (a host
  * callback or real-time loop that must not enter the allocator, a plugin whose host

@@ -72,6 +72,9 @@ PROTOTYPES = {
                                   vp, vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]),
     "e0_moe_decode_layer_noalloc": (i32, [P(e0_dims), P(e0_experts), P(e0_experts), P(e0_qlora), P(e0_prerouter),
                                           vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
+    "e0_prefill_workspace_size": (sz, [P(e0_dims), i32, i32]),
+    "e0_moe_prefill_layer": (i32, [P(e0_dims), P(e0_experts), P(e0_experts), P(e0_qlora), vp, vp, i32, vp, vp, vp,
+                                   vp, vp, sz, vp]),
     "e0_stack_create": (i32, [P(vp), P(e0_dims), P(e0_layer), i32, vp]),
     "e0_stack_destroy": (None, [vp]),
     "e0_stack_workspace_size": (sz, [vp]),

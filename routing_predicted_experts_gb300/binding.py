@@ -156,6 +156,29 @@ def e0_moe_decode_layer(dm: L.e0_dims, routed: Experts, shared: Optional[Experts
     return {"h_out": h_out, "delta": delta, "next_logits": nl, "next_ids": ni, "next_weights": nw}
 
 
+def e0_prefill_workspace(dm: L.e0_dims, T: int, lora_out: int = 0, device=None) -> torch.Tensor:
+    n = lib().e0_prefill_workspace_size(C.byref(dm), T, lora_out)
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def e0_moe_prefill_layer(dm: L.e0_dims, routed: Experts, shared: Optional[Experts], lora: Optional[QLora],
+                         h_in: torch.Tensor, logits: torch.Tensor, ws: torch.Tensor, want_delta: bool = True,
+                         stream=None):
+    """T tokens (h_in bf16 bits [T][d], logits fp32 [T][E]) through one layer on the tensor cores.
+    Returns dict(h_out, delta, ids, weights)."""
+    T = h_in.shape[0]
+    dev = h_in.device
+    h_out = torch.empty((T, dm.d), dtype=torch.int16, device=dev)
+    delta = torch.empty((T, dm.d), dtype=torch.float32, device=dev) if want_delta else None
+    ids = torch.empty((T, dm.K), dtype=torch.int32, device=dev)
+    w = torch.empty((T, dm.K), dtype=torch.float32, device=dev)
+    r, s_, l_ = routed.c(), (shared.c() if shared else None), (lora.c() if lora else None)
+    check(lib().e0_moe_prefill_layer(C.byref(dm), C.byref(r), C.byref(s_) if s_ else None,
+                                     C.byref(l_) if l_ else None, _p(h_in), _p(logits), T, _p(h_out), _p(delta),
+                                     _p(ids), _p(w), _p(ws), ws.numel(), _stream(stream)))
+    return {"h_out": h_out, "delta": delta, "ids": ids, "weights": w}
+
+
 def e0_prerouter_forward(head: Prerouter, d: int, E: int, K: int, h: torch.Tensor, ids_cur, ids_prev,
                          ws: torch.Tensor, logit_bias=None, stream=None):
     T = h.shape[0] if h.dim() == 2 else 1

@@ -153,4 +153,46 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// ------------------------------------------------------------------ top-K keys
+// Order key of (logit, id): larger logit first, equal logits to the lower id.
+__device__ __forceinline__ uint64_t topk_key(float v, int e) {
+  uint32_t u = __float_as_uint(v);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  if (v != v) u = 0u;
+  return ((uint64_t)u << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)e);
+}
+
+// Top-K of logits held in registers (lane holds z[lane + 32 j], j < NPL), descending,
+// ties to the lower index, with the same key order as warp_topk.  Each round takes the
+// warp maximum of the keys below the previous pick with two integer reductions (high
+// then low word).  Lane k < K receives the k-th id (-1 if none) and its logit.
+__device__ __forceinline__ float topk_key_value(uint32_t hi) {
+  return __uint_as_float((hi & 0x80000000u) ? (hi & 0x7FFFFFFFu) : ~hi);
+}
+template <int NPL>
+__device__ __forceinline__ void warp_topk_regs(const float (&z)[NPL], int E, int K, int lane, int& id, float& val) {
+  uint64_t key[NPL];
+#pragma unroll
+  for (int j = 0; j < NPL; ++j) {
+    const int e = lane + 32 * j;
+    key[j] = e < E ? topk_key(z[j], e) : 0ull;
+  }
+  uint64_t prev = ~0ull;
+  id = -1;
+  val = 0.f;
+  for (int k = 0; k < K; ++k) {
+    uint64_t m = 0ull;
+#pragma unroll
+    for (int j = 0; j < NPL; ++j)
+      if (key[j] < prev && key[j] > m) m = key[j];
+    const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(m >> 32));
+    const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(m >> 32) == hi ? (uint32_t)m : 0u);
+    prev = ((uint64_t)hi << 32) | lo;
+    if (lane == k && prev != 0ull) {
+      id = (int)(0xFFFFFFFFu - lo);
+      val = topk_key_value(hi);
+    }
+  }
+}
+
 }  // namespace e0dev
