@@ -37,7 +37,7 @@ using namespace e0tc;
 namespace e0pf {
 
 constexpr int BM = 128, BN = 256, BK = 64;  // tile: rows x output columns x reduction block
-constexpr int GT = 256;                      // threads per GEMM CTA
+constexpr int GT = 512;                      // threads per GEMM CTA: two per B row
 constexpr int STAGES = 5;                    // raw (A tile + packed B) stages in flight
 constexpr int LOOK = STAGES - 2;             // k-blocks loaded ahead
 constexpr int A_BYTES = BM * BK * 2;         // 16 KB
@@ -86,19 +86,21 @@ struct Tile {
   int m0, rows, n0, slot;
 };
 
-// Dequantise one 64-code row segment (two uint4 of codes) into the swizzled fp16 row.
-__device__ __forceinline__ void dequant_row(const uint8_t* codes, uint8_t* dst_row, int n, __half2 s2, __half2 b2) {
+// Dequantise half of a 64-code row segment (one uint4 = 32 codes, chunks 4h .. 4h + 3
+// of the row) into the swizzled fp16 row.
+__device__ __forceinline__ void dequant_half_row(const uint8_t* codes, uint8_t* dst_row, int n, int h, __half2 s2,
+                                                 __half2 b2) {
   const uint4 w0 = *reinterpret_cast<const uint4*>(codes);
-  const uint4 w1 = *reinterpret_cast<const uint4*>(codes + 16);
-  const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+  const uint32_t words[4] = {w0.x, w0.y, w0.z, w0.w};
   const __half2 magic = __halves2half2(__ushort_as_half((unsigned short)0x6400), __ushort_as_half((unsigned short)0x6400));
 #pragma unroll
-  for (int m = 0; m < 8; ++m) {
+  for (int mm = 0; mm < 4; ++mm) {
+    const int m = 4 * h + mm;
     uint32_t out[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       // codes j and j + 4 of this word as fp16 (1024 + c), then exactly c, then s*c + b
-      const uint32_t t = ((words[m] >> (4 * j)) & 0x000F000Fu) | 0x64006400u;
+      const uint32_t t = ((words[mm] >> (4 * j)) & 0x000F000Fu) | 0x64006400u;
       __half2 c = *reinterpret_cast<const __half2*>(&t);
       c = __hsub2(c, magic);
       const __half2 w = __hfma2(c, s2, b2);
@@ -165,18 +167,24 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
   };
 
   // all threads: issue the copies of job j (tile j / KB, k-block j % KB) into its stage
+  int ld_i = -1;  // tile the loader decoded last
+  Tile ld_T{};
   auto load_job = [&](int j) {
     if (j < jobs) {
-      const Tile T = tile_of(j / KB);
+      if (j / KB != ld_i) {
+        ld_i = j / KB;
+        ld_T = tile_of(ld_i);
+      }
+      const Tile T = ld_T;
       const int kb = j % KB;
       uint8_t* sA = raw + (size_t)(j % STAGES) * RAW_BYTES;
       uint8_t* sBq = sA + A_BYTES;
-#pragma unroll
-      for (int c = tid; c < BM * 8; c += GT) {
+      // rows past the group's end are not loaded: they only feed accumulator rows that
+      // the epilogue discards
+      for (int c = tid; c < T.rows * 8; c += GT) {
         const int r = c >> 3, ch = c & 7;
-        const bool ok = r < T.rows;
-        const __half* src = g.A + (size_t)(T.m0 + (ok ? r : 0)) * g.lda + kb * BK + ch * 8;
-        cp_async16(sA + r * 128 + ((ch ^ (r & 7)) << 4), src, ok ? 16u : 0u);
+        const __half* src = g.A + (size_t)(T.m0 + r) * g.lda + kb * BK + ch * 8;
+        cp_async16(sA + r * 128 + ((ch ^ (r & 7)) << 4), src, 16u);
       }
 #pragma unroll
       for (int c = tid; c < BN * 2; c += GT) {
@@ -206,9 +214,9 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
       if (kb < KB) {
         size_t idx;
         if (LAYOUT == E0_LAYOUT_ROWS)
-          idx = ((size_t)T.slot * g.N + T.n0 + tid) * (g.K / 64) + kb;
+          idx = ((size_t)T.slot * g.N + T.n0 + (tid >> 1)) * (g.K / 64) + kb;
         else
-          idx = ((size_t)T.slot * (g.K / 64) + kb) * g.N + T.n0 + tid;
+          idx = ((size_t)T.slot * (g.K / 64) + kb) * g.N + T.n0 + (tid >> 1);
         ds[u] = __ldg(g.s + idx);
         db[u] = __ldg(g.b + idx);
       }
@@ -251,8 +259,9 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
           sv = cs[q];
           bv = cb[q];
         }
-      const uint8_t* codes = raw + (size_t)(j % STAGES) * RAW_BYTES + A_BYTES + tid * 32;
-      dequant_row(codes, bdq + (size_t)(j & 1) * BD_BYTES + tid * 128, tid, bf16pair_to_h2(sv), bf16pair_to_h2(bv));
+      const int n = tid >> 1, h = tid & 1;
+      const uint8_t* codes = raw + (size_t)(j % STAGES) * RAW_BYTES + A_BYTES + n * 32 + h * 16;
+      dequant_half_row(codes, bdq + (size_t)(j & 1) * BD_BYTES + n * 128, n, h, bf16pair_to_h2(sv), bf16pair_to_h2(bv));
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     fence_before_sync();
@@ -272,12 +281,12 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
       const bool done = wait_bar(&mma_bar[j & 1], (j >> 1) & 1, g);
       fence_after_sync();
       const Tile T = tile_of(j / KB);
-      const int quad = warp & 3, half = warp >> 2;
+      const int quad = warp & 3, cblk = warp >> 2;  // lanes 32 quad.., columns 64 cblk..
       const int r = quad * 32 + lane;
       const bool row_ok = done && r < T.rows;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN / 2; c0 += 32) {
-        const int col = half * (BN / 2) + c0;
+      for (int c0 = 0; c0 < BN / 4; c0 += 32) {
+        const int col = cblk * (BN / 4) + c0;
         uint32_t v[32];
         tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)col, v);
         if (!row_ok) continue;
@@ -287,7 +296,7 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const float gt = __uint_as_float(v[2 * i]), up = __uint_as_float(v[2 * i + 1]);
-            a[i] = gt / (1.0f + expf(-gt)) * up;
+            a[i] = __fdividef(gt, 1.0f + __expf(-gt)) * up;
           }
           __half* dst = g.out16 + (size_t)(T.m0 + r) * g.ldo + (T.n0 + col) / 2;
 #pragma unroll
