@@ -102,12 +102,16 @@ typedef struct {
  *   down:    E0_LAYOUT_COLSLAB, [n][d][F] (i.e. q [n][F/32][d][4], s/b [n][F/64][d]).
  *   n:       experts stored (E for a full stack, 1 for a shared expert, S slots).
  *   slot_of: int16 [E] expert id -> stored index, < 0 = not resident; NULL = identity.
+ *   stride:  bytes between consecutive stored experts in all six tensors (a slot pool
+ *            keeps each expert's six tensors together in one bundle); 0 = each tensor
+ *            packed densely, [n][...].  A multiple of 16.
  */
 typedef struct {
   e0_q4 gate_up;
   e0_q4 down;
   int32_t n;
   const int16_t* slot_of;
+  int64_t stride;
 } e0_experts;
 
 /* Unmerged recovery LoRA linear (§3.3): y = W x + (alpha/r) * B (A x).
@@ -282,11 +286,51 @@ size_t e0_stack_workspace_size(const e0_stack* stack);
  *   attention (h_l = bf16(h_out_{l-1} + incr_l), h_out_{-1} = h0);
  *   h_out: bf16 [d] output of the last layer.
  *   ids_out int32 [L][K], weights_out fp32 [L][K], h_trace bf16 [L][d]: nullable
- *   diagnostics (routing used per layer; each layer's input hidden state). */
+ *   diagnostics (routing used per layer; each layer's input hidden state).
+ *   logit_bias fp32 [2][L][E], nullable: [0][l] is added to layer l's own-gate logits
+ *   at this token, [1][l] to the head logits that commit layer l's routing for the
+ *   next token, before the top-K (a synthetic routing trace is injected this way: a
+ *   large bias on the trace's ids makes the routing pick them). */
 e0_status e0_stack_step(e0_stack* stack, int32_t step, const uint16_t* h0,
                         const uint16_t* incr, uint16_t* h_out, int32_t* ids_out,
-                        float* weights_out, uint16_t* h_trace, void* workspace,
-                        size_t workspace_bytes, e0_stream stream);
+                        float* weights_out, uint16_t* h_trace, const float* logit_bias,
+                        void* workspace, size_t workspace_bytes, e0_stream stream);
+
+/* --------------------------------------------------------------------------------
+ * Bounded HBM expert-slot pool (§3.1, §3.2: experts stay off the GPU and a bounded set
+ * of slots holds the ones the routing needs; the prerouter's one-token lead is the
+ * time to stage them).  Experts live in pinned host memory as one bundle per
+ * (layer, expert): gate/up codes, scales, biases, down codes, scales, biases, at the
+ * offsets e0_expert_bundle_bytes reports (layouts as in e0_experts).  Each layer owns
+ * `slots` bundle slots in HBM, replaced least-recently-used; the experts of the
+ * previous staging of a layer (the running token's) and the ones being staged are
+ * never evicted, so 2K <= slots.
+ * ------------------------------------------------------------------------------ */
+typedef struct e0_slot_pool e0_slot_pool;
+typedef struct {
+  int32_t hits;        /* staged ids already resident */
+  int32_t misses;      /* staged ids copied in */
+  int32_t evictions;   /* misses that replaced a resident expert */
+  int64_t h2d_bytes;   /* bytes copied host -> device */
+} e0_stage_stats;
+
+/* Bytes of one expert bundle for these dims; offsets6 (nullable) receives the byte
+ * offsets of the six tensors inside a bundle. */
+size_t e0_expert_bundle_bytes(const e0_dims* dims, size_t* offsets6);
+/* host_bundles: pinned host memory [layers][E][bundle_bytes], caller-owned, outliving
+ * the pool.  The pool (slots and id -> slot tables) is library-owned. */
+e0_status e0_slot_pool_create(e0_slot_pool** out, const e0_dims* dims, int32_t layers,
+                              int32_t slots, const void* host_bundles, size_t bundle_bytes);
+void e0_slot_pool_destroy(e0_slot_pool* pool);
+/* The device view of a layer's slots, to pass as e0_layer.routed (n = slots, slot_of
+ * the layer's id -> slot table, stride = bundle bytes). */
+e0_status e0_slot_pool_view(const e0_slot_pool* pool, int32_t layer, e0_experts* out);
+/* Make next_ids (HOST int32 [K]) resident in the layer's slots: copies of missing
+ * bundles and the updated id -> slot table are queued on copy_stream, then `ready`
+ * (nullable) is recorded there; launches that use these experts wait on it.  stats
+ * (nullable) is accumulated into. */
+e0_status e0_stage_slots(e0_slot_pool* pool, int32_t layer, const int32_t* next_ids, int32_t K,
+                         e0_stream copy_stream, e0_event ready, e0_stage_stats* stats);
 
 /* --------------------------------------------------------------------------------
  * Input generation (not part of the method): the seeded counter-based generator

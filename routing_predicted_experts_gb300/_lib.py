@@ -36,7 +36,7 @@ class e0_q4(C.Structure):
 
 
 class e0_experts(C.Structure):
-    _fields_ = [("gate_up", e0_q4), ("down", e0_q4), ("n", i32), ("slot_of", vp)]
+    _fields_ = [("gate_up", e0_q4), ("down", e0_q4), ("n", i32), ("slot_of", vp), ("stride", i64)]
 
 
 class e0_qlora(C.Structure):
@@ -50,6 +50,10 @@ class e0_prerouter(C.Structure):
 
 class e0_dims(C.Structure):
     _fields_ = [("d", i32), ("E", i32), ("F", i32), ("K", i32)]
+
+
+class e0_stage_stats(C.Structure):
+    _fields_ = [("hits", i32), ("misses", i32), ("evictions", i32), ("h2d_bytes", i64)]
 
 
 class e0_layer(C.Structure):
@@ -75,10 +79,15 @@ PROTOTYPES = {
     "e0_prefill_workspace_size": (sz, [P(e0_dims), i32, i32]),
     "e0_moe_prefill_layer": (i32, [P(e0_dims), P(e0_experts), P(e0_experts), P(e0_qlora), vp, vp, i32, vp, vp, vp,
                                    vp, vp, sz, vp]),
+    "e0_expert_bundle_bytes": (sz, [P(e0_dims), vp]),
+    "e0_slot_pool_create": (i32, [P(vp), P(e0_dims), i32, i32, vp, sz]),
+    "e0_slot_pool_destroy": (None, [vp]),
+    "e0_slot_pool_view": (i32, [vp, i32, P(e0_experts)]),
+    "e0_stage_slots": (i32, [vp, i32, vp, i32, vp, vp, P(e0_stage_stats)]),
     "e0_stack_create": (i32, [P(vp), P(e0_dims), P(e0_layer), i32, vp]),
     "e0_stack_destroy": (None, [vp]),
     "e0_stack_workspace_size": (sz, [vp]),
-    "e0_stack_step": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+    "e0_stack_step": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
     "e0_synth_normal": (i32, [vp, i64, u64, u32, i64, f64, i32, vp]),
     "e0_debug_inject_stall": (i32, [vp, u64, vp]),
     "e0_debug_trace": (i32, [vp, sz]),

@@ -49,9 +49,10 @@ class Experts:
     down: Q4              # column-slab layout [n][d][F]
     n: int
     slot_of: Optional[torch.Tensor] = None   # int16 [E]
+    stride: int = 0                           # bytes between stored experts (slot bundles); 0 = dense
 
     def c(self) -> L.e0_experts:
-        return L.e0_experts(self.gate_up.c(), self.down.c(), self.n, _p(self.slot_of))
+        return L.e0_experts(self.gate_up.c(), self.down.c(), self.n, _p(self.slot_of), self.stride)
 
 
 @dataclass
@@ -225,9 +226,9 @@ class Stack:
         return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
     def step(self, step: int, h0: torch.Tensor, incr: torch.Tensor, h_out: torch.Tensor, ws: torch.Tensor,
-             ids_out=None, w_out=None, h_trace=None, stream=None) -> None:
+             ids_out=None, w_out=None, h_trace=None, stream=None, logit_bias=None) -> None:
         check(lib().e0_stack_step(self.handle, step, _p(h0), _p(incr), _p(h_out), _p(ids_out), _p(w_out),
-                                  _p(h_trace), _p(ws), ws.numel(), _stream(stream)))
+                                  _p(h_trace), _p(logit_bias), _p(ws), ws.numel(), _stream(stream)))
 
     def close(self):
         if self.handle:
@@ -253,3 +254,67 @@ def e0_layer_struct(routed: Experts, shared: Optional[Experts], lora: Optional[Q
         ly.head = head.c()
     ly.router = _p(router)
     return ly
+
+
+# ------------------------------------------------------------------ slot pool
+def expert_bundle_layout(dm: L.e0_dims):
+    """(bundle bytes, offsets of the six tensors) of one expert bundle."""
+    offs = (C.c_size_t * 6)()
+    total = lib().e0_expert_bundle_bytes(C.byref(dm), C.cast(offs, C.c_void_p))
+    return int(total), [int(o) for o in offs]
+
+
+def host_bundles(dm: L.e0_dims, stacks: list, pin: bool = True) -> torch.Tensor:
+    """Pinned host bundles [len(stacks)][E][bundle] from dense device expert stacks (n == E)."""
+    total, offs = expert_bundle_layout(dm)
+    E = dm.E
+    hb = torch.zeros((len(stacks), E, total), dtype=torch.uint8, pin_memory=pin)
+    for l, ex in enumerate(stacks):
+        parts = [ex.gate_up.q, ex.gate_up.scale, ex.gate_up.bias, ex.down.q, ex.down.scale, ex.down.bias]
+        for off, t in zip(offs, parts):
+            src = t.contiguous().view(torch.uint8).reshape(E, -1)
+            hb[l, :, off:off + src.shape[1]].copy_(src.cpu())
+    return hb
+
+
+class _RawExperts:
+    def __init__(self, st: L.e0_experts):
+        self.st = st
+
+    def c(self) -> L.e0_experts:
+        return self.st
+
+
+class SlotPool:
+    """Owns an e0_slot_pool: per layer, `slots` HBM bundle slots over pinned host bundles."""
+
+    def __init__(self, dm: L.e0_dims, layers: int, slots: int, bundles: torch.Tensor):
+        total, _ = expert_bundle_layout(dm)
+        assert bundles.is_pinned() and bundles.numel() == layers * dm.E * total
+        h = C.c_void_p()
+        check(lib().e0_slot_pool_create(C.byref(h), C.byref(dm), layers, slots, C.c_void_p(bundles.data_ptr()),
+                                        total))
+        self.handle = h
+        self.bundles = bundles
+        self.stats = L.e0_stage_stats()
+
+    def view(self, layer: int) -> _RawExperts:
+        ex = L.e0_experts()
+        check(lib().e0_slot_pool_view(self.handle, layer, C.byref(ex)))
+        return _RawExperts(ex)
+
+    def stage(self, layer: int, ids, copy_stream=None) -> None:
+        arr = (C.c_int32 * len(ids))(*[int(i) for i in ids])
+        check(lib().e0_stage_slots(self.handle, layer, C.cast(arr, C.c_void_p), len(ids), _stream(copy_stream), None,
+                                   C.byref(self.stats)))
+
+    def close(self):
+        if self.handle:
+            lib().e0_slot_pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -247,6 +247,8 @@ e0_status fill_experts(const e0_experts* ex, const e0_dims* dm, bool routed, Lay
     L->dn_q = ex->down.q; L->dn_s = ex->down.scale; L->dn_b = ex->down.bias;
     L->slot_of = ex->slot_of;
     L->n_routed = ex->n;
+    E0_REQUIRE(ex->stride >= 0 && ex->stride % 16 == 0, E0_ERR_INVALID, "expert stride must be a multiple of 16");
+    L->ex_stride = ex->stride;
     E0_REQUIRE(ex->slot_of || ex->n >= dm->E, E0_ERR_INVALID, "routed stack without slot_of must hold all E experts");
   } else {
     L->sgu_q = ex->gate_up.q; L->sgu_s = ex->gate_up.scale; L->sgu_b = ex->gate_up.bias;
@@ -612,7 +614,8 @@ extern "C" size_t e0_stack_workspace_size(const e0_stack* s) {
 
 extern "C" e0_status e0_stack_step(e0_stack* s, int32_t step, const uint16_t* h0, const uint16_t* incr,
                                    uint16_t* h_out, int32_t* ids_out, float* weights_out, uint16_t* h_trace,
-                                   void* workspace, size_t workspace_bytes, e0_stream stream) {
+                                   const float* logit_bias, void* workspace, size_t workspace_bytes,
+                                   e0_stream stream) {
   E0_REQUIRE(s && h0 && h_out, E0_ERR_INVALID, "e0_stack_step: NULL required argument");
   E0_REQUIRE(step >= 0, E0_ERR_INVALID, "step must be >= 0");
   e0_status st = check_ws(&s->dims, s->L, workspace, workspace_bytes);
@@ -635,6 +638,7 @@ extern "C" e0_status e0_stack_step(e0_stack* s, int32_t step, const uint16_t* h0
   P.ids_trace = ids_out;
   P.w_trace = weights_out;
   P.h_trace = h_trace;
+  P.logit_bias = logit_bias;
   P.ws = reinterpret_cast<uint8_t*>(workspace);
   E0_CHECK_CUDA(launch_engine(P, (cudaStream_t)stream));
   return E0_OK;

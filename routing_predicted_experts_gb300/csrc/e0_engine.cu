@@ -477,6 +477,7 @@ __device__ __forceinline__ void self_route_regs(Prod& pr, int l) {
         const uint64_t w = ld_relaxed_u64(z + e);
         have = have && (uint32_t)(w >> 32) == tag;
         zv[j] = __uint_as_float((uint32_t)w);
+        if (P.mode == MODE_STACK && P.logit_bias) zv[j] += P.logit_bias[(size_t)l * P.E + e];
       }
     }
     if (__all_sync(0xffffffffu, have)) break;
@@ -583,15 +584,21 @@ __device__ __forceinline__ void issue_unit(Prod& pr, const LayerDesc& Ld, const 
       if (!pr.ok) return;
       if (shared ? !Ld.has_shared : !((C.rt_valid[l] >> u.k) & 1u)) return;
       const int idx = shared ? 0 : C.rt_idx[l][u.k];
-      const uint32_t* guq = (shared ? Ld.sgu_q : Ld.gu_q) + (size_t)idx * (2 * P.F) * (d / 8);
-      const uint16_t* gus = (shared ? Ld.sgu_s : Ld.gu_s) + (size_t)idx * (2 * P.F) * (d / 64);
-      const uint16_t* gub = (shared ? Ld.sgu_b : Ld.gu_b) + (size_t)idx * (2 * P.F) * (d / 64);
+      // a stored expert: dense per-tensor arrays, or one bundle per slot (slot pools)
+      const int64_t xs = shared ? 0 : Ld.ex_stride;
+      auto at = [&](const auto* base, size_t dense_elems) {
+        return xs ? reinterpret_cast<decltype(base)>(reinterpret_cast<const uint8_t*>(base) + (size_t)idx * xs)
+                  : base + (size_t)idx * dense_elems;
+      };
+      const uint32_t* guq = at(shared ? Ld.sgu_q : Ld.gu_q, (size_t)(2 * P.F) * (d / 8));
+      const uint16_t* gus = at(shared ? Ld.sgu_s : Ld.gu_s, (size_t)(2 * P.F) * (d / 64));
+      const uint16_t* gub = at(shared ? Ld.sgu_b : Ld.gu_b, (size_t)(2 * P.F) * (d / 64));
       const int per = q4_rows_per_stage(d);
       for (int r = 64 * u.r0; r < 64 * u.r0 + 64; r += per)
         issue_q4_rows(pr, guq, gus, gub, d, r, min(per, 64 * u.r0 + 64 - r));
-      const uint32_t* dq = (shared ? Ld.sdn_q : Ld.dn_q) + (size_t)idx * (P.F / 32) * d * 4 + (size_t)u.r0 * d * 4;
-      const uint16_t* ds = (shared ? Ld.sdn_s : Ld.dn_s) + (size_t)idx * (P.F / 64) * d + (size_t)(u.r0 >> 1) * d;
-      const uint16_t* db = (shared ? Ld.sdn_b : Ld.dn_b) + (size_t)idx * (P.F / 64) * d + (size_t)(u.r0 >> 1) * d;
+      const uint32_t* dq = at(shared ? Ld.sdn_q : Ld.dn_q, (size_t)(P.F / 32) * d * 4) + (size_t)u.r0 * d * 4;
+      const uint16_t* ds = at(shared ? Ld.sdn_s : Ld.dn_s, (size_t)(P.F / 64) * d) + (size_t)(u.r0 >> 1) * d;
+      const uint16_t* db = at(shared ? Ld.sdn_b : Ld.dn_b, (size_t)(P.F / 64) * d) + (size_t)(u.r0 >> 1) * d;
       const int pd = dn_rows_per_stage(d);
       for (int i0 = 0; i0 < d; i0 += pd) {
         const int nr = min(pd, d - i0);
@@ -748,7 +755,8 @@ __device__ void router_warp(const EngineParams& P, Ctl& C) {
         }
         const float* z = zhat_ptr(P, pnext3, l - 1);
 #pragma unroll 8
-        for (int e = pr.lane; e < P.E; e += 32) C.zbuf[e] = __ldcg(z + e);
+        for (int e = pr.lane; e < P.E; e += 32)
+          C.zbuf[e] = __ldcg(z + e) + (P.logit_bias ? P.logit_bias[((size_t)P.L + l) * P.E + e] : 0.f);
         __syncwarp();
         int id;
         float w;

@@ -72,6 +72,7 @@ struct LayerDesc {
   const uint16_t* dn_s;
   const uint16_t* dn_b;
   const int16_t* slot_of;
+  int64_t ex_stride;  // bytes between stored routed experts (0: dense per tensor)
   int32_t n_routed;
   int32_t has_shared;
   // shared expert (same layouts, one expert)
