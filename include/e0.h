@@ -331,6 +331,11 @@ e0_status e0_slot_pool_view(const e0_slot_pool* pool, int32_t layer, e0_experts*
  * (nullable) is accumulated into. */
 e0_status e0_stage_slots(e0_slot_pool* pool, int32_t layer, const int32_t* next_ids, int32_t K,
                          e0_stream copy_stream, e0_event ready, e0_stage_stats* stats);
+/* The same for several layers in one call: layers HOST int32 [n_layers] (pool layer
+ * indices), next_ids HOST int32 [n_layers][K]; `ready` is recorded once, after all. */
+e0_status e0_stage_slots_layers(e0_slot_pool* pool, const int32_t* layers, int32_t n_layers,
+                                const int32_t* next_ids, int32_t K, e0_stream copy_stream,
+                                e0_event ready, e0_stage_stats* stats);
 
 /* --------------------------------------------------------------------------------
  * Input generation (not part of the method): the seeded counter-based generator

@@ -84,6 +84,7 @@ PROTOTYPES = {
     "e0_slot_pool_destroy": (None, [vp]),
     "e0_slot_pool_view": (i32, [vp, i32, P(e0_experts)]),
     "e0_stage_slots": (i32, [vp, i32, vp, i32, vp, vp, P(e0_stage_stats)]),
+    "e0_stage_slots_layers": (i32, [vp, vp, i32, vp, i32, vp, vp, P(e0_stage_stats)]),
     "e0_stack_create": (i32, [P(vp), P(e0_dims), P(e0_layer), i32, vp]),
     "e0_stack_destroy": (None, [vp]),
     "e0_stack_workspace_size": (sz, [vp]),

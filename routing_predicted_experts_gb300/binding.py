@@ -308,6 +308,15 @@ class SlotPool:
         check(lib().e0_stage_slots(self.handle, layer, C.cast(arr, C.c_void_p), len(ids), _stream(copy_stream), None,
                                    C.byref(self.stats)))
 
+    def stage_layers(self, layers, ids, copy_stream=None) -> None:
+        """Stage ids [len(layers)][K] (host array) into the given pool layers in one call."""
+        import numpy as np
+        lay = np.ascontiguousarray(np.asarray(layers, dtype=np.int32))
+        arr = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+        check(lib().e0_stage_slots_layers(self.handle, C.c_void_p(lay.ctypes.data), len(lay),
+                                          C.c_void_p(arr.ctypes.data), arr.shape[-1], _stream(copy_stream), None,
+                                          C.byref(self.stats)))
+
     def close(self):
         if self.handle:
             lib().e0_slot_pool_destroy(self.handle)

@@ -135,12 +135,37 @@ extern "C" e0_status e0_slot_pool_view(const e0_slot_pool* p, int32_t layer, e0_
   return E0_OK;
 }
 
+namespace {
+e0_status stage_one(e0_slot_pool* p, int32_t layer, const int32_t* next_ids, int32_t K, cudaStream_t st,
+                    e0_stage_stats* stats);
+}  // namespace
+
 extern "C" e0_status e0_stage_slots(e0_slot_pool* p, int32_t layer, const int32_t* next_ids, int32_t K,
                                     e0_stream copy_stream, e0_event ready, e0_stage_stats* stats) {
   E0_REQUIRE(p && next_ids, E0_ERR_INVALID, "e0_stage_slots: NULL argument");
+  e0_status s = stage_one(p, layer, next_ids, K, (cudaStream_t)copy_stream, stats);
+  if (s != E0_OK) return s;
+  if (ready) E0_CHECK_CUDA(cudaEventRecord((cudaEvent_t)ready, (cudaStream_t)copy_stream));
+  return E0_OK;
+}
+
+extern "C" e0_status e0_stage_slots_layers(e0_slot_pool* p, const int32_t* layers, int32_t n_layers,
+                                           const int32_t* next_ids, int32_t K, e0_stream copy_stream, e0_event ready,
+                                           e0_stage_stats* stats) {
+  E0_REQUIRE(p && layers && next_ids && n_layers >= 0, E0_ERR_INVALID, "e0_stage_slots_layers: NULL argument");
+  for (int i = 0; i < n_layers; ++i) {
+    e0_status s = stage_one(p, layers[i], next_ids + (size_t)i * K, K, (cudaStream_t)copy_stream, stats);
+    if (s != E0_OK) return s;
+  }
+  if (ready) E0_CHECK_CUDA(cudaEventRecord((cudaEvent_t)ready, (cudaStream_t)copy_stream));
+  return E0_OK;
+}
+
+namespace {
+e0_status stage_one(e0_slot_pool* p, int32_t layer, const int32_t* next_ids, int32_t K, cudaStream_t st,
+                    e0_stage_stats* stats) {
   E0_REQUIRE(layer >= 0 && layer < p->L, E0_ERR_INVALID, "e0_stage_slots: layer out of range");
   E0_REQUIRE(K >= 1 && K <= KMAX && 2 * K <= p->S, E0_ERR_SHAPE, "e0_stage_slots: K out of range");
-  cudaStream_t st = (cudaStream_t)copy_stream;
   const int E = p->E, S = p->S;
   int* slot_id = &p->slot_id[(size_t)layer * S];
   int* id_slot = &p->id_slot[(size_t)layer * E];
@@ -212,7 +237,6 @@ extern "C" e0_status e0_stage_slots(e0_slot_pool* p, int32_t layer, const int32_
   int* cw = &p->cur[(size_t)layer * KMAX];
   for (int k = 0; k < K; ++k) cw[k] = next_ids[k];
   p->ncur[layer] = K;
-  if (ready) E0_CHECK_CUDA(cudaEventRecord((cudaEvent_t)ready, st));
   if (stats) {
     stats->hits += s.hits;
     stats->misses += s.misses;
@@ -221,3 +245,4 @@ extern "C" e0_status e0_stage_slots(e0_slot_pool* p, int32_t layer, const int32_
   }
   return E0_OK;
 }
+}  // namespace
