@@ -112,7 +112,8 @@ e0_status build_plan(const PlanSpec& s, int ncta, Unit* units, uint8_t* counts) 
   // 2. divisible work as granules
   std::vector<Granule> gs;
   // the LoRA down projection first: the CTAs that own LoRA base rows wait for its v
-  if (s.lora_ab) gs.push_back({U_LORA_A, 0, s.lr, W_BF16 * 2.0 * d * s.lr});
+  // (its cost adds the latency of publishing v: a CTA of its own, as a rule)
+  if (s.lora_ab) gs.push_back({U_LORA_A, 0, s.lr, W_BF16 * 2.0 * d * s.lr + 2.0 * UNIT_COST});
   if (s.lora)
     for (int r = 0; r < s.lout; r += 16)
       gs.push_back({U_QROWS, r, 16, W_INT4 * 16.0 * q4_row_bytes(d) + W_BF16 * 16.0 * 2.0 * s.lr});

@@ -67,6 +67,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Four phase tests issued back to back (independent, so their latencies overlap); true
+// when all four phases have completed.  Unused slots repeat a barrier already tested.
+__device__ __forceinline__ bool mbar_try_wait4(const uint64_t* b0, uint32_t p0, const uint64_t* b1, uint32_t p1,
+                                               const uint64_t* b2, uint32_t p2, const uint64_t* b3, uint32_t p3) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred q0, q1, q2, q3;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 q2, [%5], %6;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 q3, [%7], %8;\n\t"
+      "and.pred q0, q0, q1;\n\tand.pred q2, q2, q3;\n\tand.pred q0, q0, q2;\n\t"
+      "selp.u32 %0, 1, 0, q0; }"
+      : "=r"(ok)
+      : "r"(smem_u32(b0)), "r"(p0), "r"(smem_u32(b1)), "r"(p1), "r"(smem_u32(b2)), "r"(p2), "r"(smem_u32(b3)),
+        "r"(p3)
+      : "memory");
+  return ok != 0;
+}
+
 // Bulk async copy global -> shared, completion signalled on `bar` (complete_tx).
 // dst, src 16-byte aligned; bytes a positive multiple of 16.
 __device__ __forceinline__ void tma_bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {

@@ -799,9 +799,21 @@ struct Cons {
     const bool timed = P.trace && tid == 0;
     const uint64_t t0 = timed ? globaltimer() : 0;
     bool ok = true;
-    for (int i = 0; i < cnt && ok; ++i) {
-      const uint32_t m = n + i;
-      ok = wait_mbar(P, C, &C.full[m % NSTAGES], (m / NSTAGES) & 1u);
+    // fast path: all the stages have landed (the usual case: the copy warp runs ahead)
+    {
+      const uint64_t* bar[4];
+      uint32_t par[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t m = n + (uint32_t)min(i, cnt - 1);
+        bar[i] = &C.full[m % NSTAGES];
+        par[i] = (m / NSTAGES) & 1u;
+      }
+      if (!mbar_try_wait4(bar[0], par[0], bar[1], par[1], bar[2], par[2], bar[3], par[3]))
+        for (int i = 0; i < cnt && ok; ++i) {
+          const uint32_t m = n + i;
+          ok = wait_mbar(P, C, &C.full[m % NSTAGES], (m / NSTAGES) & 1u);
+        }
     }
     if (timed) {
       t_acq += globaltimer() - t0;
@@ -1259,18 +1271,31 @@ __device__ __forceinline__ void layer_input(Cons& cs, int l, uint32_t par, const
   const float r = xmax > 0.f ? 32767.0f / xmax : 0.f;
   const float inv = xmax > 0.f ? xmax / 32767.0f : 0.f;
   int16_t* xq16 = reinterpret_cast<int16_t*>(C.xq);
+  // independent chunks: codes first, then their stores and sums, so the steps overlap
+  int q[PER], sq[PER];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int v = __float2int_rn(h[k] * scale * r);
+    q[k] = v > 32767 ? 32767 : (v < -32767 ? -32767 : v);
+  }
+  const int j = cs.lane, idx = j & 7;
+  const int pos = (j >> 3) * (DMAX / 32) * 8 + ((idx & 1) ? 4 + (idx >> 1) : (idx >> 1));
 #pragma unroll
   for (int k = 0; k < PER; ++k) {
     const int i = tid + NCT * k;
+    sq[k] = 0;
     if (i < D) {  // warp-uniform: chunks are warp-aligned
-      int q = __float2int_rn(h[k] * scale * r);
-      q = q > 32767 ? 32767 : (q < -32767 ? -32767 : q);
-      const int c = i >> 5, j = cs.lane, idx = j & 7;
-      xq16[((j >> 3) * (DMAX / 32) + c) * 8 + ((idx & 1) ? 4 + (idx >> 1) : (idx >> 1))] = (int16_t)q;
-      const int sq = __reduce_add_sync(0xffffffffu, q);
+      xq16[(i >> 5) * 8 + pos] = (int16_t)q[k];
+      sq[k] = __reduce_add_sync(0xffffffffu, q[k]);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int i = tid + NCT * k;
+    if (i < D) {
       if (cs.lane == 0) {
-        C.xinv[c] = inv;
-        C.xsum[c] = (float)sq * inv;
+        C.xinv[i >> 5] = inv;
+        C.xsum[i >> 5] = (float)sq[k] * inv;
       }
       if (P.mode == MODE_STACK && P.h_trace && blockIdx.x == 0)
         P.h_trace[(size_t)l * D + i] = f32_to_bf16_bits(h[k]);
