@@ -1,6 +1,7 @@
 // Host side of libe0: argument checks, the per-CTA work planner and the C ABI
 // entry points that launch the streaming engine (e0_engine.cu).
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -84,18 +85,115 @@ struct Granule {
 // byte of bf16 rows.
 constexpr double W_INT4 = 1.25;
 constexpr double W_BF16 = 1.0;
+// LoRA base rows measure slower per byte than expert slabs (each CTA also runs their B
+// rows after waiting for v)
+constexpr double W_QROWS = 1.25;
 // Fixed cost of one unit on a CTA, in the same units (bf16 bytes): the fragment load
 // of x, the first stage's wait and the barriers between phases take about as long as
 // streaming 32 KB.  It steers the planner away from giving one CTA several small units.
 constexpr double UNIT_COST = 32768.0;
 
-e0_status build_plan(const PlanSpec& s, int ncta, Unit* units, uint8_t* counts) {
+// Water-fill granules over CTAs [c0, c1): the level T at which the CTAs below it take
+// exactly the granules and one unit cost each, sum_c max(0, T - load[c]) = total +
+// UNIT_COST * n_below (CTAs already above T, e.g. ones with an expert slab heavier than
+// the mean, get nothing more); granules are assigned in order with cumulative
+// capacity, so rounding spreads evenly, and contiguous granules of one type merge.
+void waterfill(const PlanSpec& s, const std::vector<Granule>& gs, int c0, int c1, std::vector<double>& load,
+               std::vector<std::vector<Unit>>& lists) {
+  if (gs.empty() || c1 <= c0) return;
+  double gtotal = 0.0;
+  bool rows_with_b = false;  // LoRA rows bring a second unit (their B rows) to every CTA
+  for (auto& g : gs) {
+    gtotal += g.cost;
+    rows_with_b = rows_with_b || (g.type == U_QROWS && s.lr > 0);
+  }
+  const double per_cta = UNIT_COST * (rows_with_b ? 2.0 : 1.0);
+  double level = 0.0;
+  {
+    std::vector<double> sorted(load.begin() + c0, load.begin() + c1);
+    std::sort(sorted.begin(), sorted.end());
+    const int n = (int)sorted.size();
+    double below = 0.0;  // sum of the loads of the CTAs under the level
+    for (int c = 0; c < n; ++c) {
+      below += sorted[c];
+      const double t = (gtotal + below) / (c + 1) + per_cta;  // level if CTAs 0..c take everything
+      if (c + 1 == n || t <= sorted[c + 1]) {
+        level = t;
+        break;
+      }
+    }
+  }
+  // place granule gr on CTA c (merging with a contiguous unit of its type); its cost
+  auto place = [&](int c, const Granule& gr, bool dry) -> double {
+    auto& L = lists[c];
+    Unit* into = nullptr;
+    for (auto& u : L) {
+      if (u.type == gr.type && u.r1 == gr.row) {
+        // unit size limits: head buffers; the B slice of a LoRA row unit fits one stage
+        const int limit = (gr.type == U_HEAD || gr.type == U_LRES) ? HEAD_ROWS
+                          : gr.type == U_QROWS && s.lr > 0 ? (STAGE_BYTES / (2 * s.lr)) / 16 * 16
+                          : gr.type == U_LORA_A            ? 4
+                                                           : 65535;
+        if ((int)u.r1 - (int)u.r0 + gr.rows <= limit) into = &u;
+        break;
+      }
+    }
+    double cost = gr.cost + (into ? 0.0 : UNIT_COST);
+    bool new_b = false;
+    if (gr.type == U_QROWS && s.lr > 0) {
+      new_b = true;
+      for (auto& u : L)
+        if (u.type == U_LORA_B && u.r1 == gr.row &&
+            (int)u.r1 - (int)u.r0 + gr.rows <= (STAGE_BYTES / (2 * s.lr)) / 16 * 16) {
+          if (!dry) u.r1 = (uint16_t)(gr.row + gr.rows);
+          new_b = false;
+          break;
+        }
+      if (new_b) cost += UNIT_COST;  // waits for v: one more unit's worth of latency
+    }
+    if (dry) return cost;
+    if (into)
+      into->r1 = (uint16_t)(gr.row + gr.rows);
+    else
+      L.push_back(Unit{gr.type, 0, (uint16_t)gr.row, (uint16_t)(gr.row + gr.rows), 0});
+    if (new_b) L.push_back(Unit{U_LORA_B, 0, (uint16_t)gr.row, (uint16_t)(gr.row + gr.rows), 0});
+    load[c] += cost;
+    return cost;
+  };
+  double cum_cap = 0.0, cum_assigned = 0.0;
+  size_t g = 0;
+  for (int c = c0; c < c1 && g < gs.size(); ++c) {
+    cum_cap += std::max(0.0, level - load[c]);
+    while (g < gs.size()) {
+      const double cost = place(c, gs[g], true);
+      if (cum_assigned + 0.5 * cost > cum_cap) break;
+      cum_assigned += place(c, gs[g], false);
+      ++g;
+    }
+  }
+  // what rounding left over goes, one granule at a time, to the least loaded CTA
+  for (; g < gs.size(); ++g) {
+    int best = c0;
+    for (int c = c0 + 1; c < c1; ++c)
+      if (load[c] < load[best]) best = c;
+    place(best, gs[g], false);
+  }
+}
+
+// The work plan of one layer kind: expert slabs round robin, then the divisible work
+// water-filled.  With `defer` (stack layers with a head), the prerouter's work (HEAD,
+// LRES: needed only by the next token) goes to CTAs of its own, [n_crit, ncta), which
+// do not hold up the layer: defer[c] = 1 there, *n_crit_out = n_crit.  The router rows
+// of an own-gate layer go to CTAs [0, crit_limit).
+e0_status build_plan(const PlanSpec& s, int ncta, Unit* units, uint8_t* counts, uint8_t* defer = nullptr,
+                     int* n_crit_out = nullptr, int crit_limit = 0) {
   std::vector<std::vector<Unit>> lists(ncta);
   std::vector<double> load(ncta, 0.0);
   const int d = s.d;
+  const double c_exp = W_INT4 * (64.0 * q4_row_bytes(d) + 20.0 * d) + UNIT_COST;
+  int n_slabs = 0;
   // 1. expert slabs, round robin
   if (s.routed || s.shared) {
-    const double c_exp = W_INT4 * (64.0 * q4_row_bytes(d) + 20.0 * d) + UNIT_COST;
     int idx = 0;
     const int kmax = s.routed ? s.K : 0;
     for (int k = 0; k <= kmax; ++k) {
@@ -108,85 +206,48 @@ e0_status build_plan(const PlanSpec& s, int ncta, Unit* units, uint8_t* counts) 
         }
       }
     }
+    n_slabs = idx;
   }
-  // 2. divisible work as granules
-  std::vector<Granule> gs;
+  // 2. divisible work as granules: the layer's own (crit) and the prerouter's (def)
+  std::vector<Granule> crit, def;
   // the LoRA down projection first: the CTAs that own LoRA base rows wait for its v
   // (its cost adds the latency of publishing v: a CTA of its own, as a rule)
-  if (s.lora_ab) gs.push_back({U_LORA_A, 0, s.lr, W_BF16 * 2.0 * d * s.lr + 2.0 * UNIT_COST});
+  // in slices of 4 ranks on CTAs of their own, so that v is published early
+  if (s.lora_ab)
+    for (int q = 0; q < s.lr; q += 4)
+      crit.push_back({U_LORA_A, q, std::min(4, s.lr - q), W_BF16 * 2.0 * d * std::min(4, s.lr - q) + 4.0 * UNIT_COST});
   if (s.lora)
     for (int r = 0; r < s.lout; r += 16)
-      gs.push_back({U_QROWS, r, 16, W_INT4 * 16.0 * q4_row_bytes(d) + W_BF16 * 16.0 * 2.0 * s.lr});
+      crit.push_back({U_QROWS, r, 16, W_QROWS * 16.0 * q4_row_bytes(d) + W_BF16 * 16.0 * 2.0 * s.lr});
+  if (s.router)
+    for (int e = 0; e < s.E; e += 8) crit.push_back({U_ROUTER, e, 8, W_BF16 * 8.0 * 2.0 * d});
   if (s.lres)
-    for (int e = 0; e < s.E; e += 8) gs.push_back({U_LRES, e, 8, W_BF16 * 8.0 * 2.0 * d});
+    for (int e = 0; e < s.E; e += 8) def.push_back({U_LRES, e, 8, W_BF16 * 8.0 * 2.0 * d});
   if (s.head)
     for (int i = 0; i < s.H; i += 8)
-      gs.push_back({U_HEAD, i, 8, W_BF16 * 8.0 * (2.0 * d + 2.0 * s.E + 2.0 * (1 + 2 * s.K))});
-  if (s.router)
-    for (int e = 0; e < s.E; e += 8) gs.push_back({U_ROUTER, e, 8, W_BF16 * 8.0 * 2.0 * d});
-  double gtotal = 0.0;
-  for (auto& g : gs) gtotal += g.cost;
-  // 3. water-fill: the level T at which the CTAs below it take exactly the granules
-  //    and one unit cost each, sum_c max(0, T - load[c]) = gtotal + UNIT_COST * n_below
-  //    (CTAs already above T, e.g. ones with an expert slab heavier than the mean, get
-  //    nothing more)
-  double level = 0.0;
-  {
-    std::vector<double> sorted(load);
-    std::sort(sorted.begin(), sorted.end());
-    double below = 0.0;  // sum of the loads of the CTAs under the level
-    for (int c = 0; c < ncta; ++c) {
-      below += sorted[c];
-      const double t = (gtotal + below) / (c + 1) + UNIT_COST;  // level if CTAs 0..c take everything
-      if (c + 1 == ncta || t <= sorted[c + 1]) {
-        level = t;
-        break;
-      }
-    }
+      def.push_back({U_HEAD, i, 8, W_BF16 * 8.0 * (2.0 * d + 2.0 * s.E + 2.0 * (1 + 2 * s.K))});
+  // 3. split: enough CTAs beside the expert ones for the layer's own work at the load
+  //    of an expert CTA; the rest take the prerouter's work
+  int n_crit = ncta;
+  if (defer && !def.empty() && n_slabs > 0 && n_slabs < ncta) {
+    double c_crit = 0.0;
+    for (auto& g : crit) c_crit += g.cost;
+    // a CTA of LoRA rows carries two units (rows, then B), an expert CTA one
+    const int n_own = (int)std::ceil(c_crit / std::max(c_exp - 2.0 * UNIT_COST, 1.0));
+    if (n_slabs + n_own <= ncta - 8) n_crit = std::min(ncta, n_slabs + n_own);
   }
-  // assign granules in order with cumulative capacity (rounding spreads evenly)
-  double cum_cap = 0.0, cum_assigned = 0.0;
-  size_t g = 0;
-  for (int c = 0; c < ncta && g < gs.size(); ++c) {
-    cum_cap += std::max(0.0, level - load[c]);
-    const bool last = (c == ncta - 1);
-    while (g < gs.size()) {
-      const Granule& gr = gs[g];
-      auto& L = lists[c];
-      // merge with the previous unit when contiguous and of the same type
-      Unit* into = nullptr;
-      for (auto& u : L) {
-        if (u.type == gr.type && u.r1 == gr.row) {
-          // unit size limits: head buffers; the B slice of a LoRA row unit fits one stage
-          const int limit = (gr.type == U_HEAD || gr.type == U_LRES) ? HEAD_ROWS
-                            : gr.type == U_QROWS && s.lr > 0 ? (STAGE_BYTES / (2 * s.lr)) / 16 * 16
-                                                             : 65535;
-          if ((int)u.r1 - (int)u.r0 + gr.rows <= limit) into = &u;
-          break;
-        }
-      }
-      const double cost = gr.cost + (into ? 0.0 : UNIT_COST);
-      if (!last && cum_assigned + 0.5 * cost > cum_cap) break;
-      if (into)
-        into->r1 = (uint16_t)(gr.row + gr.rows);
-      else
-        L.push_back(Unit{gr.type, 0, (uint16_t)gr.row, (uint16_t)(gr.row + gr.rows), 0});
-      if (gr.type == U_QROWS && s.lr > 0) {
-        // the B rows of the same LoRA rows go with them, as a unit of their own
-        bool merged_b = false;
-        for (auto& u : L)
-          if (u.type == U_LORA_B && u.r1 == gr.row && (int)u.r1 - (int)u.r0 + gr.rows <= (STAGE_BYTES / (2 * s.lr)) / 16 * 16) {
-            u.r1 = (uint16_t)(gr.row + gr.rows);
-            merged_b = true;
-            break;
-          }
-        if (!merged_b) L.push_back(Unit{U_LORA_B, 0, (uint16_t)gr.row, (uint16_t)(gr.row + gr.rows), 0});
-      }
-      load[c] += cost;
-      cum_assigned += cost;
-      ++g;
-    }
+  const int limit = crit_limit > 0 ? std::min(crit_limit, ncta) : ncta;
+  if (n_crit < ncta) {
+    waterfill(s, crit, 0, n_crit, load, lists);
+    waterfill(s, def, n_crit, ncta, load, lists);
+  } else {
+    std::vector<Granule> all(crit);
+    all.insert(all.end(), def.begin(), def.end());
+    waterfill(s, all, 0, limit, load, lists);
   }
+  if (defer)
+    for (int c = 0; c < ncta; ++c) defer[c] = c >= n_crit ? 1 : 0;
+  if (n_crit_out) *n_crit_out = n_crit;
   // 4. order: id-independent work first, experts last.  U_LORA_A must precede U_LORA_B
   //    on a CTA that has both (B waits for the v that A publishes); B goes late so that
   //    v is normally there by the time it is needed.
@@ -299,6 +360,7 @@ void base_params(EngineParams& P, int d, int E, int F, int K, int L, int ncta, i
   std::memset(&P, 0, sizeof(P));
   P.d = d; P.E = E; P.F = F; P.K = K; P.L = L; P.ncta = ncta; P.mode = mode;
   P.norm = 1; P.out_dim = d; P.kinds = 1;
+  for (int k = 0; k < KINDS_MAX; ++k) P.n_arrive[k] = ncta;
   P.timeout_ns = DEFAULT_TIMEOUT_NS;
   P.wl = ws_layout(E, L);
   P.trace = g_trace;
@@ -509,6 +571,8 @@ struct e0_stack {
   LayerDesc* d_layers = nullptr;
   Unit* d_plan = nullptr;
   uint8_t* d_counts = nullptr;
+  uint8_t* d_defer = nullptr;   // [KINDS_MAX][ncta]: CTAs that only hold prerouter work
+  int n_defer[KINDS_MAX] = {};
 };
 
 extern "C" e0_status e0_stack_create(e0_stack** out, const e0_dims* dims, const e0_layer* layers, int32_t L,
@@ -571,13 +635,20 @@ extern "C" e0_status e0_stack_create(e0_stack** out, const e0_dims* dims, const 
   rs.d = dims->d; rs.E = dims->E; rs.F = dims->F; rs.K = dims->K; rs.router = true;
   std::vector<Unit> units((size_t)KINDS_MAX * ncta * MAXU);
   std::vector<uint8_t> counts((size_t)KINDS_MAX * ncta, 0);
+  std::vector<uint8_t> defer((size_t)KINDS_MAX * ncta, 0);
+  // layers with a head: the prerouter's work on CTAs of its own (deferred, see build_plan)
+  int n_crit = ncta;
   for (int k = 0; k < 2; ++k)
     if (have_spec[k]) {
-      st = build_plan(spec[k], ncta, units.data() + (size_t)k * ncta * MAXU, counts.data() + (size_t)k * ncta);
+      int nc = ncta;
+      st = build_plan(spec[k], ncta, units.data() + (size_t)k * ncta * MAXU, counts.data() + (size_t)k * ncta,
+                      k == KIND_MAIN ? defer.data() + (size_t)k * ncta : nullptr, &nc);
       if (st) return st;
+      n_crit = std::min(n_crit, nc);
     }
+  // the router rows of own-gate layers stay off the deferred CTAs
   st = build_plan(rs, ncta, units.data() + (size_t)KIND_ROUTER * ncta * MAXU,
-                  counts.data() + (size_t)KIND_ROUTER * ncta);
+                  counts.data() + (size_t)KIND_ROUTER * ncta, nullptr, nullptr, n_crit);
   if (st) return st;
 
   e0_stack* s = new e0_stack();
@@ -586,9 +657,16 @@ extern "C" e0_status e0_stack_create(e0_stack** out, const e0_dims* dims, const 
   s->ncta = ncta;
   s->prerouted.assign(L, 0);
   for (int l = 0; l < L; ++l) s->prerouted[l] = descs[l].prerouted ? 1 : 0;
+  for (int k = 0; k < KINDS_MAX; ++k) {
+    int nd = 0;
+    for (int c = 0; c < ncta; ++c) nd += defer[(size_t)k * ncta + c];
+    s->n_defer[k] = nd;
+  }
   cudaError_t e = cudaMalloc(&s->d_layers, sizeof(LayerDesc) * L);
   if (e == cudaSuccess) e = cudaMalloc(&s->d_plan, sizeof(Unit) * units.size());
   if (e == cudaSuccess) e = cudaMalloc(&s->d_counts, counts.size());
+  if (e == cudaSuccess) e = cudaMalloc(&s->d_defer, defer.size());
+  if (e == cudaSuccess) e = cudaMemcpy(s->d_defer, defer.data(), defer.size(), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(s->d_layers, descs.data(), sizeof(LayerDesc) * L, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(s->d_plan, units.data(), sizeof(Unit) * units.size(), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(s->d_counts, counts.data(), counts.size(), cudaMemcpyHostToDevice);
@@ -605,6 +683,7 @@ extern "C" void e0_stack_destroy(e0_stack* s) {
   if (s->d_layers) cudaFree(s->d_layers);
   if (s->d_plan) cudaFree(s->d_plan);
   if (s->d_counts) cudaFree(s->d_counts);
+  if (s->d_defer) cudaFree(s->d_defer);
   delete s;
 }
 
@@ -627,6 +706,11 @@ extern "C" e0_status e0_stack_step(e0_stack* s, int32_t step, const uint16_t* h0
   P.layers = s->d_layers;
   P.plan = s->d_plan;
   P.plan_n = s->d_counts;
+  P.defer = s->d_defer;
+  for (int k = 0; k < KINDS_MAX; ++k) {
+    P.n_defer[k] = s->n_defer[k];
+    P.n_arrive[k] = s->ncta - s->n_defer[k];
+  }
   P.kinds = KINDS_MAX;
   P.step = step;
   uint64_t mask = 0;

@@ -43,6 +43,7 @@ struct Ctl {
   int32_t is_last;
   uint32_t epoch;
   Unit su[KINDS_MAX][MAXU];   // this CTA's work units per plan kind
+  uint8_t defer[KINDS_MAX];   // per plan kind: this CTA holds only prerouter work
   int32_t sn[KINDS_MAX];
   uint32_t rt_tag[LMAX];      // staged: epoch each committed route is for
 };
@@ -448,11 +449,11 @@ __device__ __forceinline__ bool prod_keep_waiting(Prod& pr, uint64_t t0, uint32_
 }
 
 // Wait (bounded) until counter `which` of layer l has every CTA's arrival.
-__device__ __forceinline__ bool prod_wait_counter(Prod& pr, int l, int which) {
+__device__ __forceinline__ bool prod_wait_counter(Prod& pr, int l, int which, uint32_t target) {
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     bool r = false;
-    if (pr.lane == 0) r = ld_acquire_u32(ctr(pr.P, pr.par, l, which)) >= (uint32_t)pr.P.ncta;
+    if (pr.lane == 0) r = ld_acquire_u32(ctr(pr.P, pr.par, l, which)) >= target;
     if (__shfl_sync(0xffffffffu, r ? 1 : 0, 0)) return true;
     if (!prod_keep_waiting(pr, t0, it)) return false;
   }
@@ -749,7 +750,11 @@ __device__ void router_warp(const EngineParams& P, Ctl& C) {
         if (P.w_trace) P.w_trace[l * P.K + pr.lane] = C.rt_w[l][pr.lane];
       }
       if (layer_at(P, l).prerouted && l > 0) {
-        if (!prod_wait_counter(pr, l - 1, 0)) {
+        // head l-1 done: on its own counter when that work runs on deferred CTAs
+        const int hk = layer_at(P, l - 1).plan_kind;
+        const bool on_head = P.plan && P.n_defer[hk] > 0;
+        if (!prod_wait_counter(pr, l - 1, on_head ? 1 : 0,
+                               (uint32_t)(on_head ? P.n_defer[hk] : (P.plan ? P.n_arrive[hk] : P.ncta)))) {
           pr.ok = false;
           break;
         }
@@ -1334,7 +1339,8 @@ __device__ void consumer(const EngineParams& P, Ctl& C, uint8_t* ring) {
     }
     if (l > 0 && P.mode == MODE_STACK) {
       if (tid == 0)
-        wait_count(P, C, ctr(P, par, l - 1, 0), (uint32_t)ncta);
+        wait_count(P, C, ctr(P, par, l - 1, 0),
+                   (uint32_t)(P.plan ? P.n_arrive[layer_at(P, l - 1).plan_kind] : ncta));
       cbar();
     }
     if (tid == 0) stamp(P, l, 1);
@@ -1389,9 +1395,14 @@ __device__ void consumer(const EngineParams& P, Ctl& C, uint8_t* ring) {
     cbar();
     if (tid == 0) {
       // the bar.sync above orders every consumer thread's reductions before this release
-      if (l == P.L - 1) {
+      const int kind = P.plan ? Ld.plan_kind : 0;
+      if (P.plan && C.defer[kind]) {
+        // prerouter work only: the next layer does not wait for it, the commit does
+        red_release_add_u32(ctr(P, par, l, 1), 1u);
+        if (l == P.L - 1) C.is_last = 0;
+      } else if (l == P.L - 1) {
         const uint32_t old = atom_acq_rel_add_u32(ctr(P, par, l, 0), 1u);
-        C.is_last = (old == (uint32_t)ncta - 1u);
+        C.is_last = (old == (uint32_t)(P.plan ? P.n_arrive[kind] : ncta) - 1u);
       } else {
         red_release_add_u32(ctr(P, par, l, 0), 1u);
       }
@@ -1466,7 +1477,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) engine_kernel(const __grid_consta
       if (P.plan) {
         if (kind < P.kinds) {
           C.su[kind][u] = P.plan[((size_t)kind * P.ncta + blockIdx.x) * MAXU + u];
-          if (u == 0) C.sn[kind] = P.plan_n[kind * P.ncta + blockIdx.x];
+          if (u == 0) {
+            C.sn[kind] = P.plan_n[kind * P.ncta + blockIdx.x];
+            C.defer[kind] = P.defer ? P.defer[kind * P.ncta + blockIdx.x] : 0;
+          }
         }
       } else if (kind == 0) {
         C.su[0][u] = P.inline_plan[(size_t)blockIdx.x * MAXU + u];

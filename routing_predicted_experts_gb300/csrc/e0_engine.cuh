@@ -161,6 +161,10 @@ struct EngineParams {
   const LayerDesc* layers;     // stack: device array [L]; else nullptr (inline_layer)
   const Unit* plan;            // stack: device [kinds][ncta][MAXU]; else nullptr (inline)
   const uint8_t* plan_n;       // stack: device [kinds][ncta]
+  const uint8_t* defer;        // stack: device [kinds][ncta], 1 = the CTA holds only prerouter work
+                               // of that kind: it arrives on the head counter, not the layer's
+  int32_t n_arrive[KINDS_MAX]; // CTAs arriving on a layer's counter, per plan kind
+  int32_t n_defer[KINDS_MAX];  // CTAs arriving on its head counter instead
   // inputs
   const uint16_t* h_in;
   const uint16_t* incr;
