@@ -155,7 +155,8 @@ __device__ __forceinline__ void cbar() { named_bar_sync(1, NCT); }
 // Diagnostics: stamp %globaltimer into trace[cta][l][slot] when a trace buffer is set.
 // Slots: 0 consumer layer start, 1 dependency satisfied, 2 layer input built,
 // 3 units done, 4 producer route published, 5 producer issued the layer's last stage,
-// 6 ns warp 0 waited for stages, 7 stages it took, 8 + unit type: ns in that unit type.
+// 6 ns warp 0 waited for stages, 7 stages it took, 8 routing warp began the layer's own-
+// gate routing, 8 + unit type (types >= 1): ns in that unit type.
 __device__ __forceinline__ void stamp(const EngineParams& P, int l, int slot) {
   if (P.trace) P.trace[((size_t)blockIdx.x * P.L + l) * 16 + slot] = globaltimer();
 }
@@ -302,6 +303,18 @@ __device__ __forceinline__ void publish_route(Prod& pr, int l, int id, float w) 
     C.rt_w[l][lane] = (v && tot > 0.f) ? wv / tot : 0.f;
   }
   if (lane == 0) C.rt_valid[l] = valid;
+  if (P.mode == MODE_STACK && Ld.has_head) {
+    // the previous-token ids this layer's head one-hots (staged at launch): valid ones
+    bool pv = false;
+    if (lane < K) {
+      const int pid = C.rt_prev[l][lane];
+      pv = pid >= 0 && pid < P.E;
+      for (int j = 0; j < lane; ++j)
+        if (C.rt_prev[l][j] == pid) pv = false;
+    }
+    const uint32_t pvalid = __ballot_sync(0xffffffffu, pv);
+    if (lane == 0) C.rt_pvalid[l] = pvalid;
+  }
   __syncwarp();
   if (lane == 0) {
     __threadfence_block();
@@ -404,18 +417,8 @@ __device__ __forceinline__ void load_routes(Prod& pr) {
     if (lane + 32 < L) C.rt_tag[lane + 32] = t1;
   }
   __syncwarp();
-  for (int l = 0; l < L; ++l) {
-    bool pv = false;
-    if (lane < K) {
-      const int pid = C.rt_prev[l][lane];
-      pv = pid >= 0 && pid < P.E;
-      for (int j = 0; j < lane; ++j)
-        if (C.rt_prev[l][j] == pid) pv = false;
-    }
-    const uint32_t pvalid = __ballot_sync(0xffffffffu, pv);
-    if (lane == 0) C.rt_pvalid[l] = pvalid;
-  }
-  __syncwarp();
+  // (the previous-token validity of each head's layer is settled when its route is
+  // published: publish_route)
 }
 
 // Publish the staged route of a prerouted layer (committed by the previous launch).
@@ -498,6 +501,7 @@ __device__ __forceinline__ void self_route_regs(Prod& pr, int l) {
 // is published (tagged words, see st_tagged), then publish their top-K (routing warp).
 __device__ __forceinline__ void compute_self_route(Prod& pr, int l) {
   if (!pr.ok || pr.C.rt_ready[l]) return;
+  if (pr.lane == 0) stamp(pr.P, l, 8);
   if (pr.P.E <= 256)
     self_route_regs<8>(pr, l);
   else if (pr.P.E <= 512)
@@ -722,9 +726,12 @@ __device__ void producer(const EngineParams& P, Ctl& C, uint8_t* ring) {
 // complete) and, in the stack, the bookkeeping for the next token.
 __device__ void router_warp(const EngineParams& P, Ctl& C) {
   Prod pr{P, C, nullptr, 0u, true, (int)(threadIdx.x & 31), C.epoch & 1u, C.epoch % 3u, C.epoch};
-  // The first layer's own route is needed first: compute it before staging the rest
-  // (a layer with a head also needs its previous-token ids, staged below).
-  if (P.mode == MODE_STACK && self_routes(P, 0) && !layer_at(P, 0).has_head) compute_self_route(pr, 0);
+  // The leading layers that route with their own gate and have no head need nothing
+  // from the staged routes: publish theirs first and stage the rest afterwards (the
+  // staging takes several microseconds; a head's layer needs its previous-token ids).
+  if (P.mode == MODE_STACK)
+    for (int l = 0; l < P.L && pr.ok && self_routes(P, l) && !layer_at(P, l).has_head; ++l)
+      compute_self_route(pr, l);
   load_routes(pr);
   if (P.mode == MODE_STACK)
     for (int l = 0; l < P.L && pr.ok; ++l) {
