@@ -75,8 +75,8 @@ __device__ __forceinline__ WsHeader* hdr(const EngineParams& P) { return reinter
 __device__ __forceinline__ uint32_t* ctr(const EngineParams& P, uint32_t par, int l, int which) {
   return reinterpret_cast<uint32_t*>(P.ws + P.wl.counters) + ((size_t)par * P.L + l) * 4 + which;
 }
-__device__ __forceinline__ float* lv_ptr(const EngineParams& P, uint32_t par, int l) {
-  return reinterpret_cast<float*>(P.ws + P.wl.lv) + ((size_t)par * P.L + l) * RANKS_MAX;
+__device__ __forceinline__ uint64_t* lv_ptr(const EngineParams& P, uint32_t par, int l) {
+  return reinterpret_cast<uint64_t*>(P.ws + P.wl.lv) + ((size_t)par * P.L + l) * RANKS_MAX;
 }
 __device__ __forceinline__ float* acc_ptr(const EngineParams& P, uint32_t par, int l) {
   return reinterpret_cast<float*>(P.ws + P.wl.acc) + ((size_t)par * P.L + l) * OUTMAX;
@@ -1138,11 +1138,45 @@ __device__ __forceinline__ void consume_unit(Cons& cs, const LayerDesc& Ld, cons
       consume_q4_part<D, false>(cs, u.r1 - u.r0, nullptr, acc, u.r0);
       break;
     case U_LORA_B: {
-      // (alpha/r) B v for rows [r0, r1), once every rank of v is published
+      // (alpha/r) B v for rows [r0, r1), once every rank of v is published: warp 0
+      // polls the launch-tagged words of v (one round trip when they are there)
       const uint32_t par = C.epoch & 1u;
-      if (tid == 0) wait_count(P, C, ctr(P, par, l, 2), (uint32_t)Ld.lr);
-      cbar();
-      if (tid < Ld.lr) C.lvs[tid] = __ldcg(lv_ptr(P, par, l) + tid);
+      if (cs.cw == 0) {
+        const uint64_t* lvp = lv_ptr(P, par, l);
+        const uint32_t tag = C.epoch + 1u;
+        const uint64_t t0 = globaltimer();
+        for (uint32_t it = 1;; ++it) {
+          bool have = true;
+          float v0 = 0.f, v1 = 0.f;
+          if (cs.lane < Ld.lr) {
+            const uint64_t w = ld_relaxed_u64(lvp + cs.lane);
+            have = (uint32_t)(w >> 32) == tag;
+            v0 = __uint_as_float((uint32_t)w);
+          }
+          if (cs.lane + 32 < Ld.lr) {
+            const uint64_t w = ld_relaxed_u64(lvp + cs.lane + 32);
+            have = have && (uint32_t)(w >> 32) == tag;
+            v1 = __uint_as_float((uint32_t)w);
+          }
+          if (__all_sync(0xffffffffu, have)) {
+            if (cs.lane < Ld.lr) C.lvs[cs.lane] = v0;
+            if (cs.lane + 32 < Ld.lr) C.lvs[cs.lane + 32] = v1;
+            break;
+          }
+          if ((it & 15u) == 0) {
+            int stop = 0;
+            if (cs.lane == 0) {
+              if (aborted(P, C)) {
+                stop = 1;
+              } else if (globaltimer() - t0 > P.timeout_ns) {
+                raise_error(P, C, E0_DEV_TIMEOUT);
+                stop = 1;
+              }
+            }
+            if (__shfl_sync(0xffffffffu, stop, 0)) break;
+          }
+        }
+      }
       cbar();
       const int nr = u.r1 - u.r0;
       if (cs.acquire(1)) {
@@ -1163,14 +1197,10 @@ __device__ __forceinline__ void consume_unit(Cons& cs, const LayerDesc& Ld, cons
     }
     case U_LORA_A: {
       // v = A x for ranks [r0, r1), published for the CTAs that own the B rows
+      // (each rank's value goes out as a launch-tagged word: no counter, no fence)
       const uint32_t par = C.epoch & 1u;
       const int n = u.r1 - u.r0;
-      cbar();  // vbuf reuse
-      consume_bf_rows<D>(cs, n, BF_SMEM, C.vbuf, nullptr);
-      cbar();
-      if (tid < n) lv_ptr(P, par, l)[u.r0 + tid] = C.vbuf[tid];
-      cbar();  // orders every thread's store before the release below
-      if (tid == 0) red_release_add_u32(ctr(P, par, l, 2), (uint32_t)n);
+      consume_bf_rows<D>(cs, n, BF_TAGGED, reinterpret_cast<float*>(lv_ptr(P, par, l) + u.r0), nullptr);
       break;
     }
     case U_HEAD: {

@@ -121,7 +121,7 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 64, "header size");
 
 struct WsLayout {
-  size_t counters;   // u32 [2][L][4]: layer done, own gate done, LoRA v published
+  size_t counters;   // u32 [2][L][4]: layer done, prerouter work done (deferred CTAs), spare
   size_t acc;        // f32 [2][L][OUTMAX]
   size_t zhat;       // f32 [3][L][E]
   size_t zr;         // u64 [2][L][E]  own-gate logits, tagged with the launch (see st_tagged)
@@ -130,7 +130,7 @@ struct WsLayout {
   size_t rg_ids;     // i32 [2][L][KMAX] routes committed for the next launch
   size_t rg_w;       // f32 [2][L][KMAX]
   size_t rg_tag;     // u32 [2][L]  epoch the route is for
-  size_t lv;         // f32 [2][L][RANKS_MAX]  LoRA v = A x
+  size_t lv;         // u64 [2][L][RANKS_MAX]  LoRA v = A x, tagged with the launch
   size_t total;
 };
 
@@ -148,7 +148,7 @@ __host__ __device__ inline WsLayout ws_layout(int E, int L) {
   w.rg_ids = o;   o = ws_align(o + sizeof(int32_t) * 2 * (size_t)L * KMAX);
   w.rg_w = o;     o = ws_align(o + sizeof(float) * 2 * (size_t)L * KMAX);
   w.rg_tag = o;   o = ws_align(o + sizeof(uint32_t) * 2 * (size_t)L);
-  w.lv = o;       o = ws_align(o + sizeof(float) * 2 * (size_t)L * RANKS_MAX);
+  w.lv = o;       o = ws_align(o + sizeof(uint64_t) * 2 * (size_t)L * RANKS_MAX);
   w.total = o;
   return w;
 }
