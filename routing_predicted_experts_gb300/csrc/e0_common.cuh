@@ -67,6 +67,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Phase test that lets the hardware suspend the thread until the phase completes or
+// about `hint_ns` pass (no busy issue slots while a warp waits).
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Four phase tests issued back to back (independent, so their latencies overlap); true
 // when all four phases have completed.  Unused slots repeat a barrier already tested.
 __device__ __forceinline__ bool mbar_try_wait4(const uint64_t* b0, uint32_t p0, const uint64_t* b1, uint32_t p1,

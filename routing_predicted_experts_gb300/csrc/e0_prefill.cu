@@ -36,28 +36,34 @@ using namespace e0tc;
 
 namespace e0pf {
 
-constexpr int BM = 128, BN = 256, BK = 64;  // tile: rows x output columns x reduction block
-constexpr int GT = 512;                      // threads per GEMM CTA: two per B row
-constexpr int STAGES = 5;                    // raw (A tile + packed B) stages in flight
-constexpr int LOOK = STAGES - 2;             // k-blocks loaded ahead
-constexpr int A_BYTES = BM * BK * 2;         // 16 KB
-constexpr int BQ_BYTES = BN * BK / 2;        // 8 KB of int4 codes
-constexpr int RAW_BYTES = A_BYTES + BQ_BYTES;
-constexpr int BD_BYTES = BN * BK * 2;        // 32 KB of dequantised fp16 B
+constexpr int WM = 128;                      // weight rows per tile: the MMA's M
+constexpr int TT = 64;                       // token rows per tile, at most: the MMA's N
+constexpr int BK = 64;                       // reduction block
+constexpr int STAGES = 12;                   // copy stages in flight (48 KB of codes)
+constexpr int X_BYTES = TT * BK * 2;         // 8 KB of fp16 token rows
+constexpr int Q_BYTES = WM * BK / 2;         // 4 KB of int4 codes
+constexpr int RAW_BYTES = X_BYTES + Q_BYTES;
+constexpr int WD_BYTES = WM * BK * 2;        // 16 KB of dequantised fp16 weights
 constexpr int EMAXP = 1024;
-constexpr size_t GEMM_SMEM = 1024 + (size_t)STAGES * RAW_BYTES + 2 * BD_BYTES + 2 * (EMAXP + 1) * sizeof(int);
-static_assert(RAW_BYTES % 1024 == 0, "stages stay 1024-byte aligned");
+// roles: warp 0 copies, warps 1..8 dequantise, warp 9 issues the MMAs, warps 10..13 run
+// the epilogue (tensor-memory lane quadrants 2, 3, 0, 1)
+constexpr int W_COPY = 0, W_DQ0 = 1, N_DQ = 8, W_MMA = 9, W_EPI0 = 10, N_EPI = 4;
+constexpr int GT = 32 * (W_EPI0 + N_EPI);
+constexpr size_t GEMM_SMEM = 1024 + (size_t)STAGES * RAW_BYTES + 2 * WD_BYTES + 2 * (EMAXP + 1) * sizeof(int);
+static_assert(X_BYTES % 1024 == 0 && RAW_BYTES % 1024 == 0, "stages stay 1024-byte aligned");
+static_assert(2 * TT >= 32 && (2 * TT & (2 * TT - 1)) == 0, "tensor memory columns: a power of two >= 32");
 static_assert(GEMM_SMEM <= 227 * 1024, "shared memory");
+static_assert(N_DQ * 32 == 2 * WM, "two dequantising threads per weight row");
 
 enum Epi : int { EPI_SWIGLU = 0, EPI_F32 = 1 };
 
 struct GemmArgs {
-  const __half* A;        // [rows][K] fp16, reduction index permuted within groups of 8
+  const __half* A;        // token rows [rows][K] fp16, reduction index permuted within groups of 8
   int lda;
-  int K, N;               // reduction length (multiple of 64), outputs per group (multiple of 256)
+  int K, N;               // reduction length (multiple of 64), outputs per group (multiple of 128)
   int ngroups;
   const int* row_off;     // [ngroups + 1] rows of group g: [row_off[g], row_off[g + 1])
-  const int* tile_off;    // [ngroups + 1] prefix sums of ceil(rows_g / BM)
+  const int* tile_off;    // [ngroups + 1] prefix sums of ceil(rows_g / TT)
   const uint32_t* q;      // int4 codes of all groups (group g = weight slot g)
   const uint16_t* s;      // bf16 scales
   const uint16_t* b;      // bf16 biases
@@ -69,25 +75,18 @@ struct GemmArgs {
   uint64_t timeout_ns;
 };
 
-// Bounded wait on an mbarrier phase; false (and a device status bit) if it runs out.
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const GemmArgs& g) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0 && globaltimer() - t0 > g.timeout_ns) {
-      atomicOr(g.status, (uint32_t)E0_DEV_TIMEOUT);
-      return false;
-    }
-  }
-}
-
 struct Tile {
   int m0, rows, n0, slot;
 };
 
-// Dequantise half of a 64-code row segment (one uint4 = 32 codes, chunks 4h .. 4h + 3
-// of the row) into the swizzled fp16 row.
+__device__ __forceinline__ __half2 bf16pair_to_h2(uint16_t v) {
+  const __half h = __float2half_rn(__uint_as_float((uint32_t)v << 16));
+  return __halves2half2(h, h);
+}
+
+// Dequantise half of a 64-code weight row segment (one uint4 = 32 codes, chunks
+// 4h .. 4h + 3 of the row) into the swizzled fp16 row: codes j and j + 4 of each word
+// become an fp16 pair (1024 + c by the exponent trick, then exactly c, then s*c + b).
 __device__ __forceinline__ void dequant_half_row(const uint8_t* codes, uint8_t* dst_row, int n, int h, __half2 s2,
                                                  __half2 b2) {
   const uint4 w0 = *reinterpret_cast<const uint4*>(codes);
@@ -99,7 +98,6 @@ __device__ __forceinline__ void dequant_half_row(const uint8_t* codes, uint8_t* 
     uint32_t out[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      // codes j and j + 4 of this word as fp16 (1024 + c), then exactly c, then s*c + b
       const uint32_t t = ((words[mm] >> (4 * j)) & 0x000F000Fu) | 0x64006400u;
       __half2 c = *reinterpret_cast<const __half2*>(&t);
       c = __hsub2(c, magic);
@@ -110,225 +108,255 @@ __device__ __forceinline__ void dequant_half_row(const uint8_t* codes, uint8_t* 
   }
 }
 
-__device__ __forceinline__ __half2 bf16pair_to_h2(uint16_t v) {
-  const __half h = __float2half_rn(__uint_as_float((uint32_t)v << 16));
-  return __halves2half2(h, h);
+__device__ __forceinline__ void cp_async_bar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Grouped GEMM out[rows][n] = sum_k x[row][k] W_g[n][k] with the operands swapped for
+// the tensor core: the weight tile (128 rows, dequantised to fp16 in shared memory) is
+// the MMA's A and the group's token rows (up to 64, rounded up to 16) its B, so a
+// group of few tokens costs few MMA columns.  The accumulator [weight row][token]
+// lives in tensor memory, double-buffered so the epilogue of one tile overlaps the
+// next tile's MMAs.  Copy, dequantisation, MMA and epilogue run in their own warps,
+// handing stages over through mbarriers; every wait is bounded.
 template <int LAYOUT, int EPI>
 __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ GemmArgs g) {
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
-  uint8_t* raw = sm;                               // STAGES x [A tile | packed B]
-  uint8_t* bdq = sm + (size_t)STAGES * RAW_BYTES;  // 2 x dequantised B
-  int* s_row = reinterpret_cast<int*>(bdq + 2 * BD_BYTES);
+  uint8_t* raw = sm;                                // STAGES x [token rows | codes]
+  uint8_t* wdq = sm + (size_t)STAGES * RAW_BYTES;   // 2 x dequantised weights
+  int* s_row = reinterpret_cast<int*>(wdq + 2 * WD_BYTES);
   int* s_tile = s_row + (EMAXP + 1);
-  __shared__ __align__(8) uint64_t mma_bar[2];
+  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], wd_full[2], wd_empty[2], acc_full[2], acc_empty[2], fin;
   __shared__ uint32_t tmem_slot;
-  __shared__ int s_abort;
+  __shared__ volatile int s_abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int NT = g.N / BN, KB = g.K / BK;
+  const int WT = g.N / WM, KB = g.K / BK;
 
   for (int i = tid; i <= g.ngroups; i += GT) {
     s_row[i] = g.row_off[i];
     s_tile[i] = g.tile_off[i];
   }
   if (tid == 0) {
-    mbar_init(&mma_bar[0], 1);
-    mbar_init(&mma_bar[1], 1);
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full[i], 32);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&wd_full[i], N_DQ);
+      mbar_init(&wd_empty[i], 1);
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], N_EPI);
+    }
+    mbar_init(&fin, 1);
     fence_mbar_init();
     s_abort = 0;
   }
-  if (warp == 0) tmem_alloc(&tmem_slot, BN);
+  if (warp == W_MMA) tmem_alloc(&tmem_slot, 2 * TT);
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = tmem_slot;
-  const int total = s_tile[g.ngroups] * NT;
+  const int total = s_tile[g.ngroups] * WT;
   const int my_tiles = total > (int)blockIdx.x ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
   const int jobs = my_tiles * KB;
 
-  // tile i of this CTA -> rows, output columns and weight slot (group search in shared memory)
+  // tile i of this CTA: token rows, weight rows and weight slot (group search in shared memory)
   auto tile_of = [&](int i) -> Tile {
     const int t = (int)blockIdx.x + i * (int)gridDim.x;
-    int lo = 0, hi = g.ngroups;  // s_tile[lo] * NT <= t < s_tile[hi] * NT
+    int lo = 0, hi = g.ngroups;  // s_tile[lo] * WT <= t < s_tile[hi] * WT
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (s_tile[mid] * NT <= t) lo = mid; else hi = mid;
+      if (s_tile[mid] * WT <= t) lo = mid; else hi = mid;
     }
-    const int mt_g = s_tile[lo + 1] - s_tile[lo];
-    const int local = t - s_tile[lo] * NT;
+    const int tt_g = s_tile[lo + 1] - s_tile[lo];  // token tiles of the group
+    const int local = t - s_tile[lo] * WT;
     Tile T;
-    T.m0 = s_row[lo] + (local % mt_g) * BM;
-    T.rows = min(BM, s_row[lo + 1] - T.m0);
-    T.n0 = (local / mt_g) * BN;
+    T.m0 = s_row[lo] + (local % tt_g) * TT;
+    T.rows = min(TT, s_row[lo + 1] - T.m0);
+    T.n0 = (local / tt_g) * WM;
     T.slot = lo;
     return T;
   };
-
-  // all threads: issue the copies of job j (tile j / KB, k-block j % KB) into its stage
-  int ld_i = -1;  // tile the loader decoded last
-  Tile ld_T{};
-  auto load_job = [&](int j) {
-    if (j < jobs) {
-      if (j / KB != ld_i) {
-        ld_i = j / KB;
-        ld_T = tile_of(ld_i);
+  // bounded wait: false after an abort or once the time limit passes (sets the status)
+  auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+      if (mbar_try_wait_hint(bar, parity, 10000u)) return true;  // suspended, not spinning
+      if ((it & 3u) == 0) {
+        if (s_abort) return false;
+        if (globaltimer() - t0 > g.timeout_ns) {
+          atomicOr(g.status, (uint32_t)E0_DEV_TIMEOUT);
+          s_abort = 1;
+          return false;
+        }
       }
-      const Tile T = ld_T;
+    }
+  };
+
+  if (warp == W_COPY) {
+    // ---------------- copies: token rows and codes of job j into stage j % STAGES
+    int cur_i = -1;
+    Tile T{};
+    for (int j = 0; j < jobs; ++j) {
+      const int st = j % STAGES, round = j / STAGES;
+      if (round > 0 && !wait(&empty[st], (round - 1) & 1)) break;
+      if (j / KB != cur_i) {
+        cur_i = j / KB;
+        T = tile_of(cur_i);
+      }
       const int kb = j % KB;
-      uint8_t* sA = raw + (size_t)(j % STAGES) * RAW_BYTES;
-      uint8_t* sBq = sA + A_BYTES;
-      // rows past the group's end are not loaded: they only feed accumulator rows that
-      // the epilogue discards
-      for (int c = tid; c < T.rows * 8; c += GT) {
+      uint8_t* sx = raw + (size_t)st * RAW_BYTES;
+      uint8_t* sq = sx + X_BYTES;
+      for (int c = lane; c < T.rows * 8; c += 32) {
         const int r = c >> 3, ch = c & 7;
-        const __half* src = g.A + (size_t)(T.m0 + r) * g.lda + kb * BK + ch * 8;
-        cp_async16(sA + r * 128 + ((ch ^ (r & 7)) << 4), src, 16u);
+        cp_async16(sx + r * 128 + ((ch ^ (r & 7)) << 4), g.A + (size_t)(T.m0 + r) * g.lda + kb * BK + ch * 8, 16u);
       }
 #pragma unroll
-      for (int c = tid; c < BN * 2; c += GT) {
+      for (int c = lane; c < WM * 2; c += 32) {
         const int n = c >> 1, h = c & 1;
         const uint32_t* src;
         if (LAYOUT == E0_LAYOUT_ROWS)
           src = g.q + ((size_t)T.slot * g.N + T.n0 + n) * (g.K / 8) + kb * 8 + h * 4;
         else
           src = g.q + ((size_t)T.slot * (g.K / 32) + 2 * kb + h) * (size_t)g.N * 4 + (size_t)(T.n0 + n) * 4;
-        cp_async16(sBq + n * 32 + h * 16, src, 16u);
+        cp_async16(sq + n * 32 + h * 16, src, 16u);
       }
+      cp_async_bar_arrive(&full[st]);  // completes when this lane's copies have landed
     }
-    cp_async_commit();
-  };
-
-  // scale and bias of row (tid) of the B tile, loaded 8 k-blocks ahead
-  uint16_t cs[8], cb[8], ns[8], nb[8];
-  auto load_sb = [&](int j, uint16_t (&ds)[8], uint16_t (&db)[8]) {
+    cp_async_wait<0>();
+  } else if (warp >= W_DQ0 && warp < W_DQ0 + N_DQ) {
+    // ---------------- dequantisation: thread pair (2n, 2n + 1) owns weight row n
+    const int dt = tid - 32 * W_DQ0, n = dt >> 1, h = dt & 1;
+    // scales and biases of this row, in chunks of up to 8 k-blocks of one tile; the
+    // next chunk is loaded while the current one is in use
+    uint16_t cs[8], cb[8], ns[8], nb[8];
+    auto load_sb = [&](int j0) {
 #pragma unroll
-    for (int u = 0; u < 8; ++u) ds[u] = db[u] = 0;
-    if (j >= jobs) return;
-    const Tile T = tile_of(j / KB);
-    const int kb0 = j % KB;
+      for (int u = 0; u < 8; ++u) ns[u] = nb[u] = 0;
+      if (j0 >= jobs) return;
+      const Tile Tn = tile_of(j0 / KB);
+      const int kb0 = j0 % KB;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int kb = kb0 + u;
-      if (kb < KB) {
-        size_t idx;
-        if (LAYOUT == E0_LAYOUT_ROWS)
-          idx = ((size_t)T.slot * g.N + T.n0 + (tid >> 1)) * (g.K / 64) + kb;
-        else
-          idx = ((size_t)T.slot * (g.K / 64) + kb) * g.N + T.n0 + (tid >> 1);
-        ds[u] = __ldg(g.s + idx);
-        db[u] = __ldg(g.b + idx);
+      for (int u = 0; u < 8; ++u)
+        if (kb0 + u < KB) {
+          size_t idx;
+          if (LAYOUT == E0_LAYOUT_ROWS)
+            idx = ((size_t)Tn.slot * g.N + Tn.n0 + n) * (g.K / 64) + kb0 + u;
+          else
+            idx = ((size_t)Tn.slot * (g.K / 64) + kb0 + u) * g.N + Tn.n0 + n;
+          ns[u] = __ldg(g.s + idx);
+          nb[u] = __ldg(g.b + idx);
+        }
+    };
+    load_sb(0);
+    for (int j = 0; j < jobs; ++j) {
+      const int st = j % STAGES, kb = j % KB, buf = j & 1;
+      if ((kb & 7) == 0) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          cs[u] = ns[u];
+          cb[u] = nb[u];
+        }
+        load_sb(kb + 8 < KB ? j + 8 : (j / KB + 1) * KB);
       }
-    }
-  };
-
-  const uint32_t idesc = idesc_f16_f32(BM, BN);
-  for (int j = 0; j < LOOK; ++j) load_job(j);
-  // Scales and biases come in chunks of up to 8 k-blocks of one tile; the next chunk
-  // is loaded while the current one is in use.
-  load_sb(0, ns, nb);
-
-  for (int j = 0; j < jobs; ++j) {
-    const int kb = j % KB;
-    // 1. the tensor core is done with job j - 2: its dequantised B buffer and raw stage are free
-    if (j >= 2 && !wait_bar(&mma_bar[j & 1], ((j >> 1) - 1) & 1, g)) s_abort = 1;
-    // 2. copies of job j + LOOK into the stage job j - 2 used
-    load_job(j + LOOK);
-    // 3. job j's copies have landed (this thread's), and are visible to the tensor core
-    cp_async_wait<LOOK>();
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncthreads();
-    if (s_abort) break;
-    // 4. scales of this k-block
-    if ((kb & 7) == 0) {
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        cs[u] = ns[u];
-        cb[u] = nb[u];
-      }
-      load_sb(kb + 8 < KB ? j + 8 : (j / KB + 1) * KB, ns, nb);
-    }
-    // 5. dequantise this thread's B row into the swizzled fp16 buffer
-    {
-      const int u = kb & 7;
+      if (!wait(&full[st], (j / STAGES) & 1)) break;
+      if (j >= 2 && !wait(&wd_empty[buf], ((j >> 1) - 1) & 1)) break;
       uint16_t sv = 0, bv = 0;
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (q == u) {
-          sv = cs[q];
-          bv = cb[q];
+      for (int u = 0; u < 8; ++u)
+        if (u == (kb & 7)) {
+          sv = cs[u];
+          bv = cb[u];
         }
-      const int n = tid >> 1, h = tid & 1;
-      const uint8_t* codes = raw + (size_t)(j % STAGES) * RAW_BYTES + A_BYTES + n * 32 + h * 16;
-      dequant_half_row(codes, bdq + (size_t)(j & 1) * BD_BYTES + n * 128, n, h, bf16pair_to_h2(sv), bf16pair_to_h2(bv));
+      dequant_half_row(raw + (size_t)st * RAW_BYTES + X_BYTES + n * 32 + h * 16, wdq + (size_t)buf * WD_BYTES + n * 128, n,
+                       h, bf16pair_to_h2(sv), bf16pair_to_h2(bv));
+      // the copied token rows and these weights are read by the tensor core (async proxy)
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&wd_full[buf]);
     }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    fence_before_sync();
-    __syncthreads();
-    // 6. one thread issues the four K=16 steps of this k-block and commits them
-    if (tid == 0) {
-      fence_after_sync();
-      const uint32_t a_addr = smem_u32(raw + (size_t)(j % STAGES) * RAW_BYTES);
-      const uint32_t b_addr = smem_u32(bdq + (size_t)(j & 1) * BD_BYTES);
+  } else if (warp == W_MMA) {
+    // ---------------- one thread issues the MMAs of every job and commits them
+    if (lane == 0) {
+      int cur_i = -1;
+      Tile T{};
+      uint32_t idesc = 0;
+      for (int j = 0; j < jobs; ++j) {
+        const int st = j % STAGES, kb = j % KB, buf = j & 1;
+        const int i = j / KB, ab = i & 1;
+        if (i != cur_i) {
+          cur_i = i;
+          T = tile_of(i);
+          idesc = idesc_f16_f32(WM, (T.rows + 15) & ~15);
+          if (i >= 2 && !wait(&acc_empty[ab], ((i >> 1) - 1) & 1)) break;  // epilogue done with this accumulator
+        }
+        if (!wait(&wd_full[buf], (j >> 1) & 1)) break;
+        fence_after_sync();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        const uint32_t w_addr = smem_u32(wdq + (size_t)buf * WD_BYTES);
+        const uint32_t x_addr = smem_u32(raw + (size_t)st * RAW_BYTES);
 #pragma unroll
-      for (int kk = 0; kk < BK / 16; ++kk)
-        mma_f16(tmem, sdesc_k128(a_addr + 32 * kk), sdesc_k128(b_addr + 32 * kk), idesc, kb > 0 || kk > 0);
-      commit(&mma_bar[j & 1]);
+        for (int kk = 0; kk < BK / 16; ++kk)
+          mma_f16(tmem + (uint32_t)(ab * TT), sdesc_k128(w_addr + 32 * kk), sdesc_k128(x_addr + 32 * kk), idesc,
+                  kb > 0 || kk > 0);
+        commit(&empty[st]);
+        commit(&wd_empty[buf]);
+        if (kb == KB - 1) commit(&acc_full[ab]);
+      }
+      commit(&fin);  // every MMA issued so far has completed when this arrives
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(&fin, 0) && globaltimer() - t0 < g.timeout_ns) {
+      }
     }
-    // 7. last k-block of a tile: epilogue from tensor memory
-    if (kb == KB - 1) {
-      const bool done = wait_bar(&mma_bar[j & 1], (j >> 1) & 1, g);
+    __syncwarp();
+  } else {
+    // ---------------- epilogue: accumulator [weight row][token] from tensor memory
+    const int quad = warp & 3, r = quad * 32 + lane;  // this thread's weight row
+    for (int i = 0; i < my_tiles; ++i) {
+      const int ab = i & 1;
+      const bool ok = wait(&acc_full[ab], (i >> 1) & 1);
       fence_after_sync();
-      const Tile T = tile_of(j / KB);
-      const int quad = warp & 3, cblk = warp >> 2;  // lanes 32 quad.., columns 64 cblk..
-      const int r = quad * 32 + lane;
-      const bool row_ok = done && r < T.rows;
+      if (!ok) break;
+      const Tile T = tile_of(i);
+      const int nout = T.n0 + r;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN / 4; c0 += 32) {
-        const int col = cblk * (BN / 4) + c0;
+      for (int c0 = 0; c0 < T.rows; c0 += 32) {
         uint32_t v[32];
-        tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)col, v);
-        if (!row_ok) continue;
+        tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(ab * TT + c0), v);
+        const int nc = min(32, T.rows - c0);
         if (EPI == EPI_SWIGLU) {
-          // columns 2i / 2i + 1 are gate / up of output (n0 + col) / 2 + i
-          float a[16];
+          // rows 2j / 2j + 1 of the weight tile (lanes 2j / 2j + 1) are gate / up of output j
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float gt = __uint_as_float(v[2 * i]), up = __uint_as_float(v[2 * i + 1]);
-            a[i] = __fdividef(gt, 1.0f + __expf(-gt)) * up;
-          }
-          __half* dst = g.out16 + (size_t)(T.m0 + r) * g.ldo + (T.n0 + col) / 2;
-#pragma unroll
-          for (int grp = 0; grp < 2; ++grp) {
-            uint32_t w[4];
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-              const __half2 h2 = __floats2half2_rn(a[8 * grp + jj], a[8 * grp + jj + 4]);
-              w[jj] = *reinterpret_cast<const uint32_t*>(&h2);
+          for (int c = 0; c < 32; ++c) {
+            const float gt = __uint_as_float(v[c]);
+            const float up = __shfl_down_sync(0xffffffffu, gt, 1);
+            if ((lane & 1) == 0 && c < nc) {
+              const int o = nout >> 1;  // output index
+              const int pos = (o & ~7) + ((o & 7) < 4 ? 2 * (o & 7) : 2 * ((o & 7) - 4) + 1);
+              g.out16[(size_t)(T.m0 + c0 + c) * g.ldo + pos] = __float2half_rn(__fdividef(gt, 1.0f + __expf(-gt)) * up);
             }
-            *reinterpret_cast<uint4*>(dst + 8 * grp) = make_uint4(w[0], w[1], w[2], w[3]);
           }
         } else {
-          const float f = g.rowscale ? g.rowscale[T.m0 + r] : 1.0f;
-          float* dst = g.out32 + (size_t)(T.m0 + r) * g.ldo + T.n0 + col;
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(dst + i) =
-                make_float4(f * __uint_as_float(v[i]), f * __uint_as_float(v[i + 1]), f * __uint_as_float(v[i + 2]),
-                            f * __uint_as_float(v[i + 3]));
+          for (int c = 0; c < 32; ++c)
+            if (c < nc) {
+              const int row = T.m0 + c0 + c;
+              const float f = g.rowscale ? g.rowscale[row] : 1.0f;
+              g.out32[(size_t)row * g.ldo + nout] = f * __uint_as_float(v[c]);
+            }
         }
       }
-      if (!done) s_abort = 1;
       fence_before_sync();
-      __syncthreads();
-      if (s_abort) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[ab]);
     }
   }
-  cp_async_wait<0>();
   fence_before_sync();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, BN);
+  fence_after_sync();
+  if (warp == W_MMA) tmem_dealloc(tmem, 2 * TT);
 }
 
 // ------------------------------------------------------------------ small kernels
@@ -404,7 +432,7 @@ __global__ void __launch_bounds__(1024) sort_kernel(const int32_t* ids, const fl
   const int n = e < E ? cnt[e] : 0;
   int tot_rows, tot_tiles;
   const int ro = block_excl_scan(n, s_warp, tot_rows);
-  const int to = block_excl_scan((n + BM - 1) / BM, s_warp, tot_tiles);
+  const int to = block_excl_scan((n + TT - 1) / TT, s_warp, tot_tiles);
   if (e < E) {
     row_off[e] = ro;
     tile_off[e] = to;
@@ -416,7 +444,7 @@ __global__ void __launch_bounds__(1024) sort_kernel(const int32_t* ids, const fl
     one_row[0] = 0;
     one_row[1] = T;
     one_tile[0] = 0;
-    one_tile[1] = (T + BM - 1) / BM;
+    one_tile[1] = (T + TT - 1) / TT;
   }
   __syncthreads();
   for (int p = threadIdx.x; p < P; p += blockDim.x) {

@@ -55,8 +55,8 @@ def test_prefill_tiny_every_token():
 
 
 def test_prefill_ragged_tiles_and_one_hot_expert():
-    """T = 129 tokens all routed to the same K experts: two row tiles per expert, the
-    second holding one row; the other experts get no rows."""
+    """T = 129 tokens all routed to the same K experts: three 64-row token tiles per
+    expert, the last holding one row; the other experts get no rows."""
     sh, seed, T = S.TINY, 1, 129
     z = S.zipf_gumbel_logits(seed, T, sh.E)
     z[:, :sh.K] += 100.0
