@@ -1392,6 +1392,7 @@ __device__ void consumer(const EngineParams& P, Ctl& C, uint8_t* ring) {
       int nu;
       const Unit* us = units_of(P, KIND_ROUTER, cta, nu);
       for (int i = 0; i < nu; ++i) consume_unit<D>(cs, Ld, us[i], l, acc, zh, zr);
+      if (tid == 0) stamp(P, l, 8 + U_ROUTER);  // gate rows of this CTA published
     }
     int nu;
     const Unit* us = units_of(P, P.plan ? Ld.plan_kind : 0, cta, nu);

@@ -183,7 +183,11 @@ struct EngineParams {
   uint16_t* h_trace;
   int32_t accumulate;
   int32_t pad1;
-  uint64_t* trace;             // nullable: [ncta][L][8] %globaltimer stamps (diagnostics)
+  uint64_t* trace;             // nullable: [ncta][L][16] %globaltimer diagnostics: 0 layer start,
+                               // 1 input dependency met, 2 input built, 3 units done, 4 route
+                               // published, 5 copies issued, 6/7 stage-wait time/count, 8 own-gate
+                               // routing started, 8 + type: time in units of that type (for
+                               // U_ROUTER: when this CTA's gate rows were published)
   uint8_t* ws;
   WsLayout wl;
   LayerDesc inline_layer;

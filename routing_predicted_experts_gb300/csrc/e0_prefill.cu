@@ -43,7 +43,9 @@ constexpr int STAGES = 12;                   // copy stages in flight (48 KB of 
 constexpr int X_BYTES = TT * BK * 2;         // 8 KB of fp16 token rows
 constexpr int Q_BYTES = WM * BK / 2;         // 4 KB of int4 codes
 constexpr int RAW_BYTES = X_BYTES + Q_BYTES;
-constexpr int WD_BYTES = WM * BK * 2;        // 16 KB of dequantised fp16 weights
+constexpr int BKD = 2 * BK;                  // reduction block of one dequantise -> MMA hand-over
+constexpr int WD_SUB = WM * BK * 2;          // 16 KB: one 64-wide block of dequantised fp16 weights
+constexpr int WD_BYTES = WM * BKD * 2;       // 32 KB: two of them per hand-over buffer
 constexpr int EMAXP = 1024;
 // roles: warp 0 copies, warps 1..8 dequantise, warp 9 issues the MMAs, warps 10..13 run
 // the epilogue (tensor-memory lane quadrants 2, 3, 0, 1)
@@ -54,13 +56,14 @@ static_assert(X_BYTES % 1024 == 0 && RAW_BYTES % 1024 == 0, "stages stay 1024-by
 static_assert(2 * TT >= 32 && (2 * TT & (2 * TT - 1)) == 0, "tensor memory columns: a power of two >= 32");
 static_assert(GEMM_SMEM <= 227 * 1024, "shared memory");
 static_assert(N_DQ * 32 == 2 * WM, "two dequantising threads per weight row");
+static_assert(BKD % BK == 0 && BKD / BK == 2, "a hand-over covers two copy stages");
 
 enum Epi : int { EPI_SWIGLU = 0, EPI_F32 = 1 };
 
 struct GemmArgs {
   const __half* A;        // token rows [rows][K] fp16, reduction index permuted within groups of 8
   int lda;
-  int K, N;               // reduction length (multiple of 64), outputs per group (multiple of 128)
+  int K, N;               // reduction length (multiple of 128), outputs per group (multiple of 128)
   int ngroups;
   const int* row_off;     // [ngroups + 1] rows of group g: [row_off[g], row_off[g + 1])
   const int* tile_off;    // [ngroups + 1] prefix sums of ceil(rows_g / TT)
@@ -251,27 +254,33 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
         }
     };
     load_sb(0);
-    for (int j = 0; j < jobs; ++j) {
-      const int st = j % STAGES, kb = j % KB, buf = j & 1;
+    // hand-over p covers copy stages 2p and 2p + 1 (a tile has an even number of them)
+    for (int p = 0; 2 * p < jobs; ++p) {
+      const int j0 = 2 * p, kb = j0 % KB, buf = p & 1;
       if ((kb & 7) == 0) {
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           cs[u] = ns[u];
           cb[u] = nb[u];
         }
-        load_sb(kb + 8 < KB ? j + 8 : (j / KB + 1) * KB);
+        load_sb(kb + 8 < KB ? j0 + 8 : (j0 / KB + 1) * KB);
       }
-      if (!wait(&full[st], (j / STAGES) & 1)) break;
-      if (j >= 2 && !wait(&wd_empty[buf], ((j >> 1) - 1) & 1)) break;
-      uint16_t sv = 0, bv = 0;
+      if (!wait(&full[j0 % STAGES], (j0 / STAGES) & 1)) break;
+      if (!wait(&full[(j0 + 1) % STAGES], ((j0 + 1) / STAGES) & 1)) break;
+      if (p >= 2 && !wait(&wd_empty[buf], ((p >> 1) - 1) & 1)) break;
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (u == (kb & 7)) {
-          sv = cs[u];
-          bv = cb[u];
-        }
-      dequant_half_row(raw + (size_t)st * RAW_BYTES + X_BYTES + n * 32 + h * 16, wdq + (size_t)buf * WD_BYTES + n * 128, n,
-                       h, bf16pair_to_h2(sv), bf16pair_to_h2(bv));
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint16_t sv = 0, bv = 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (u == ((kb + h2) & 7)) {
+            sv = cs[u];
+            bv = cb[u];
+          }
+        dequant_half_row(raw + (size_t)((j0 + h2) % STAGES) * RAW_BYTES + X_BYTES + n * 32 + h * 16,
+                         wdq + (size_t)buf * WD_BYTES + (size_t)h2 * WD_SUB + n * 128, n, h, bf16pair_to_h2(sv),
+                         bf16pair_to_h2(bv));
+      }
       // the copied token rows and these weights are read by the tensor core (async proxy)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
@@ -283,27 +292,31 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
       int cur_i = -1;
       Tile T{};
       uint32_t idesc = 0;
-      for (int j = 0; j < jobs; ++j) {
-        const int st = j % STAGES, kb = j % KB, buf = j & 1;
-        const int i = j / KB, ab = i & 1;
+      for (int p = 0; 2 * p < jobs; ++p) {
+        const int j0 = 2 * p, kb = j0 % KB, buf = p & 1;
+        const int i = j0 / KB, ab = i & 1;
         if (i != cur_i) {
           cur_i = i;
           T = tile_of(i);
           idesc = idesc_f16_f32(WM, (T.rows + 15) & ~15);
           if (i >= 2 && !wait(&acc_empty[ab], ((i >> 1) - 1) & 1)) break;  // epilogue done with this accumulator
         }
-        if (!wait(&wd_full[buf], (j >> 1) & 1)) break;
+        if (!wait(&wd_full[buf], (p >> 1) & 1)) break;
         fence_after_sync();
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        const uint32_t w_addr = smem_u32(wdq + (size_t)buf * WD_BYTES);
-        const uint32_t x_addr = smem_u32(raw + (size_t)st * RAW_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          mma_f16(tmem + (uint32_t)(ab * TT), sdesc_k128(w_addr + 32 * kk), sdesc_k128(x_addr + 32 * kk), idesc,
-                  kb > 0 || kk > 0);
-        commit(&empty[st]);
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const uint32_t w_addr = smem_u32(wdq + (size_t)buf * WD_BYTES + (size_t)h2 * WD_SUB);
+          const uint32_t x_addr = smem_u32(raw + (size_t)((j0 + h2) % STAGES) * RAW_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_f16(tmem + (uint32_t)(ab * TT), sdesc_k128(w_addr + 32 * kk), sdesc_k128(x_addr + 32 * kk), idesc,
+                    kb > 0 || h2 > 0 || kk > 0);
+        }
+        commit(&empty[j0 % STAGES]);
+        commit(&empty[(j0 + 1) % STAGES]);
         commit(&wd_empty[buf]);
-        if (kb == KB - 1) commit(&acc_full[ab]);
+        if (kb + 2 == KB) commit(&acc_full[ab]);
       }
       commit(&fin);  // every MMA issued so far has completed when this arrives
       const uint64_t t0 = globaltimer();
