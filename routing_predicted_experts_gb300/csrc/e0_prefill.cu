@@ -39,7 +39,8 @@ namespace e0pf {
 constexpr int WM = 128;                      // weight rows per tile: the MMA's M
 constexpr int TT = 64;                       // token rows per tile, at most: the MMA's N
 constexpr int BK = 64;                       // reduction block
-constexpr int STAGES = 12;                   // copy stages in flight (48 KB of codes)
+constexpr int STAGES = 7;                    // copy stages in flight (28 KB of codes)
+constexpr int NWD = 4;                       // dequantise -> MMA hand-over buffers
 constexpr int X_BYTES = TT * BK * 2;         // 8 KB of fp16 token rows
 constexpr int Q_BYTES = WM * BK / 2;         // 4 KB of int4 codes
 constexpr int RAW_BYTES = X_BYTES + Q_BYTES;
@@ -47,15 +48,21 @@ constexpr int BKD = 2 * BK;                  // reduction block of one dequantis
 constexpr int WD_SUB = WM * BK * 2;          // 16 KB: one 64-wide block of dequantised fp16 weights
 constexpr int WD_BYTES = WM * BKD * 2;       // 32 KB: two of them per hand-over buffer
 constexpr int EMAXP = 1024;
-// roles: warp 0 copies, warps 1..8 dequantise, warp 9 issues the MMAs, warps 10..13 run
-// the epilogue (tensor-memory lane quadrants 2, 3, 0, 1)
-constexpr int W_COPY = 0, W_DQ0 = 1, N_DQ = 8, W_MMA = 9, W_EPI0 = 10, N_EPI = 4;
+// roles: warps 0..3 copy (job j by warp j % 4), warps 4..19 dequantise, warp 20 issues the
+// MMAs, warps 21..24 run the epilogue (tensor-memory lane quadrants 1, 2, 3, 0)
+constexpr int W_COPY = 0, N_COPY = 4, W_DQ0 = 4, N_DQ = 16, W_MMA = 20, W_EPI0 = 21, N_EPI = 4;
+// the dequantising warps form two groups that take alternate hand-overs (buffers g, g + 2
+// for group g), so that one group's proxy fence and hand-over overlap the other's work
+constexpr int DQ_GROUPS = 2, N_DQG = N_DQ / DQ_GROUPS;
+constexpr int DQ_PER_ROW = N_DQG * 32 / WM;  // dequantising threads per weight row in a group
+constexpr int DQ_WORDS = 8 / DQ_PER_ROW;     // code words (8 codes each) a thread converts per 64-wide block
 constexpr int GT = 32 * (W_EPI0 + N_EPI);
-constexpr size_t GEMM_SMEM = 1024 + (size_t)STAGES * RAW_BYTES + 2 * WD_BYTES + 2 * (EMAXP + 1) * sizeof(int);
+constexpr size_t GEMM_SMEM = 1024 + (size_t)STAGES * RAW_BYTES + NWD * WD_BYTES + 2 * (EMAXP + 1) * sizeof(int);
 static_assert(X_BYTES % 1024 == 0 && RAW_BYTES % 1024 == 0, "stages stay 1024-byte aligned");
 static_assert(2 * TT >= 32 && (2 * TT & (2 * TT - 1)) == 0, "tensor memory columns: a power of two >= 32");
 static_assert(GEMM_SMEM <= 227 * 1024, "shared memory");
-static_assert(N_DQ * 32 == 2 * WM, "two dequantising threads per weight row");
+static_assert(N_DQG * 32 == DQ_PER_ROW * WM && 8 % DQ_PER_ROW == 0, "whole code words per dequantising thread");
+static_assert(NWD % DQ_GROUPS == 0, "every hand-over buffer belongs to one dequantising group");
 static_assert(BKD % BK == 0 && BKD / BK == 2, "a hand-over covers two copy stages");
 
 enum Epi : int { EPI_SWIGLU = 0, EPI_F32 = 1 };
@@ -87,17 +94,24 @@ __device__ __forceinline__ __half2 bf16pair_to_h2(uint16_t v) {
   return __halves2half2(h, h);
 }
 
-// Dequantise half of a 64-code weight row segment (one uint4 = 32 codes, chunks
-// 4h .. 4h + 3 of the row) into the swizzled fp16 row: codes j and j + 4 of each word
-// become an fp16 pair (1024 + c by the exponent trick, then exactly c, then s*c + b).
-__device__ __forceinline__ void dequant_half_row(const uint8_t* codes, uint8_t* dst_row, int n, int h, __half2 s2,
-                                                 __half2 b2) {
-  const uint4 w0 = *reinterpret_cast<const uint4*>(codes);
-  const uint32_t words[4] = {w0.x, w0.y, w0.z, w0.w};
+// Dequantise DQ_WORDS code words (8 codes each) of a 64-code weight row segment, words
+// q*DQ_WORDS .. (q+1)*DQ_WORDS - 1, into the swizzled fp16 row: word m holds chunk m
+// (16 bytes of fp16), codes j and j + 4 of the word become one fp16 pair (1024 + c by
+// the exponent trick, then exactly c, then s*c + b).
+__device__ __forceinline__ void dequant_words(const uint8_t* codes, uint8_t* dst_row, int n, int q, __half2 s2,
+                                              __half2 b2) {
+  uint32_t words[DQ_WORDS];
+  if (DQ_WORDS == 4) {
+    const uint4 w0 = *reinterpret_cast<const uint4*>(codes);
+    words[0] = w0.x; words[1] = w0.y; words[2 % DQ_WORDS] = w0.z; words[3 % DQ_WORDS] = w0.w;
+  } else {
+    const uint2 w0 = *reinterpret_cast<const uint2*>(codes);
+    words[0] = w0.x; words[1 % DQ_WORDS] = w0.y;
+  }
   const __half2 magic = __halves2half2(__ushort_as_half((unsigned short)0x6400), __ushort_as_half((unsigned short)0x6400));
 #pragma unroll
-  for (int mm = 0; mm < 4; ++mm) {
-    const int m = 4 * h + mm;
+  for (int mm = 0; mm < DQ_WORDS; ++mm) {
+    const int m = DQ_WORDS * q + mm;
     uint32_t out[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -128,9 +142,9 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
   uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
   uint8_t* raw = sm;                                // STAGES x [token rows | codes]
   uint8_t* wdq = sm + (size_t)STAGES * RAW_BYTES;   // 2 x dequantised weights
-  int* s_row = reinterpret_cast<int*>(wdq + 2 * WD_BYTES);
+  int* s_row = reinterpret_cast<int*>(wdq + NWD * WD_BYTES);
   int* s_tile = s_row + (EMAXP + 1);
-  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], wd_full[2], wd_empty[2], acc_full[2], acc_empty[2], fin;
+  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], wd_full[NWD], wd_empty[NWD], acc_full[2], acc_empty[2], fin;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int s_abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -145,9 +159,11 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
       mbar_init(&full[i], 32);
       mbar_init(&empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&wd_full[i], N_DQ);
+    for (int i = 0; i < NWD; ++i) {
+      mbar_init(&wd_full[i], N_DQG);
       mbar_init(&wd_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], N_EPI);
     }
@@ -198,11 +214,11 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
     }
   };
 
-  if (warp == W_COPY) {
+  if (warp >= W_COPY && warp < W_COPY + N_COPY) {
     // ---------------- copies: token rows and codes of job j into stage j % STAGES
     int cur_i = -1;
     Tile T{};
-    for (int j = 0; j < jobs; ++j) {
+    for (int j = warp - W_COPY; j < jobs; j += N_COPY) {
       const int st = j % STAGES, round = j / STAGES;
       if (round > 0 && !wait(&empty[st], (round - 1) & 1)) break;
       if (j / KB != cur_i) {
@@ -230,61 +246,56 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
     }
     cp_async_wait<0>();
   } else if (warp >= W_DQ0 && warp < W_DQ0 + N_DQ) {
-    // ---------------- dequantisation: thread pair (2n, 2n + 1) owns weight row n
-    const int dt = tid - 32 * W_DQ0, n = dt >> 1, h = dt & 1;
-    // scales and biases of this row, in chunks of up to 8 k-blocks of one tile; the
-    // next chunk is loaded while the current one is in use
-    uint16_t cs[8], cb[8], ns[8], nb[8];
-    auto load_sb = [&](int j0) {
-#pragma unroll
-      for (int u = 0; u < 8; ++u) ns[u] = nb[u] = 0;
-      if (j0 >= jobs) return;
-      const Tile Tn = tile_of(j0 / KB);
-      const int kb0 = j0 % KB;
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (kb0 + u < KB) {
-          size_t idx;
-          if (LAYOUT == E0_LAYOUT_ROWS)
-            idx = ((size_t)Tn.slot * g.N + Tn.n0 + n) * (g.K / 64) + kb0 + u;
-          else
-            idx = ((size_t)Tn.slot * (g.K / 64) + kb0 + u) * g.N + Tn.n0 + n;
-          ns[u] = __ldg(g.s + idx);
-          nb[u] = __ldg(g.b + idx);
-        }
-    };
-    load_sb(0);
-    // hand-over p covers copy stages 2p and 2p + 1 (a tile has an even number of them)
-    for (int p = 0; 2 * p < jobs; ++p) {
-      const int j0 = 2 * p, kb = j0 % KB, buf = p & 1;
-      if ((kb & 7) == 0) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          cs[u] = ns[u];
-          cb[u] = nb[u];
-        }
-        load_sb(kb + 8 < KB ? j0 + 8 : (j0 / KB + 1) * KB);
+    // ---------------- dequantisation: group grp takes hand-overs p = grp, grp + 2, ...;
+    // DQ_PER_ROW consecutive threads of the group own weight row n
+    const int dt = tid - 32 * W_DQ0, grp = dt / (32 * N_DQG), gtid = dt % (32 * N_DQG);
+    const int n = gtid / DQ_PER_ROW, h = gtid % DQ_PER_ROW;
+    // scales and biases of this row for the two k-blocks of hand-over p (prefetched two
+    // hand-overs of the group ahead); the tile of the last fetch is cached
+    int t_i = -1;
+    Tile tt{};
+    auto fetch = [&](int p, uint16_t (&sv)[2], uint16_t (&bv)[2]) {
+      sv[0] = sv[1] = bv[0] = bv[1] = 0;
+      if (2 * p >= jobs) return;
+      const int j0 = 2 * p, i = j0 / KB, kb = j0 % KB;
+      if (i != t_i) {
+        t_i = i;
+        tt = tile_of(i);
       }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        size_t idx;
+        if (LAYOUT == E0_LAYOUT_ROWS)
+          idx = ((size_t)tt.slot * g.N + tt.n0 + n) * (g.K / 64) + kb + u;
+        else
+          idx = ((size_t)tt.slot * (g.K / 64) + kb + u) * g.N + tt.n0 + n;
+        sv[u] = __ldg(g.s + idx);
+        bv[u] = __ldg(g.b + idx);
+      }
+    };
+    uint16_t cs[2], cb[2], ns[2], nb[2];
+    fetch(grp, cs, cb);
+    fetch(grp + DQ_GROUPS, ns, nb);
+    for (int p = grp; 2 * p < jobs; p += DQ_GROUPS) {
+      const int j0 = 2 * p, buf = p % NWD;  // a buffer of this group: p % NWD == grp (mod 2)
       if (!wait(&full[j0 % STAGES], (j0 / STAGES) & 1)) break;
       if (!wait(&full[(j0 + 1) % STAGES], ((j0 + 1) / STAGES) & 1)) break;
-      if (p >= 2 && !wait(&wd_empty[buf], ((p >> 1) - 1) & 1)) break;
+      if (p >= NWD && !wait(&wd_empty[buf], (p / NWD - 1) & 1)) break;
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        uint16_t sv = 0, bv = 0;
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (u == ((kb + h2) & 7)) {
-            sv = cs[u];
-            bv = cb[u];
-          }
-        dequant_half_row(raw + (size_t)((j0 + h2) % STAGES) * RAW_BYTES + X_BYTES + n * 32 + h * 16,
-                         wdq + (size_t)buf * WD_BYTES + (size_t)h2 * WD_SUB + n * 128, n, h, bf16pair_to_h2(sv),
-                         bf16pair_to_h2(bv));
-      }
+      for (int h2 = 0; h2 < 2; ++h2)
+        dequant_words(raw + (size_t)((j0 + h2) % STAGES) * RAW_BYTES + X_BYTES + n * 32 + h * 4 * DQ_WORDS,
+                      wdq + (size_t)buf * WD_BYTES + (size_t)h2 * WD_SUB + n * 128, n, h, bf16pair_to_h2(cs[h2]),
+                      bf16pair_to_h2(cb[h2]));
       // the copied token rows and these weights are read by the tensor core (async proxy)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(&wd_full[buf]);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        cs[u] = ns[u];
+        cb[u] = nb[u];
+      }
+      fetch(p + 2 * DQ_GROUPS, ns, nb);
     }
   } else if (warp == W_MMA) {
     // ---------------- one thread issues the MMAs of every job and commits them
@@ -293,7 +304,7 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
       Tile T{};
       uint32_t idesc = 0;
       for (int p = 0; 2 * p < jobs; ++p) {
-        const int j0 = 2 * p, kb = j0 % KB, buf = p & 1;
+        const int j0 = 2 * p, kb = j0 % KB, buf = p % NWD;
         const int i = j0 / KB, ab = i & 1;
         if (i != cur_i) {
           cur_i = i;
@@ -301,7 +312,7 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
           idesc = idesc_f16_f32(WM, (T.rows + 15) & ~15);
           if (i >= 2 && !wait(&acc_empty[ab], ((i >> 1) - 1) & 1)) break;  // epilogue done with this accumulator
         }
-        if (!wait(&wd_full[buf], (p >> 1) & 1)) break;
+        if (!wait(&wd_full[buf], (p / NWD) & 1)) break;
         fence_after_sync();
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 #pragma unroll
