@@ -39,30 +39,35 @@ namespace e0pf {
 constexpr int WM = 128;                      // weight rows per tile: the MMA's M
 constexpr int TT = 64;                       // token rows per tile, at most: the MMA's N
 constexpr int BK = 64;                       // reduction block
-constexpr int STAGES = 7;                    // copy stages in flight (28 KB of codes)
-constexpr int NWD = 4;                       // dequantise -> MMA hand-over buffers
+constexpr int STAGES = 10;                   // copy stages in flight: token rows and codes
+constexpr int NWD = 2;                       // dequantise -> MMA hand-over buffers
 constexpr int X_BYTES = TT * BK * 2;         // 8 KB of fp16 token rows
 constexpr int Q_BYTES = WM * BK / 2;         // 4 KB of int4 codes
 constexpr int RAW_BYTES = X_BYTES + Q_BYTES;
 constexpr int BKD = 2 * BK;                  // reduction block of one dequantise -> MMA hand-over
 constexpr int WD_SUB = WM * BK * 2;          // 16 KB: one 64-wide block of dequantised fp16 weights
 constexpr int WD_BYTES = WM * BKD * 2;       // 32 KB: two of them per hand-over buffer
+// A hand-over buffer holds the MMA's operands for two k-blocks: the dequantised weights
+// (A) and a copy of the token rows (B), so that the copy stage is free as soon as it has
+// been converted and only the hand-over buffers wait for the tensor core.
+constexpr int HB_BYTES = WD_BYTES + 2 * X_BYTES;
 constexpr int EMAXP = 1024;
 // roles: warps 0..3 copy (job j by warp j % 4), warps 4..19 dequantise, warp 20 issues the
 // MMAs, warps 21..24 run the epilogue (tensor-memory lane quadrants 1, 2, 3, 0)
 constexpr int W_COPY = 0, N_COPY = 4, W_DQ0 = 4, N_DQ = 16, W_MMA = 20, W_EPI0 = 21, N_EPI = 4;
-// the dequantising warps form two groups that take alternate hand-overs (buffers g, g + 2
-// for group g), so that one group's proxy fence and hand-over overlap the other's work
+// the dequantising warps form two groups that take alternate hand-overs (buffer g for
+// group g), so that one group's proxy fence and hand-over overlap the other's work
 constexpr int DQ_GROUPS = 2, N_DQG = N_DQ / DQ_GROUPS;
 constexpr int DQ_PER_ROW = N_DQG * 32 / WM;  // dequantising threads per weight row in a group
 constexpr int DQ_WORDS = 8 / DQ_PER_ROW;     // code words (8 codes each) a thread converts per 64-wide block
 constexpr int GT = 32 * (W_EPI0 + N_EPI);
-constexpr size_t GEMM_SMEM = 1024 + (size_t)STAGES * RAW_BYTES + NWD * WD_BYTES + 2 * (EMAXP + 1) * sizeof(int);
+constexpr size_t GEMM_SMEM = 1024 + (size_t)STAGES * RAW_BYTES + NWD * HB_BYTES + 2 * (EMAXP + 1) * sizeof(int);
 static_assert(X_BYTES % 1024 == 0 && RAW_BYTES % 1024 == 0, "stages stay 1024-byte aligned");
 static_assert(2 * TT >= 32 && (2 * TT & (2 * TT - 1)) == 0, "tensor memory columns: a power of two >= 32");
 static_assert(GEMM_SMEM <= 227 * 1024, "shared memory");
 static_assert(N_DQG * 32 == DQ_PER_ROW * WM && 8 % DQ_PER_ROW == 0, "whole code words per dequantising thread");
-static_assert(NWD % DQ_GROUPS == 0, "every hand-over buffer belongs to one dequantising group");
+static_assert(NWD == DQ_GROUPS, "one hand-over buffer per dequantising group");
+static_assert(STAGES % 2 == 0, "a hand-over's two stages sit in one ring pass");
 static_assert(BKD % BK == 0 && BKD / BK == 2, "a hand-over covers two copy stages");
 
 enum Epi : int { EPI_SWIGLU = 0, EPI_F32 = 1 };
@@ -141,8 +146,8 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
   uint8_t* raw = sm;                                // STAGES x [token rows | codes]
-  uint8_t* wdq = sm + (size_t)STAGES * RAW_BYTES;   // 2 x dequantised weights
-  int* s_row = reinterpret_cast<int*>(wdq + NWD * WD_BYTES);
+  uint8_t* hbuf = sm + (size_t)STAGES * RAW_BYTES;  // NWD x [dequantised weights | token rows]
+  int* s_row = reinterpret_cast<int*>(hbuf + NWD * HB_BYTES);
   int* s_tile = s_row + (EMAXP + 1);
   __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], wd_full[NWD], wd_empty[NWD], acc_full[2], acc_empty[2], fin;
   __shared__ uint32_t tmem_slot;
@@ -157,7 +162,7 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
   if (tid == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&full[i], 32);
-      mbar_init(&empty[i], 1);
+      mbar_init(&empty[i], N_DQG);  // freed by the dequantising group that converts it
     }
     for (int i = 0; i < NWD; ++i) {
       mbar_init(&wd_full[i], N_DQG);
@@ -277,19 +282,32 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
     fetch(grp, cs, cb);
     fetch(grp + DQ_GROUPS, ns, nb);
     for (int p = grp; 2 * p < jobs; p += DQ_GROUPS) {
-      const int j0 = 2 * p, buf = p % NWD;  // a buffer of this group: p % NWD == grp (mod 2)
+      const int j0 = 2 * p, buf = p % NWD;  // this group's buffer: p % NWD == grp
       if (!wait(&full[j0 % STAGES], (j0 / STAGES) & 1)) break;
       if (!wait(&full[(j0 + 1) % STAGES], ((j0 + 1) / STAGES) & 1)) break;
       if (p >= NWD && !wait(&wd_empty[buf], (p / NWD - 1) & 1)) break;
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2)
         dequant_words(raw + (size_t)((j0 + h2) % STAGES) * RAW_BYTES + X_BYTES + n * 32 + h * 4 * DQ_WORDS,
-                      wdq + (size_t)buf * WD_BYTES + (size_t)h2 * WD_SUB + n * 128, n, h, bf16pair_to_h2(cs[h2]),
+                      hbuf + (size_t)buf * HB_BYTES + (size_t)h2 * WD_SUB + n * 128, n, h, bf16pair_to_h2(cs[h2]),
                       bf16pair_to_h2(cb[h2]));
-      // the copied token rows and these weights are read by the tensor core (async proxy)
+      // token rows of both k-blocks into the hand-over buffer (16-byte chunks keep their
+      // swizzled places; rows past the tile's are copied too and never read back)
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const uint4* src = reinterpret_cast<const uint4*>(raw + (size_t)((j0 + h2) % STAGES) * RAW_BYTES);
+        uint4* dst = reinterpret_cast<uint4*>(hbuf + (size_t)buf * HB_BYTES + WD_BYTES + (size_t)h2 * X_BYTES);
+#pragma unroll
+        for (int c = gtid; c < X_BYTES / 16; c += 32 * N_DQG) dst[c] = src[c];
+      }
+      // these weights and token rows are read by the tensor core (async proxy)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      if (lane == 0) mbar_arrive(&wd_full[buf]);
+      if (lane == 0) {
+        mbar_arrive(&wd_full[buf]);
+        mbar_arrive(&empty[j0 % STAGES]);  // this warp is done with both copy stages
+        mbar_arrive(&empty[(j0 + 1) % STAGES]);
+      }
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         cs[u] = ns[u];
@@ -317,15 +335,13 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
-          const uint32_t w_addr = smem_u32(wdq + (size_t)buf * WD_BYTES + (size_t)h2 * WD_SUB);
-          const uint32_t x_addr = smem_u32(raw + (size_t)((j0 + h2) % STAGES) * RAW_BYTES);
+          const uint32_t w_addr = smem_u32(hbuf + (size_t)buf * HB_BYTES + (size_t)h2 * WD_SUB);
+          const uint32_t x_addr = smem_u32(hbuf + (size_t)buf * HB_BYTES + WD_BYTES + (size_t)h2 * X_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             mma_f16(tmem + (uint32_t)(ab * TT), sdesc_k128(w_addr + 32 * kk), sdesc_k128(x_addr + 32 * kk), idesc,
                     kb > 0 || h2 > 0 || kk > 0);
         }
-        commit(&empty[j0 % STAGES]);
-        commit(&empty[(j0 + 1) % STAGES]);
         commit(&wd_empty[buf]);
         if (kb + 2 == KB) commit(&acc_full[ab]);
       }
