@@ -39,18 +39,18 @@ namespace e0pf {
 constexpr int WM = 128;                      // weight rows per tile: the MMA's M
 constexpr int TT = 64;                       // token rows per tile, at most: the MMA's N
 constexpr int BK = 64;                       // reduction block
-constexpr int STAGES = 10;                   // copy stages in flight: token rows and codes
+constexpr int STAGES = 14;                   // copy stages in flight: token rows and codes
 constexpr int NWD = 2;                       // dequantise -> MMA hand-over buffers
 constexpr int X_BYTES = TT * BK * 2;         // 8 KB of fp16 token rows
 constexpr int Q_BYTES = WM * BK / 2;         // 4 KB of int4 codes
 constexpr int RAW_BYTES = X_BYTES + Q_BYTES;
 constexpr int BKD = 2 * BK;                  // reduction block of one dequantise -> MMA hand-over
-constexpr int WD_SUB = WM * BK * 2;          // 16 KB: one 64-wide block of dequantised fp16 weights
-constexpr int WD_BYTES = WM * BKD * 2;       // 32 KB: two of them per hand-over buffer
-// A hand-over buffer holds the MMA's operands for two k-blocks: the dequantised weights
-// (A) and a copy of the token rows (B), so that the copy stage is free as soon as it has
-// been converted and only the hand-over buffers wait for the tensor core.
-constexpr int HB_BYTES = WD_BYTES + 2 * X_BYTES;
+// A hand-over carries the MMA's operands for two k-blocks: the dequantised weights (A) in
+// tensor memory, 64 columns (lane = weight row, two fp16 per column), and a copy of the
+// token rows (B) in shared memory, so that a copy stage is free as soon as it has been
+// converted and only the hand-over buffers wait for the tensor core.
+constexpr int A_COLS = BKD / 2;              // tensor-memory columns of one hand-over's weights
+constexpr int HB_BYTES = 2 * X_BYTES;        // 16 KB of token rows per hand-over buffer
 constexpr int EMAXP = 1024;
 // roles: warps 0..3 copy (job j by warp j % 4), warps 4..19 dequantise, warp 20 issues the
 // MMAs, warps 21..24 run the epilogue (tensor-memory lane quadrants 1, 2, 3, 0)
@@ -58,14 +58,16 @@ constexpr int W_COPY = 0, N_COPY = 4, W_DQ0 = 4, N_DQ = 16, W_MMA = 20, W_EPI0 =
 // the dequantising warps form two groups that take alternate hand-overs (buffer g for
 // group g), so that one group's proxy fence and hand-over overlap the other's work
 constexpr int DQ_GROUPS = 2, N_DQG = N_DQ / DQ_GROUPS;
-constexpr int DQ_PER_ROW = N_DQG * 32 / WM;  // dequantising threads per weight row in a group
-constexpr int DQ_WORDS = 8 / DQ_PER_ROW;     // code words (8 codes each) a thread converts per 64-wide block
+// warp i of a group writes tensor-memory lanes 32 (warp % 4) .. + 31 (the lane quadrant a
+// warp may access) and half i / 4 of each 64-wide k-block: 4 code words, 16 columns
+constexpr int TMEM_COLS = 2 * TT + NWD * A_COLS;
 constexpr int GT = 32 * (W_EPI0 + N_EPI);
 constexpr size_t GEMM_SMEM = 1024 + (size_t)STAGES * RAW_BYTES + NWD * HB_BYTES + 2 * (EMAXP + 1) * sizeof(int);
 static_assert(X_BYTES % 1024 == 0 && RAW_BYTES % 1024 == 0, "stages stay 1024-byte aligned");
 static_assert(2 * TT >= 32 && (2 * TT & (2 * TT - 1)) == 0, "tensor memory columns: a power of two >= 32");
 static_assert(GEMM_SMEM <= 227 * 1024, "shared memory");
-static_assert(N_DQG * 32 == DQ_PER_ROW * WM && 8 % DQ_PER_ROW == 0, "whole code words per dequantising thread");
+static_assert(N_DQG == 8 && WM == 128 && W_DQ0 % 4 == 0, "two warps per lane quadrant in a group, one per half block");
+static_assert(TMEM_COLS == 256, "tensor memory columns: a power of two >= 32");
 static_assert(NWD == DQ_GROUPS, "one hand-over buffer per dequantising group");
 static_assert(STAGES % 2 == 0, "a hand-over's two stages sit in one ring pass");
 static_assert(BKD % BK == 0 && BKD / BK == 2, "a hand-over covers two copy stages");
@@ -99,35 +101,24 @@ __device__ __forceinline__ __half2 bf16pair_to_h2(uint16_t v) {
   return __halves2half2(h, h);
 }
 
-// Dequantise DQ_WORDS code words (8 codes each) of a 64-code weight row segment, words
-// q*DQ_WORDS .. (q+1)*DQ_WORDS - 1, into the swizzled fp16 row: word m holds chunk m
-// (16 bytes of fp16), codes j and j + 4 of the word become one fp16 pair (1024 + c by
-// the exponent trick, then exactly c, then s*c + b).
-__device__ __forceinline__ void dequant_words(const uint8_t* codes, uint8_t* dst_row, int n, int q, __half2 s2,
-                                              __half2 b2) {
-  uint32_t words[DQ_WORDS];
-  if (DQ_WORDS == 4) {
-    const uint4 w0 = *reinterpret_cast<const uint4*>(codes);
-    words[0] = w0.x; words[1] = w0.y; words[2 % DQ_WORDS] = w0.z; words[3 % DQ_WORDS] = w0.w;
-  } else {
-    const uint2 w0 = *reinterpret_cast<const uint2*>(codes);
-    words[0] = w0.x; words[1 % DQ_WORDS] = w0.y;
-  }
+// Dequantise 32 codes (one uint4: half of a 64-code weight row segment) to 16 fp16 pairs:
+// codes j and j + 4 of each 8-code word become one pair (1024 + c by the exponent trick,
+// then exactly c, then s*c + b), which is the element order [0,4,1,5,2,6,3,7] within
+// every group of 8 that the token rows use as well.
+__device__ __forceinline__ void dequant32(const uint8_t* codes, __half2 s2, __half2 b2, uint32_t (&out)[16]) {
+  const uint4 w0 = *reinterpret_cast<const uint4*>(codes);
+  const uint32_t words[4] = {w0.x, w0.y, w0.z, w0.w};
   const __half2 magic = __halves2half2(__ushort_as_half((unsigned short)0x6400), __ushort_as_half((unsigned short)0x6400));
 #pragma unroll
-  for (int mm = 0; mm < DQ_WORDS; ++mm) {
-    const int m = DQ_WORDS * q + mm;
-    uint32_t out[4];
+  for (int mm = 0; mm < 4; ++mm)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const uint32_t t = ((words[mm] >> (4 * j)) & 0x000F000Fu) | 0x64006400u;
       __half2 c = *reinterpret_cast<const __half2*>(&t);
       c = __hsub2(c, magic);
       const __half2 w = __hfma2(c, s2, b2);
-      out[j] = *reinterpret_cast<const uint32_t*>(&w);
+      out[4 * mm + j] = *reinterpret_cast<const uint32_t*>(&w);
     }
-    *reinterpret_cast<uint4*>(dst_row + ((m ^ (n & 7)) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
-  }
 }
 
 __device__ __forceinline__ void cp_async_bar_arrive(uint64_t* bar) {
@@ -146,7 +137,7 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
   uint8_t* raw = sm;                                // STAGES x [token rows | codes]
-  uint8_t* hbuf = sm + (size_t)STAGES * RAW_BYTES;  // NWD x [dequantised weights | token rows]
+  uint8_t* hbuf = sm + (size_t)STAGES * RAW_BYTES;  // NWD x token rows of a hand-over
   int* s_row = reinterpret_cast<int*>(hbuf + NWD * HB_BYTES);
   int* s_tile = s_row + (EMAXP + 1);
   __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], wd_full[NWD], wd_empty[NWD], acc_full[2], acc_empty[2], fin;
@@ -176,7 +167,7 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
     fence_mbar_init();
     s_abort = 0;
   }
-  if (warp == W_MMA) tmem_alloc(&tmem_slot, 2 * TT);
+  if (warp == W_MMA) tmem_alloc(&tmem_slot, TMEM_COLS);
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
@@ -252,9 +243,10 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
     cp_async_wait<0>();
   } else if (warp >= W_DQ0 && warp < W_DQ0 + N_DQ) {
     // ---------------- dequantisation: group grp takes hand-overs p = grp, grp + 2, ...;
-    // DQ_PER_ROW consecutive threads of the group own weight row n
+    // a thread owns weight row n (its tensor-memory lane) and half h of each 64-wide block
     const int dt = tid - 32 * W_DQ0, grp = dt / (32 * N_DQG), gtid = dt % (32 * N_DQG);
-    const int n = gtid / DQ_PER_ROW, h = gtid % DQ_PER_ROW;
+    const int n = 32 * (warp & 3) + lane, h = (gtid >> 5) >> 2;
+    const uint32_t a_lane = (uint32_t)(32 * (warp & 3)) << 16;
     // scales and biases of this row for the two k-blocks of hand-over p (prefetched two
     // hand-overs of the group ahead); the tile of the last fetch is cached
     int t_i = -1;
@@ -278,30 +270,41 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
         bv[u] = __ldg(g.b + idx);
       }
     };
-    uint16_t cs[2], cb[2], ns[2], nb[2];
+    // three hand-overs of scales in flight: current, next and the one after
+    uint16_t cs[2], cb[2], ns[2], nb[2], ms[2], mb[2];
     fetch(grp, cs, cb);
     fetch(grp + DQ_GROUPS, ns, nb);
+    fetch(grp + 2 * DQ_GROUPS, ms, mb);
+    int x_i = -1, x_bytes = X_BYTES;  // token-row bytes to hand over: the tile's rows rounded to 16
     for (int p = grp; 2 * p < jobs; p += DQ_GROUPS) {
       const int j0 = 2 * p, buf = p % NWD;  // this group's buffer: p % NWD == grp
+      if (j0 / KB != x_i) {
+        x_i = j0 / KB;
+        x_bytes = ((tile_of(x_i).rows + 15) & ~15) * 128;
+      }
       if (!wait(&full[j0 % STAGES], (j0 / STAGES) & 1)) break;
       if (!wait(&full[(j0 + 1) % STAGES], ((j0 + 1) / STAGES) & 1)) break;
       if (p >= NWD && !wait(&wd_empty[buf], (p / NWD - 1) & 1)) break;
+      fence_after_sync();  // the MMAs that read this buffer's tensor memory are complete
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2)
-        dequant_words(raw + (size_t)((j0 + h2) % STAGES) * RAW_BYTES + X_BYTES + n * 32 + h * 4 * DQ_WORDS,
-                      hbuf + (size_t)buf * HB_BYTES + (size_t)h2 * WD_SUB + n * 128, n, h, bf16pair_to_h2(cs[h2]),
-                      bf16pair_to_h2(cb[h2]));
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t w[16];
+        dequant32(raw + (size_t)((j0 + h2) % STAGES) * RAW_BYTES + X_BYTES + n * 32 + h * 16, bf16pair_to_h2(cs[h2]),
+                  bf16pair_to_h2(cb[h2]), w);
+        tmem_st16(tmem + a_lane + (uint32_t)(2 * TT + buf * A_COLS + h2 * (A_COLS / 2) + h * 16), w);
+      }
       // token rows of both k-blocks into the hand-over buffer (16-byte chunks keep their
-      // swizzled places; rows past the tile's are copied too and never read back)
+      // swizzled places; the MMA reads the tile's rows rounded up to 16)
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
         const uint4* src = reinterpret_cast<const uint4*>(raw + (size_t)((j0 + h2) % STAGES) * RAW_BYTES);
-        uint4* dst = reinterpret_cast<uint4*>(hbuf + (size_t)buf * HB_BYTES + WD_BYTES + (size_t)h2 * X_BYTES);
-#pragma unroll
-        for (int c = gtid; c < X_BYTES / 16; c += 32 * N_DQG) dst[c] = src[c];
+        uint4* dst = reinterpret_cast<uint4*>(hbuf + (size_t)buf * HB_BYTES + (size_t)h2 * X_BYTES);
+        for (int c = gtid; c < x_bytes / 16; c += 32 * N_DQG) dst[c] = src[c];
       }
-      // these weights and token rows are read by the tensor core (async proxy)
+      // the weights (tensor memory) and token rows (async proxy) are read by the tensor core
+      tmem_st_wait();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      fence_before_sync();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&wd_full[buf]);
@@ -312,39 +315,45 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
       for (int u = 0; u < 2; ++u) {
         cs[u] = ns[u];
         cb[u] = nb[u];
+        ns[u] = ms[u];
+        nb[u] = mb[u];
       }
-      fetch(p + 2 * DQ_GROUPS, ns, nb);
+      fetch(p + 3 * DQ_GROUPS, ms, mb);
     }
   } else if (warp == W_MMA) {
-    // ---------------- one thread issues the MMAs of every job and commits them
-    if (lane == 0) {
-      int cur_i = -1;
-      Tile T{};
-      uint32_t idesc = 0;
-      for (int p = 0; 2 * p < jobs; ++p) {
-        const int j0 = 2 * p, kb = j0 % KB, buf = p % NWD;
-        const int i = j0 / KB, ab = i & 1;
-        if (i != cur_i) {
-          cur_i = i;
-          T = tile_of(i);
-          idesc = idesc_f16_f32(WM, (T.rows + 15) & ~15);
-          if (i >= 2 && !wait(&acc_empty[ab], ((i >> 1) - 1) & 1)) break;  // epilogue done with this accumulator
-        }
-        if (!wait(&wd_full[buf], (p / NWD) & 1)) break;
-        fence_after_sync();
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    // ---------------- the MMA warp: every lane walks the hand-overs (operand addresses
+    // stay warp-uniform), one elected lane issues the MMAs and commits them
+    int cur_i = -1;
+    Tile T{};
+    uint32_t idesc = 0;
+    for (int p = 0; 2 * p < jobs; ++p) {
+      const int j0 = 2 * p, kb = j0 % KB, buf = p % NWD;
+      const int i = j0 / KB, ab = i & 1;
+      if (i != cur_i) {
+        cur_i = i;
+        T = tile_of(i);
+        idesc = idesc_f16_f32(WM, (T.rows + 15) & ~15);
+        // the epilogue is done with this accumulator
+        if (!__all_sync(0xffffffffu, i < 2 || wait(&acc_empty[ab], ((i >> 1) - 1) & 1))) break;
+      }
+      if (!__all_sync(0xffffffffu, wait(&wd_full[buf], (p / NWD) & 1))) break;
+      fence_after_sync();
+      if (elect_one()) {
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
-          const uint32_t w_addr = smem_u32(hbuf + (size_t)buf * HB_BYTES + (size_t)h2 * WD_SUB);
-          const uint32_t x_addr = smem_u32(hbuf + (size_t)buf * HB_BYTES + WD_BYTES + (size_t)h2 * X_BYTES);
+          const uint32_t a_col = tmem + (uint32_t)(2 * TT + buf * A_COLS + h2 * (A_COLS / 2));
+          const uint64_t xd = sdesc_k128(smem_u32(hbuf + (size_t)buf * HB_BYTES + (size_t)h2 * X_BYTES));
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            mma_f16(tmem + (uint32_t)(ab * TT), sdesc_k128(w_addr + 32 * kk), sdesc_k128(x_addr + 32 * kk), idesc,
-                    kb > 0 || h2 > 0 || kk > 0);
+          for (int kk = 0; kk < BK / 16; ++kk)  // a 16-wide k step: 8 columns of A, 32 bytes of B
+            mma_f16_ta(tmem + (uint32_t)(ab * TT), a_col + (uint32_t)(8 * kk), xd + (uint64_t)(2 * kk), idesc,
+                       kb > 0 || h2 > 0 || kk > 0);
         }
         commit(&wd_empty[buf]);
         if (kb + 2 == KB) commit(&acc_full[ab]);
       }
+      __syncwarp();
+    }
+    if (elect_one()) {
       commit(&fin);  // every MMA issued so far has completed when this arrives
       const uint64_t t0 = globaltimer();
       while (!mbar_try_wait(&fin, 0) && globaltimer() - t0 < g.timeout_ns) {
@@ -396,7 +405,7 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  if (warp == W_MMA) tmem_dealloc(tmem, 2 * TT);
+  if (warp == W_MMA) tmem_dealloc(tmem, TMEM_COLS);
 }
 
 // ------------------------------------------------------------------ small kernels
