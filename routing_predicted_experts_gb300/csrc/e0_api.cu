@@ -208,17 +208,34 @@ e0_status build_plan(const PlanSpec& s, int ncta, Unit* units, uint8_t* counts, 
     }
     n_slabs = idx;
   }
-  // 2. divisible work as granules: the layer's own (crit) and the prerouter's (def)
+  // 2. split (layers with a head, when there is room): the layer's own LoRA work on CTAs
+  //    beside the expert ones: 64 LoRA base rows (one consumer stage group) per CTA, and
+  //    a few CTAs that each compute all of v = A x and the B v of a slice of the rows (no
+  //    CTA waits for another's v); the prerouter's work (HEAD, LRES: needed only by the
+  //    next token) on the rest
+  const int qstage = q4_rows_per_stage(d);
+  const bool has_def = s.lres || s.head;
+  const int n_q = s.lora ? (s.lout + 4 * qstage - 1) / (4 * qstage) : 0;
+  // B slices of one stage each: rows in multiples of 16 with lr * rows * 2 <= STAGE_BYTES
+  const int b_rows = s.lora_ab && s.lr > 0 ? std::max(16, (STAGE_BYTES / (2 * s.lr)) / 16 * 16) : 0;
+  const int n_ab = s.lora_ab && s.lr > 0 ? std::max(1, (s.lout + b_rows - 1) / b_rows) : 0;
+  const int n_own = n_q + n_ab;
+  const bool split = defer && has_def && !s.router && n_slabs > 0 && n_slabs + n_own <= ncta - 8;
+  const int n_crit = split ? n_slabs + n_own : ncta;
+  // 3. divisible work as granules: the layer's own (crit) and the prerouter's (def)
   std::vector<Granule> crit, def;
   // the LoRA down projection first: the CTAs that own LoRA base rows wait for its v
-  // (its cost adds the latency of publishing v: a CTA of its own, as a rule)
-  // in slices of 4 ranks on CTAs of their own, so that v is published early
+  // (its cost adds the latency of publishing v), in slices of 4 ranks so that v is
+  // published early
   if (s.lora_ab)
     for (int q = 0; q < s.lr; q += 4)
       crit.push_back({U_LORA_A, q, std::min(4, s.lr - q), W_BF16 * 2.0 * d * std::min(4, s.lr - q) + 4.0 * UNIT_COST});
+  const int qg = split ? 4 * qstage : qstage;
   if (s.lora)
-    for (int r = 0; r < s.lout; r += 16)
-      crit.push_back({U_QROWS, r, 16, W_QROWS * 16.0 * q4_row_bytes(d) + W_BF16 * 16.0 * 2.0 * s.lr});
+    for (int r = 0; r < s.lout; r += qg) {
+      const int nr = std::min(qg, s.lout - r);
+      crit.push_back({U_QROWS, r, nr, W_QROWS * nr * (double)q4_row_bytes(d) + W_BF16 * nr * 2.0 * s.lr});
+    }
   if (s.router)
     for (int e = 0; e < s.E; e += 8) crit.push_back({U_ROUTER, e, 8, W_BF16 * 8.0 * 2.0 * d});
   if (s.lres)
@@ -226,20 +243,39 @@ e0_status build_plan(const PlanSpec& s, int ncta, Unit* units, uint8_t* counts, 
   if (s.head)
     for (int i = 0; i < s.H; i += 8)
       def.push_back({U_HEAD, i, 8, W_BF16 * 8.0 * (2.0 * d + 2.0 * s.E + 2.0 * (1 + 2 * s.K))});
-  // 3. split: enough CTAs beside the expert ones for the layer's own work at the load
-  //    of an expert CTA; the rest take the prerouter's work
-  int n_crit = ncta;
-  if (defer && !def.empty() && n_slabs > 0 && n_slabs < ncta) {
-    double c_crit = 0.0;
-    for (auto& g : crit) c_crit += g.cost;
-    // a CTA of LoRA rows carries two units (rows, then B), an expert CTA one
-    const int n_own = (int)std::ceil(c_crit / std::max(c_exp - 2.0 * UNIT_COST, 1.0));
-    if (n_slabs + n_own <= ncta - 8) n_crit = std::min(ncta, n_slabs + n_own);
-  }
   const int limit = crit_limit > 0 ? std::min(crit_limit, ncta) : ncta;
-  if (n_crit < ncta) {
-    waterfill(s, crit, 0, n_crit, load, lists);
-    waterfill(s, def, n_crit, ncta, load, lists);
+  if (split) {
+    for (int i = 0; i < n_ab; ++i) {  // all ranks of v, then the B rows of an even slice
+      auto& L = lists[n_slabs + i];
+      const int r0 = (int)((long long)s.lout * i / n_ab) / 16 * 16;
+      const int r1 = i + 1 == n_ab ? s.lout : (int)((long long)s.lout * (i + 1) / n_ab) / 16 * 16;
+      L.push_back(Unit{U_LORA_A, 0, 0, (uint16_t)s.lr, UF_LOCAL_V});
+      L.push_back(Unit{U_LORA_B, 0, (uint16_t)r0, (uint16_t)r1, 0});
+    }
+    for (int i = 0; i < n_q; ++i) {
+      const int r0 = i * 4 * qstage, r1 = std::min(s.lout, r0 + 4 * qstage);
+      lists[n_slabs + n_ab + i].push_back(Unit{U_QROWS, 0, (uint16_t)r0, (uint16_t)r1, 0});
+    }
+    // the prerouter's rows in contiguous runs, LRES on the first CTAs of the pool and
+    // HEAD on the rest, the CTA counts in proportion to the bytes (a head unit has three
+    // dependent phases and a high fixed cost: one run per CTA, split only at HEAD_ROWS)
+    const int n_def = ncta - n_crit;
+    double c_l = 0.0, c_h = 0.0;
+    for (auto& g : def) (g.type == U_LRES ? c_l : c_h) += g.cost;
+    int n_l = c_l > 0.0 ? (int)std::lround(n_def * c_l / (c_l + c_h)) : 0;
+    if (c_l > 0.0) n_l = std::max(1, std::min(n_l, n_def - (c_h > 0.0 ? 1 : 0)));
+    const int n_h = n_def - n_l;
+    auto spread = [&](uint8_t type, int rows, int c0, int nc) {
+      if (rows <= 0 || nc <= 0) return;
+      const int gran = 8, ng = (rows + gran - 1) / gran;
+      for (int i = 0; i < nc; ++i) {
+        const int g0 = (int)((long long)ng * i / nc), g1 = (int)((long long)ng * (i + 1) / nc);
+        for (int r = g0 * gran; r < std::min(rows, g1 * gran); r += HEAD_ROWS)
+          lists[c0 + i].push_back(Unit{type, 0, (uint16_t)r, (uint16_t)std::min({rows, g1 * gran, r + HEAD_ROWS}), 0});
+      }
+    };
+    spread(U_LRES, s.lres ? s.E : 0, n_crit, n_l);
+    spread(U_HEAD, s.head ? s.H : 0, n_crit + n_l, n_h);
   } else {
     std::vector<Granule> all(crit);
     all.insert(all.end(), def.begin(), def.end());

@@ -46,6 +46,7 @@ struct Ctl {
   uint8_t defer[KINDS_MAX];   // per plan kind: this CTA holds only prerouter work
   int32_t sn[KINDS_MAX];
   uint32_t rt_tag[LMAX];      // staged: epoch each committed route is for
+  int32_t lv_layer;           // layer whose LoRA v (all ranks) this CTA computed into lvs, else -1
 };
 
 // Dynamic shared memory: the stage ring, the control block, then a copy of the
@@ -560,6 +561,58 @@ __device__ __forceinline__ void issue_q4_rows(Prod& pr, const uint32_t* q, const
   ++pr.n;
 }
 
+// Per-lane bounded wait until stage m's slot is free (lanes of the copy warp wait on
+// different slots at once).  False after an abort or a timeout.
+__device__ __forceinline__ bool lane_wait_slot(Prod& pr, uint32_t m) {
+  const uint32_t round = m / NSTAGES;
+  if (round == 0) return true;
+  uint64_t* bar = &pr.C.empty[m % NSTAGES];
+  const uint32_t par = (round - 1) & 1u;
+  if (mbar_try_wait(bar, par)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, par)) return true;
+    if ((it & 15u) == 0) {
+      if (aborted(pr.P, pr.C)) return false;
+      if (globaltimer() - t0 > pr.P.timeout_ns) {
+        raise_error(pr.P, pr.C, E0_DEV_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Issue stages pr.n .. pr.n + nst - 1 (nst <= NSTAGES: distinct slots) at once, lane i
+// taking stage pr.n + i:
+// stage i < nq holds int4 rows [row0 + i * per, ...) of a row-layout matrix (in columns);
+// the rest come from `extra` (a callable issuing stage i's copies into its slot).
+template <class Extra>
+__device__ __forceinline__ void issue_parallel(Prod& pr, int nst, int nq, const uint32_t* q, const uint16_t* s,
+                                               const uint16_t* b, int in, int row0, int row1, Extra extra) {
+  if (!pr.ok) return;
+  bool ok = true;
+  if (pr.lane < nst) {
+    const uint32_t m = pr.n + (uint32_t)pr.lane, slot = m % NSTAGES;
+    ok = lane_wait_slot(pr, m);
+    if (ok) {
+      uint8_t* st = pr.ring + (size_t)slot * STAGE_BYTES;
+      if (pr.lane < nq) {
+        const int per = q4_rows_per_stage(in);
+        const int r = row0 + pr.lane * per, nr = min(per, row1 - r);
+        const uint32_t qb = (uint32_t)nr * in / 2, sb = (uint32_t)nr * in / 32;
+        mbar_arrive_expect_tx(&pr.C.full[slot], qb + 2 * sb);
+        tma_bulk_g2s(st, q + (size_t)r * (in / 8), qb, &pr.C.full[slot]);
+        tma_bulk_g2s(st + qb, s + (size_t)r * (in / 64), sb, &pr.C.full[slot]);
+        tma_bulk_g2s(st + qb + sb, b + (size_t)r * (in / 64), sb, &pr.C.full[slot]);
+      } else {
+        extra(pr.lane, st, &pr.C.full[slot]);
+      }
+    }
+  }
+  if (!__all_sync(0xffffffffu, ok)) pr.ok = false;
+  pr.n += (uint32_t)nst;
+}
+
 __device__ __forceinline__ void issue_bytes(Prod& pr, const void* src, uint32_t bytes) {
   if (!pr.ok) return;
   uint32_t slot;
@@ -599,31 +652,28 @@ __device__ __forceinline__ void issue_unit(Prod& pr, const LayerDesc& Ld, const 
       const uint16_t* gus = at(shared ? Ld.sgu_s : Ld.gu_s, (size_t)(2 * P.F) * (d / 64));
       const uint16_t* gub = at(shared ? Ld.sgu_b : Ld.gu_b, (size_t)(2 * P.F) * (d / 64));
       const int per = q4_rows_per_stage(d);
-      for (int r = 64 * u.r0; r < 64 * u.r0 + 64; r += per)
-        issue_q4_rows(pr, guq, gus, gub, d, r, min(per, 64 * u.r0 + 64 - r));
       const uint32_t* dq = at(shared ? Ld.sdn_q : Ld.dn_q, (size_t)(P.F / 32) * d * 4) + (size_t)u.r0 * d * 4;
       const uint16_t* ds = at(shared ? Ld.sdn_s : Ld.dn_s, (size_t)(P.F / 64) * d) + (size_t)(u.r0 >> 1) * d;
       const uint16_t* db = at(shared ? Ld.sdn_b : Ld.dn_b, (size_t)(P.F / 64) * d) + (size_t)(u.r0 >> 1) * d;
       const int pd = dn_rows_per_stage(d);
-      for (int i0 = 0; i0 < d; i0 += pd) {
-        const int nr = min(pd, d - i0);
-        if (!pr.ok) return;
-        uint32_t slot;
-        uint8_t* st = prod_begin(pr, slot);
-        if (!st) return;
-        if (pr.lane == 0) {
-          mbar_arrive_expect_tx(&C.full[slot], (uint32_t)nr * 20);
-          tma_bulk_g2s(st, dq + (size_t)i0 * 4, nr * 16, &C.full[slot]);
-          tma_bulk_g2s(st + nr * 16, ds + i0, nr * 2, &C.full[slot]);
-          tma_bulk_g2s(st + nr * 18, db + i0, nr * 2, &C.full[slot]);
-        }
-        ++pr.n;
-      }
+      const int ngu = (64 + per - 1) / per, ndn = (d + pd - 1) / pd;
+      // the gate/up stages and the down-projection stages of the slab, one lane each
+      issue_parallel(pr, ngu + ndn, ngu, guq, gus, gub, d, 64 * u.r0, 64 * u.r0 + 64,
+                     [&](int i, uint8_t* st, uint64_t* full) {
+                       const int i0 = (i - ngu) * pd, nr = min(pd, d - i0);
+                       mbar_arrive_expect_tx(full, (uint32_t)nr * 20);
+                       tma_bulk_g2s(st, dq + (size_t)i0 * 4, nr * 16, full);
+                       tma_bulk_g2s(st + nr * 16, ds + i0, nr * 2, full);
+                       tma_bulk_g2s(st + nr * 18, db + i0, nr * 2, full);
+                     });
       break;
     }
     case U_QROWS: {
       const int per = q4_rows_per_stage(d);
-      for (int r = u.r0; r < u.r1; r += per) issue_q4_rows(pr, Ld.lw_q, Ld.lw_s, Ld.lw_b, d, r, min(per, u.r1 - r));
+      for (int r0 = u.r0; r0 < u.r1; r0 += NSTAGES * per) {  // up to a ring's worth of stages at once
+        const int r1 = min((int)u.r1, r0 + NSTAGES * per), nst = (r1 - r0 + per - 1) / per;
+        issue_parallel(pr, nst, nst, Ld.lw_q, Ld.lw_s, Ld.lw_b, d, r0, r1, [](int, uint8_t*, uint64_t*) {});
+      }
       break;
     }
     case U_LORA_B: {
@@ -1141,7 +1191,7 @@ __device__ __forceinline__ void consume_unit(Cons& cs, const LayerDesc& Ld, cons
       // (alpha/r) B v for rows [r0, r1), once every rank of v is published: warp 0
       // polls the launch-tagged words of v (one round trip when they are there)
       const uint32_t par = C.epoch & 1u;
-      if (cs.cw == 0) {
+      if (cs.cw == 0 && C.lv_layer != l) {  // (v computed on this CTA is already in lvs)
         const uint64_t* lvp = lv_ptr(P, par, l);
         const uint32_t tag = C.epoch + 1u;
         const uint64_t t0 = globaltimer();
@@ -1200,7 +1250,14 @@ __device__ __forceinline__ void consume_unit(Cons& cs, const LayerDesc& Ld, cons
       // (each rank's value goes out as a launch-tagged word: no counter, no fence)
       const uint32_t par = C.epoch & 1u;
       const int n = u.r1 - u.r0;
-      consume_bf_rows<D>(cs, n, BF_TAGGED, reinterpret_cast<float*>(lv_ptr(P, par, l) + u.r0), nullptr);
+      if (u.flags & UF_LOCAL_V) {
+        // every rank, for this CTA's own B rows only (no other CTA holds B rows): v stays
+        // in shared memory
+        consume_bf_rows<D>(cs, n, BF_SMEM, C.lvs, nullptr);
+        if (tid == 0) C.lv_layer = l;
+      } else {
+        consume_bf_rows<D>(cs, n, BF_TAGGED, reinterpret_cast<float*>(lv_ptr(P, par, l) + u.r0), nullptr);
+      }
       break;
     }
     case U_HEAD: {
@@ -1535,6 +1592,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) engine_kernel(const __grid_consta
     for (int l = 0; l < LMAX; ++l) C.rt_ready[l] = 0;
     C.abort_flag = 0;
     C.is_last = 0;
+    C.lv_layer = -1;
     C.epoch = *reinterpret_cast<volatile uint32_t*>(&hdr(P)->epoch);
   }
   __syncthreads();

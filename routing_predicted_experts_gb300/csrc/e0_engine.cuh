@@ -15,9 +15,11 @@
 //             to 32 columns of its SwiGLU width: 32 gate rows + 32 up rows give 32
 //             activations a = silu(g) * u, which the matching 32-column slab of the
 //             down projection turns into a contribution to all d outputs;
-//   U_QROWS   rows of the LoRA base W;  U_LORA_A  a slice of ranks of the LoRA down
-//             projection, v = A x, published to the other CTAs;  U_LORA_B  (alpha/r) B v
-//             for LoRA rows once v is published (last on its CTA, so v is rarely waited for);  U_HEAD  rows of prerouter fc1 (plus the one-hot
+//   U_QROWS   rows of the LoRA base W;  U_LORA_A  ranks of the LoRA down projection,
+//             v = A x: all of them kept in shared memory for the CTA's own B rows, or a
+//             slice published to the other CTAs;  U_LORA_B  (alpha/r) B v for LoRA rows
+//             once v is there (last on its CTA, so v is rarely waited for);
+//   U_HEAD    rows of prerouter fc1 (plus the one-hot
 //             columns picked by the committed ids), erf-GELU, then the matching rows
 //             of fc2^T;  U_LRES  rows of the head's linear residual;  U_ROUTER  rows
 //             of a layer's own gate.
@@ -35,6 +37,7 @@ constexpr int NTHREADS = (NCW + 2) * 32;      // + producer warp + routing warp
 constexpr int NCT = NCW * 32;                 // consumer threads
 constexpr int STAGE_BYTES = 20480;
 constexpr int NSTAGES = 9;
+static_assert(NSTAGES <= 32, "the copy warp issues up to a ring's worth of stages with one lane each");
 constexpr int KMAX = 16;
 constexpr int EMAX = 1024;
 constexpr int DMAX = 2048;
@@ -47,6 +50,8 @@ constexpr int KINDS_MAX = 3;
 constexpr int LMAX = 64;                      // layers per launch
 constexpr float RMS_EPS = 1e-6f;
 
+constexpr uint16_t UF_LOCAL_V = 1;
+
 enum UnitType : uint8_t { U_NONE = 0, U_EXPERT, U_QROWS, U_LORA_A, U_HEAD, U_LRES, U_ROUTER, U_LORA_B };
 
 struct Unit {
@@ -54,7 +59,7 @@ struct Unit {
   uint8_t k;       // U_EXPERT: expert slot (k == K: shared expert)
   uint16_t r0;     // first row / slab / rank
   uint16_t r1;     // end row / rank (exclusive)
-  uint16_t pad;
+  uint16_t flags;   // U_LORA_A: UF_LOCAL_V = v stays in this CTA's shared memory (its own B rows)
 };
 static_assert(sizeof(Unit) == 8, "Unit must stay 8 bytes");
 
