@@ -354,10 +354,23 @@ e0_status e0_debug_inject_stall(void* workspace, uint64_t limit_ns, e0_stream st
  * %globaltimer stamps to buf[cta][layer][16] (u64, zero-filled device memory of at
  * least ncta * layers * 128 bytes; ncta <= 160).  Slots: 0 consumer layer start,
  * 1 layer dependency satisfied, 2 layer input built, 3 layer's units done,
- * 4 producer published the layer's routing, 5 producer issued the layer's last copy,
- * 6 ns consumer warp 0 waited for stages, 7 stages it took, 8 + unit type: ns spent
- * in units of that type (accumulated).  buf == NULL switches tracing off. */
+ * 4 routing warp published the layer's routing, 5 copy warp issued the layer's last
+ * copy, 6 ns consumer warp 0 waited for stages, 7 stages it took, 8 own-gate routing
+ * started, 8 + unit type: ns spent in units of that type (accumulated; for U_ROUTER = 6
+ * the time this CTA's gate rows were published).  buf == NULL switches tracing off. */
 e0_status e0_debug_trace(uint64_t* buf, size_t bytes);
+
+/* Debug / tests: the CTA work plan a stack of 35B-class-shaped layers would use, built
+ * on the host (no device needed), for one layer kind: 0 a layer with a prerouter head
+ * (routed and shared experts, d x d LoRA linear of rank lr, head of H fc1 rows), 1 the
+ * same without a head, 2 the own-gate router rows (over the CTAs that kind 0 leaves on
+ * the critical path).  units_out: ncta * 8 units of 8 bytes, {type u8, k u8, r0 u16,
+ * r1 u16, flags u16}, unit types as in the engine (1 expert slab, 2 LoRA base rows,
+ * 3 LoRA A ranks, 4 head fc1 rows, 5 head residual rows, 6 gate rows, 7 LoRA B rows);
+ * counts_out[ncta] units per CTA; defer_out[ncta] = 1 where a CTA holds only
+ * prerouter work.  ncta <= 160. */
+e0_status e0_debug_plan(int32_t d, int32_t E, int32_t F, int32_t K, int32_t H, int32_t lr, int32_t ncta,
+                        int32_t kind, void* units_out, uint8_t* counts_out, uint8_t* defer_out);
 
 #ifdef __cplusplus
 }

@@ -92,6 +92,7 @@ PROTOTYPES = {
     "e0_synth_normal": (i32, [vp, i64, u64, u32, i64, f64, i32, vp]),
     "e0_debug_inject_stall": (i32, [vp, u64, vp]),
     "e0_debug_trace": (i32, [vp, sz]),
+    "e0_debug_plan": (i32, [i32, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp]),
 }
 
 _lib = None

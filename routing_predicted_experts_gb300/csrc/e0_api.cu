@@ -430,6 +430,33 @@ extern "C" e0_status e0_get_device_status(const void* ws, uint32_t* status_out, 
   return E0_OK;
 }
 
+extern "C" e0_status e0_debug_plan(int32_t d, int32_t E, int32_t F, int32_t K, int32_t H, int32_t lr, int32_t ncta,
+                                   int32_t kind, void* units_out, uint8_t* counts_out, uint8_t* defer_out) {
+  E0_REQUIRE(units_out && counts_out && defer_out, E0_ERR_INVALID, "e0_debug_plan: NULL argument");
+  E0_REQUIRE(ncta >= 1 && ncta <= MAX_CTAS && kind >= 0 && kind <= 2, E0_ERR_INVALID, "e0_debug_plan: ncta or kind");
+  E0_REQUIRE(d > 0 && d % 256 == 0 && E >= 1 && F % 32 == 0 && K >= 1 && K <= E && lr >= 0 && lr <= RANKS_MAX &&
+                 H >= 0 && H % 8 == 0,
+             E0_ERR_SHAPE, "e0_debug_plan: shape");
+  PlanSpec ps;
+  ps.d = d; ps.E = E; ps.F = F; ps.K = K;
+  ps.routed = ps.shared = ps.lora = true;
+  ps.lora_ab = lr > 0; ps.lr = lr; ps.lout = d;
+  if (kind == 0) { ps.head = H > 0; ps.lres = true; ps.H = H; }
+  std::memset(units_out, 0, sizeof(Unit) * (size_t)ncta * MAXU);
+  std::memset(defer_out, 0, (size_t)ncta);
+  Unit* u = static_cast<Unit*>(units_out);
+  if (kind < 2) return build_plan(ps, ncta, u, counts_out, kind == 0 ? defer_out : nullptr);
+  std::vector<Unit> tmp((size_t)ncta * MAXU);
+  std::vector<uint8_t> tc(ncta), td(ncta);
+  int n_crit = ncta;
+  ps.head = H > 0; ps.lres = true; ps.H = H;
+  e0_status st = build_plan(ps, ncta, tmp.data(), tc.data(), td.data(), &n_crit);
+  if (st) return st;
+  PlanSpec rs;
+  rs.d = d; rs.E = E; rs.F = F; rs.K = K; rs.router = true;
+  return build_plan(rs, ncta, u, counts_out, nullptr, nullptr, n_crit);
+}
+
 extern "C" e0_status e0_debug_trace(uint64_t* buf, size_t bytes) {
   E0_REQUIRE(!buf || bytes >= 8, E0_ERR_INVALID, "e0_debug_trace: buffer too small");
   g_trace = buf;
