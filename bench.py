@@ -64,8 +64,10 @@ def _kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def _traffic_per_launch():
-    """dram bytes per launch from the committed ncu summary, if taken on this kernel source."""
+def _traffic_per_launch(bytes_per_token):
+    """DRAM bytes per launch: the committed ncu capture's traffic / algorithmic ratio (4-layer
+    stack) times this workload's algorithmic bytes, if the capture was taken on this kernel
+    source (every weight byte streams once per token, so traffic scales with them)."""
     p = os.path.join(ROOT, "profiles", "engine_stack_traffic.txt")
     if not os.path.exists(p):
         return None
@@ -76,8 +78,8 @@ def _traffic_per_launch():
             kv[k.strip()] = v.strip()
     if kv.get("kernel_src_sha") != _kernel_source_hash():
         return None
-    v = kv.get("dram_bytes_per_launch_40_layers")
-    return int(v) if v else None
+    v = kv.get("traffic_over_algorithmic")
+    return int(round(float(v) * bytes_per_token)) if v else None
 
 
 class ClockSampler:
@@ -612,7 +614,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
             "frac_of_nominal_8tbs": round(achieved / 8000.0, 4),
             "kernel": "e0eng::engine_kernel<2048> (stack mode), one launch per token",
-            "traffic": _traffic_per_launch(),
+            "traffic": _traffic_per_launch(bpt),
         },
         "e2e": {"value": round(e2e_tok_s, 1), "unit": "tok/s",
                 "h2d_bytes_per_step": int(h0_dev.numel() * 2 + incr_dev.numel() * 2),
