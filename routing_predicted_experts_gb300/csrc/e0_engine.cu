@@ -204,7 +204,7 @@ __device__ __forceinline__ float quant_chunk32(const float* v, uint32_t* xp, flo
     s += v[i];
   }
   *sum = s;
-  const float r = m > 0.f ? 32767.0f / m : 0.f;
+  const float r = m > 0.f ? __fdividef(32767.0f, m) : 0.f;
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
     int q[8];
@@ -218,7 +218,7 @@ __device__ __forceinline__ float quant_chunk32(const float* v, uint32_t* xp, flo
     xp[4 * g + 2] = (uint32_t)(q[1] & 0xFFFF) | ((uint32_t)q[3] << 16);
     xp[4 * g + 3] = (uint32_t)(q[5] & 0xFFFF) | ((uint32_t)q[7] << 16);
   }
-  return m > 0.f ? m / 32767.0f : 0.f;
+  return m * (1.0f / 32767.0f);
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
@@ -1137,8 +1137,8 @@ __device__ __forceinline__ void consume_unit(Cons& cs, const LayerDesc& Ld, cons
         // floats order like their values, so an unsigned max reduction finds it).
         const float a = ab[cs.lane];
         const float m = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(a))));
-        const float r = m > 0.f ? 32767.0f / m : 0.f;
-        const float ainv = m > 0.f ? m / 32767.0f : 0.f;
+        const float r = m > 0.f ? __fdividef(32767.0f, m) : 0.f;
+        const float ainv = m * (1.0f / 32767.0f);
         int q = __float2int_rn(a * r);
         q = q > 32767 ? 32767 : (q < -32767 ? -32767 : q);
         const float asum = (float)__reduce_add_sync(0xffffffffu, q) * ainv;
@@ -1365,10 +1365,12 @@ __device__ __forceinline__ void layer_input(Cons& cs, int l, uint32_t par, const
     tot += C.red[w];
     mxb = max(mxb, C.redm[w]);
   }
-  const float scale = P.norm ? rsqrtf(tot / (float)D + RMS_EPS) : 1.0f;
+  // (the quantisation step needs no correctly rounded division: any step near
+  // max|x| / 32767 works, the codes are clamped and each is scaled back by the same inv)
+  const float scale = P.norm ? rsqrtf(tot * (1.0f / (float)D) + RMS_EPS) : 1.0f;
   const float xmax = __uint_as_float(mxb) * scale;
-  const float r = xmax > 0.f ? 32767.0f / xmax : 0.f;
-  const float inv = xmax > 0.f ? xmax / 32767.0f : 0.f;
+  const float r = xmax > 0.f ? __fdividef(32767.0f, xmax) : 0.f;
+  const float inv = xmax * (1.0f / 32767.0f);
   int16_t* xq16 = reinterpret_cast<int16_t*>(C.xq);
   // independent chunks: codes first, then their stores and sums, so the steps overlap
   int q[PER], sq[PER];
