@@ -545,24 +545,56 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* h, int d, i
 }
 
 // (alpha/r) B (A x) added to the LoRA base output of each token (fp32 x).
-__global__ void __launch_bounds__(256) lora_ab_kernel(const uint16_t* h, const float* xscale, int d, int out,
+// LORA_TOK tokens per CTA, so that each CTA reads A and B^T once for several tokens;
+// operands in 16-byte vectors (8 bf16).
+constexpr int LORA_TOK = 4;
+__global__ void __launch_bounds__(256) lora_ab_kernel(const uint16_t* h, const float* xscale, int T, int d, int out,
                                                       const uint16_t* a, const uint16_t* bt, int r, float lscale,
                                                       float* yl) {
-  __shared__ float v[e0eng::RANKS_MAX];
-  const int t = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint16_t* ht = h + (size_t)t * d;
-  const float sc = xscale[t];
-  for (int q = warp; q < r; q += blockDim.x >> 5) {
-    float s = 0.f;
-    for (int i = lane; i < d; i += 32) s += bf16_bits_to_f32(a[(size_t)q * d + i]) * bf16_bits_to_f32(ht[i]);
-    s = warp_sum(s);
-    if (lane == 0) v[q] = s * sc;
+  __shared__ float v[LORA_TOK][e0eng::RANKS_MAX];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int t0 = blockIdx.x * LORA_TOK, nt = min(LORA_TOK, T - t0);
+  // v[t][q] = xscale_t * (A_q . h_t)
+  for (int q = warp; q < r; q += nw) {
+    float s[LORA_TOK];
+#pragma unroll
+    for (int u = 0; u < LORA_TOK; ++u) s[u] = 0.f;
+    const uint4* aq = reinterpret_cast<const uint4*>(a + (size_t)q * d);
+    for (int c = lane; c < d / 8; c += 32) {
+      const uint4 av = __ldg(aq + c);
+      const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+      for (int u = 0; u < LORA_TOK; ++u)
+        if (u < nt) {
+          const uint4 hv = __ldg(reinterpret_cast<const uint4*>(h + (size_t)(t0 + u) * d) + c);
+          const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            s[u] = fmaf(__uint_as_float(aw[m] << 16), __uint_as_float(hw[m] << 16), s[u]);
+            s[u] = fmaf(__uint_as_float(aw[m] & 0xFFFF0000u), __uint_as_float(hw[m] & 0xFFFF0000u), s[u]);
+          }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < LORA_TOK; ++u) {
+      const float w = warp_sum(s[u]);
+      if (lane == 0 && u < nt) v[u][q] = w * xscale[t0 + u];
+    }
   }
   __syncthreads();
+  // yl[t][i] += (alpha / r) * sum_q B^T[q][i] v[t][q]
   for (int i = threadIdx.x; i < out; i += blockDim.x) {
-    float s = 0.f;
-    for (int q = 0; q < r; ++q) s += bf16_bits_to_f32(bt[(size_t)q * out + i]) * v[q];
-    yl[(size_t)t * out + i] += lscale * s;
+    float y[LORA_TOK];
+#pragma unroll
+    for (int u = 0; u < LORA_TOK; ++u) y[u] = 0.f;
+    for (int q = 0; q < r; ++q) {
+      const float b = bf16_bits_to_f32(bt[(size_t)q * out + i]);
+#pragma unroll
+      for (int u = 0; u < LORA_TOK; ++u) y[u] = fmaf(b, v[u][q], y[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < LORA_TOK; ++u)
+      if (u < nt) yl[(size_t)(t0 + u) * out + i] += lscale * y[u];
   }
 }
 
@@ -668,6 +700,8 @@ extern "C" e0_status e0_moe_prefill_layer(const e0_dims* dims, const e0_experts*
     E0_REQUIRE(lora->r >= 0 && lora->r <= e0eng::RANKS_MAX, E0_ERR_SHAPE, "e0_moe_prefill_layer: LoRA rank must be in [0, 64]");
   }
   E0_REQUIRE(al16p(h_in) && al16p(h_out), E0_ERR_INVALID, "e0_moe_prefill_layer: h_in/h_out must be 16-byte aligned");
+  E0_REQUIRE(!has_lora || !lora->a || al16p(lora->a), E0_ERR_INVALID,
+             "e0_moe_prefill_layer: the LoRA A matrix must be 16-byte aligned");
   const PfLayout L = pf_layout(d, E, F, K, T, out, true, has_lora);
   E0_REQUIRE(workspace_bytes >= L.total, E0_ERR_NOMEM, "e0_moe_prefill_layer: workspace too small");
   std::call_once(g_sm_once, [] {
@@ -744,7 +778,8 @@ extern "C" e0_status e0_moe_prefill_layer(const e0_dims* dims, const e0_experts*
     g.out16 = nullptr; g.out32 = yl; g.ldo = out; g.rowscale = nullptr;
     E0_CHECK_CUDA((launch_gemm<E0_LAYOUT_ROWS, EPI_F32>(g, st)));
     if (lora->r > 0 && lora->a && lora->bt) {
-      lora_ab_kernel<<<T, 256, 0, st>>>(h_in, xscale, d, out, lora->a, lora->bt, lora->r, lora->alpha / lora->r, yl);
+      lora_ab_kernel<<<(T + LORA_TOK - 1) / LORA_TOK, 256, 0, st>>>(h_in, xscale, T, d, out, lora->a, lora->bt, lora->r,
+                                                                     lora->alpha / lora->r, yl);
       E0_CHECK_CUDA(cudaGetLastError());
     }
   }
