@@ -19,7 +19,7 @@ struct Ctl {
                               // (group-major, so that lanes reading consecutive chunks hit distinct banks)
   float xinv[DMAX / 32];      // per 32-element chunk: dequant step of xq (one step for all of x)
   float xsum[DMAX / 32];      // per 32-element chunk: sum of the dequantised chunk
-  float abuf[2][32];          // SwiGLU activations of the last two expert slabs
+  float abuf[2][64];          // gate/up row values of the last two expert slabs (rows 2j, 2j + 1 = gate, up of j)
   uint4 aqw[NCW][4];          // per warp: the activations quantised to int16 in the dot32 order
   float b2buf[HEAD_ROWS];     // head fc2 bias slice of the current LRES unit
   float ubuf[HEAD_ROWS];      // head fc1 pre-activation, then erf-GELU output
@@ -946,19 +946,49 @@ __device__ __forceinline__ float reduce_lpr(float v) {
 }
 
 // A group of int4 stages holding rows [g0, g0 + R) of a part cut into stages of `per`
-// rows (part_rows rows in total).  Items of IR rows go to warps round robin, up to NI
-// items per warp and pass, so that a full group (64 rows) takes a single pass with
-// every warp busy and several independent rows in flight per lane.  GU: rows 2j/2j+1
-// are gate/up of pair j -> abuf[j] = silu(g) * u.  Otherwise each row value is added
-// to out[row0 + row].
+// rows (part_rows rows in total).  When a row takes a whole warp (D >= 1024) the rows go
+// to warps round robin, up to NI1 rows per warp and pass (64 rows: 4 or 5 per warp);
+// otherwise items of IR rows go to warps round robin, up to NI items per warp and pass.
+// GU: each row value goes to abuf[row] (rows 2j / 2j + 1 are gate / up of activation j,
+// combined by the caller).  Otherwise each row value is added to out[row0 + row].
 template <int D, bool GU>
 __device__ __forceinline__ void q4_group(const Cons& cs, int g0, int R, int per, int part_rows,
                                          const Q4Frag<D>& f, float* abuf, float* out, int row0) {
   constexpr int LPR = Q4Frag<D>::LPR, RPW = Q4Frag<D>::RPW;
+  const int lane = cs.lane;
+  if constexpr (RPW == 1) {
+    constexpr int NI1 = 5;
+    for (int it = cs.cw; it < R; it += NI1 * NCW) {
+      float v[NI1];
+#pragma unroll
+      for (int u = 0; u < NI1; ++u) {
+        v[u] = 0.f;
+        if (it + u * NCW < R) {
+          const int rho = g0 + it + u * NCW;  // row within the part
+          const int si = rho / per - g0 / per;
+          const int nr = min(per, part_rows - (rho / per) * per);
+          v[u] = q4_partial<D>(cs.stage(si), nr, rho % per, lane, f);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < NI1; ++u) v[u] = reduce_lpr<LPR>(v[u]);
+      if (lane == 0) {
+#pragma unroll
+        for (int u = 0; u < NI1; ++u) {
+          if (it + u * NCW >= R) break;
+          const int row = g0 + it + u * NCW;
+          if (GU)
+            abuf[row] = v[u];
+          else
+            red_add_f32(out + row0 + row, v[u]);
+        }
+      }
+    }
+    return;
+  }
   constexpr int IR = RPW > 2 ? RPW : 2;
   constexpr int NP = IR / RPW;
   constexpr int NI = 3;
-  const int lane = cs.lane;
   const int items = R / IR;
   for (int it = cs.cw; it < items; it += NI * NCW) {
     float v[NI][NP];
@@ -983,16 +1013,14 @@ __device__ __forceinline__ void q4_group(const Cons& cs, int g0, int R, int per,
     for (int u = 0; u < NI; ++u) {
       if (it + u * NCW >= items) break;
       const int rbase = g0 + (it + u * NCW) * IR;
-      if (GU) {
-        if (RPW == 1) {
-          if (lane == 0) abuf[rbase / 2] = silu_f(v[u][0]) * v[u][NP - 1];
-        } else {
-          const float up = __shfl_down_sync(0xffffffffu, v[u][0], LPR);
-          if (lane % (2 * LPR) == 0) abuf[(rbase + lane / LPR) / 2] = silu_f(v[u][0]) * up;
-        }
-      } else if (lane % LPR == 0) {
+      if (lane % LPR == 0) {
 #pragma unroll
-        for (int p = 0; p < NP; ++p) red_add_f32(out + row0 + rbase + p * RPW + lane / LPR, v[u][p]);
+        for (int p = 0; p < NP; ++p) {
+          if (GU)
+            abuf[rbase + p * RPW + lane / LPR] = v[u][p];
+          else
+            red_add_f32(out + row0 + rbase + p * RPW + lane / LPR, v[u][p]);
+        }
       }
     }
   }
@@ -1124,18 +1152,19 @@ __device__ __forceinline__ void consume_unit(Cons& cs, const LayerDesc& Ld, cons
       // The named barrier below is executed unconditionally so that every warp
       // reaches it even if the route table were read inconsistently.
       const bool valid = shared ? Ld.has_shared != 0 : ((C.rt_valid[l] >> u.k) & 1u) != 0;
-      // Two activation buffers: a warp writes buffer (n & 1) of unit n only after the
+      // Two gate/up value buffers: a warp writes buffer (n & 1) of unit n only after the
       // barrier of unit n - 1, which every warp passes after reading buffer (n & 1) of
       // unit n - 2.
       float* ab = C.abuf[cs.nx & 1u];
       ++cs.nx;
       if (valid) consume_q4_part<D, true>(cs, 64, ab, nullptr, 0);
-      cbar();  // all 32 activations ready
+      cbar();  // all 64 gate/up values ready
       if (valid) {
-        // Every warp quantises the 32 activations itself (lane j holds a_j): one step
+        // Every warp forms and quantises the 32 activations itself (lane j holds
+        // a_j = silu(gate_j) * up_j): one step
         // m / 32767 for the slab, m = max |a_j| (the bit patterns of non-negative
         // floats order like their values, so an unsigned max reduction finds it).
-        const float a = ab[cs.lane];
+        const float a = silu_f(ab[2 * cs.lane]) * ab[2 * cs.lane + 1];
         const float m = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(a))));
         const float r = m > 0.f ? __fdividef(32767.0f, m) : 0.f;
         const float ainv = m * (1.0f / 32767.0f);
