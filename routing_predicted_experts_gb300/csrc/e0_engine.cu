@@ -194,33 +194,6 @@ __device__ __forceinline__ int dot32(const uint4 q, const uint32_t* xp) {
   return a0 + a1;
 }
 
-// Quantise 32 fp32 values (one chunk) to int16 with step m/32767 (m = max |v|) and
-// pack them in the dot32 order.  Returns the step; *sum receives the fp32 sum.
-__device__ __forceinline__ float quant_chunk32(const float* v, uint32_t* xp, float* sum) {
-  float m = 0.f, s = 0.f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    m = fmaxf(m, fabsf(v[i]));
-    s += v[i];
-  }
-  *sum = s;
-  const float r = m > 0.f ? __fdividef(32767.0f, m) : 0.f;
-#pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    int q[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      int t = __float2int_rn(v[8 * g + j] * r);
-      q[j] = t > 32767 ? 32767 : (t < -32767 ? -32767 : t);
-    }
-    xp[4 * g + 0] = (uint32_t)(q[0] & 0xFFFF) | ((uint32_t)q[2] << 16);
-    xp[4 * g + 1] = (uint32_t)(q[4] & 0xFFFF) | ((uint32_t)q[6] << 16);
-    xp[4 * g + 2] = (uint32_t)(q[1] & 0xFFFF) | ((uint32_t)q[3] << 16);
-    xp[4 * g + 3] = (uint32_t)(q[5] & 0xFFFF) | ((uint32_t)q[7] << 16);
-  }
-  return m * (1.0f / 32767.0f);
-}
-
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 __device__ __forceinline__ float gelu_f(float u) { return 0.5f * u * (1.0f + erff(u * 0.70710678118654752f)); }
 
@@ -542,23 +515,6 @@ __device__ __forceinline__ uint8_t* prod_begin(Prod& pr, uint32_t& slot) {
     }
   }
   return pr.ring + (size_t)slot * STAGE_BYTES;
-}
-
-// Issue one stage of int4 rows [row0, row0+nr) of a row-layout matrix (in columns).
-__device__ __forceinline__ void issue_q4_rows(Prod& pr, const uint32_t* q, const uint16_t* s, const uint16_t* b, int in, int row0,
-                              int nr) {
-  if (!pr.ok) return;
-  uint32_t slot;
-  uint8_t* st = prod_begin(pr, slot);
-  if (!st) return;
-  if (pr.lane == 0) {
-    const uint32_t qb = (uint32_t)nr * in / 2, sb = (uint32_t)nr * in / 32;
-    mbar_arrive_expect_tx(&pr.C.full[slot], qb + 2 * sb);
-    tma_bulk_g2s(st, q + (size_t)row0 * (in / 8), qb, &pr.C.full[slot]);
-    tma_bulk_g2s(st + qb, s + (size_t)row0 * (in / 64), sb, &pr.C.full[slot]);
-    tma_bulk_g2s(st + qb + sb, b + (size_t)row0 * (in / 64), sb, &pr.C.full[slot]);
-  }
-  ++pr.n;
 }
 
 // Per-lane bounded wait until stage m's slot is free (lanes of the copy warp wait on

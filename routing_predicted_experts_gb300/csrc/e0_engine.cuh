@@ -5,7 +5,7 @@
 // for one token).  Every CTA owns a list of work units per layer.  A producer warp
 // streams the weight bytes of those units, in consumption order, into a ring of
 // shared-memory stages with bulk asynchronous copies (cp.async.bulk, mbarrier
-// completion); sixteen consumer warps dequantise and reduce them against the
+// completion); fourteen consumer warps dequantise and reduce them against the
 // layer input held in shared memory.  Because weight addresses do not depend on
 // activations, the producer runs ahead across layer boundaries: the next layer's
 // weights stream in while the grid waits for the current layer to finish.
