@@ -9,12 +9,13 @@
 //   route      top-K of each token's logits, combine weights        (one warp per token)
 //   sort       counting sort of the T*K (token, k) pairs by expert   (one CTA)
 //   gather     x = RMSNorm(h) in fp16, once per token and once per pair, grouped by expert
-//   gemm_q4    grouped GEMM, int4 weights dequantised to fp16 in shared memory, tcgen05.mma
+//   gemm_q4    grouped GEMM, int4 weights dequantised to fp16 in tensor memory, tcgen05.mma
 //              with the fp32 accumulator in tensor memory:
 //                gate/up  [rows_e x d] x [d x 2F]  -> SwiGLU epilogue -> fp16 a [rows_e x F]
 //                down     [rows_e x F] x [F x d]   -> x w_(t,k)        -> fp32 y per pair
 //              the shared expert and the LoRA base run through the same kernel as one group
-//   lora_ab    (alpha/r) B (A x) per token on the CUDA cores (r = 16: too thin for a tile)
+//   lora_ab    (alpha/r) B (A x) on the CUDA cores, four tokens per CTA (r = 16: too thin
+//              for a tile)
 //   combine    h_out = bf16(h + sum_k y_(t,k) + y_shared + y_lora), sum over k in k order
 //
 // fp16 (not bf16) operands: the dequantised weight s*q + b and x are each rounded once
@@ -126,11 +127,11 @@ __device__ __forceinline__ void cp_async_bar_arrive(uint64_t* bar) {
 }
 
 // Grouped GEMM out[rows][n] = sum_k x[row][k] W_g[n][k] with the operands swapped for
-// the tensor core: the weight tile (128 rows, dequantised to fp16 in shared memory) is
-// the MMA's A and the group's token rows (up to 64, rounded up to 16) its B, so a
-// group of few tokens costs few MMA columns.  The accumulator [weight row][token]
-// lives in tensor memory, double-buffered so the epilogue of one tile overlaps the
-// next tile's MMAs.  Copy, dequantisation, MMA and epilogue run in their own warps,
+// the tensor core: the weight tile (128 rows, dequantised to fp16 in tensor memory) is
+// the MMA's A and the group's token rows (up to 64, rounded up to 16, in shared memory)
+// its B, so a group of few tokens costs few MMA columns.  The accumulator [weight row]
+// [token] lives in tensor memory, double-buffered so the epilogue of one tile overlaps
+// the next tile's MMAs.  Copy, dequantisation, MMA and epilogue run in their own warps,
 // handing stages over through mbarriers; every wait is bounded.
 template <int LAYOUT, int EPI>
 __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ GemmArgs g) {
