@@ -180,11 +180,13 @@ void waterfill(const PlanSpec& s, const std::vector<Granule>& gs, int c0, int c1
   }
 }
 
-// The work plan of one layer kind: expert slabs round robin, then the divisible work
-// water-filled.  With `defer` (stack layers with a head), the prerouter's work (HEAD,
-// LRES: needed only by the next token) goes to CTAs of its own, [n_crit, ncta), which
-// do not hold up the layer: defer[c] = 1 there, *n_crit_out = n_crit.  The router rows
-// of an own-gate layer go to CTAs [0, crit_limit).
+// The work plan of one layer kind: expert slabs round robin, then the divisible work.
+// With `defer` (stack layers with a head) and room beside the expert CTAs, the layer's
+// LoRA work goes one unit per CTA to the next CTAs and the prerouter's work (HEAD, LRES:
+// needed only by the next token) in contiguous runs to CTAs of its own, [n_crit, ncta),
+// which do not hold up the layer: defer[c] = 1 there, *n_crit_out = n_crit.  Otherwise
+// the divisible work is water-filled by cost.  The router rows of an own-gate layer go
+// to CTAs [0, crit_limit).
 e0_status build_plan(const PlanSpec& s, int ncta, Unit* units, uint8_t* counts, uint8_t* defer = nullptr,
                      int* n_crit_out = nullptr, int crit_limit = 0) {
   std::vector<std::vector<Unit>> lists(ncta);
