@@ -1,0 +1,81 @@
+"""The bench's byte accounting and cache simulation (CPU only): the algorithmic bytes per
+token against the sizes the pages print, and the LRU / Belady hit counts against brute
+force on small traces."""
+import itertools
+import json
+import os
+
+import numpy as np
+
+import bench
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "page_numbers.json")
+
+
+def test_expert_bytes_match_the_printed_sizes():
+    g = json.load(open(GOLDEN))
+    d, E, F, L = g["d"], g["E"], g["F"], g["layers"]
+    # one routed expert: the per-token bytes of a K=1, shared-free, LoRA-free, head-free
+    # stack of one layer minus the same with K=0
+    one = bench.algorithmic_bytes_per_token(d=d, E=E, F=F, K=1, r=0, L=1, heads=0, routers=0, shared=False)
+    zero = bench.algorithmic_bytes_per_token(d=d, E=E, F=F, K=0, r=0, L=1, heads=0, routers=0, shared=False)
+    expert = one - zero
+    assert abs(expert / 1e6 - g["expert_bytes_MB_printed"]) < 0.01
+    assert abs(E * expert / 1e6 - g["layer_expert_bytes_MB_printed"]) < 1.0
+    assert abs(L * E * expert / 2**30 - g["stack_expert_bytes_GiB_printed"]) < 0.1
+    assert abs(4 * expert / 1e6 - g["k4_layer_expert_bytes_MB_printed"]) < 0.1
+
+
+def test_bytes_per_token_decomposes():
+    """K=8 adds 4 experts per layer to K=4, and each of the 33 heads gathers 2 x 4 more
+    one-hot columns of fc1 (bf16, H rows each); each gate adds its own bytes."""
+    b4 = bench.algorithmic_bytes_per_token(K=4)
+    b8 = bench.algorithmic_bytes_per_token(K=8)
+    one = bench.algorithmic_bytes_per_token(K=1, r=0, L=1, heads=0, routers=0, shared=False)
+    zero = bench.algorithmic_bytes_per_token(K=0, r=0, L=1, heads=0, routers=0, shared=False)
+    assert b8 - b4 == 40 * 4 * (one - zero) + 33 * (2 * 4) * 2 * 1024
+    gate = bench.algorithmic_bytes_per_token(routers=9) - b4
+    assert gate == 2 * 256 * 2048  # one bf16 [E][d] gate
+    assert (b4, b8) == (652839424, 936495616)
+
+
+def _brute_hits(trace, slots, policy):
+    """Hits of the pool's rule written out directly: on a miss with a full pool, evict
+    among residents outside the current and previous sets the least recently used (LRU)
+    or the one whose next use is furthest (Belady)."""
+    resident, last, hits, prev = set(), {}, 0, set()
+    clock = 0
+    for t, ids in enumerate(trace):
+        pinned = set(ids) | prev
+        for e in ids:
+            clock += 1
+            if e in resident:
+                hits += 1
+            else:
+                if len(resident) >= slots:
+                    cand = sorted(r for r in resident if r not in pinned)
+                    if policy == "lru":
+                        victim = min(cand, key=lambda r: last[r])
+                    else:
+                        def nxt(r):
+                            return next((u for u in range(t + 1, len(trace)) if r in trace[u]), len(trace) + 1)
+                        victim = max(cand, key=nxt)
+                    resident.discard(victim)
+                resident.add(e)
+            last[e] = clock
+        prev = set(ids)
+    return hits
+
+
+def test_lru_and_belady_hit_counts():
+    rng = np.random.default_rng(3)
+    for _ in range(20):
+        E, K, T, slots = 10, 2, 30, 5
+        trace = [list(rng.choice(E, K, replace=False)) for _ in range(T)]
+        lru, bel = bench.lru_belady_hits(trace, slots)
+        assert lru == _brute_hits(trace, slots, "lru")
+        assert bel >= lru  # the furthest-next-use eviction never does worse than LRU here
+    # a cyclic trace over slots + 1 experts: LRU misses every time after warm-up
+    trace = [[e] for e in itertools.islice(itertools.cycle(range(4)), 40)]
+    lru, bel = bench.lru_belady_hits(trace, 3)
+    assert lru == 0 and bel > 0
