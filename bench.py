@@ -290,55 +290,23 @@ SLOTS_METRIC = ("decode tok/s with a bounded HBM expert-slot pool (40-layer int4
                 "35 slots per prerouted layer, experts in pinned host memory)")
 
 
-def lru_belady_hits(trace_l, slots):
-    """Hit counts of LRU and of Belady (evict the expert used furthest in the future) on one
-    layer's trace, both with the pool's pinning rule (the previous and the staged set are
-    never evicted)."""
-    def run(policy):
-        resident, stamp, clock, hits = [], {}, 0, 0
-        prev = []
-        T = len(trace_l)
-        for t in range(T):
-            ids = [int(e) for e in trace_l[t]]
-            pinned = set(ids) | set(prev)
-            for e in ids:
-                if e in resident:
-                    hits += 1
-                else:
-                    if len(resident) >= slots:
-                        cand = [r for r in resident if r not in pinned]
-                        if policy == "lru":
-                            victim = min(cand, key=lambda r: stamp[r])
-                        else:
-                            def next_use(r):
-                                for u in range(t + 1, T):
-                                    if r in trace_l[u]:
-                                        return u
-                                return T + 1
-                            victim = max(cand, key=next_use)
-                        resident.remove(victim)
-                    resident.append(e)
-                clock += 1
-                stamp[e] = clock
-            prev = ids
-        return hits
-    return run("lru"), run("belady")
-
-
 def run_slots(args, local_rank: int = 0):
-    """Config 5: the 40-layer stack with the experts of the prerouted layers in pinned host
-    memory and 35 HBM slots per layer; the routing follows a synthetic locality trace
-    (injected through the logit bias), whose next token is staged while this token runs."""
+    """Config 5: the 40-layer stack with the experts of the head-routed layers in pinned
+    host memory and 35 HBM slots per layer.  The routing follows a synthetic locality
+    trace, injected through the logit bias; the ids each launch commits (on the device)
+    drive the staging of the next token's experts, whose copies run while that next
+    launch is already queued and waiting, layer by layer, on the pool's ready words."""
     import math
     import numpy as np
     import torch
-    from routing_predicted_experts_gb300 import binding as B, model as M, synth as S
+    from routing_predicted_experts_gb300 import binding as B, cachesim as CS, model as M, synth as S
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     sh, L = S.LAYER35B(args.k), S.STACK_LAYERS
     owners, prerouted = stack_schedule(L)
     pooled = sorted(prerouted)
-    slots = math.ceil(0.134 * sh.E)
+    cap = 0.134
+    slots = CS.capacity(cap, sh.E)
     dm = B.dims(sh.d, sh.E, sh.F, sh.K)
     total, offs = B.expert_bundle_layout(dm)
     t_build = time.time()
@@ -363,7 +331,9 @@ def run_slots(args, local_rank: int = 0):
                                  ly["lora"], ly["head"], ly["router"]) for l, ly in enumerate(layers)]
     stack = B.Stack(dm, structs, [1 if l in prerouted else 0 for l in range(L)], keepalive=(layers, pool))
     build_s = time.time() - t_build
-    n_steps = args.warmup + args.steps
+    W, K_ = args.warmup, args.steps
+    n_nowait = min(32, K_)
+    n_steps = W + K_ + n_nowait
     trace = np.stack([S.locality_trace(SEED, l, n_steps + 1, sh.E, sh.K) for l in range(L)], axis=1)
     bias = torch.zeros((n_steps, 2, L, sh.E), dtype=torch.float32)
     for t in range(n_steps):
@@ -377,64 +347,65 @@ def run_slots(args, local_rank: int = 0):
     B.e0_synth_normal(incr, SEED, S.stream_id("bench.incr"), 0, 1.0)
     hout = torch.empty((n_steps, sh.d), dtype=torch.int16, device=dev)
     ids = torch.empty((n_steps, L, sh.K), dtype=torch.int32, device=dev)
+    nxt = torch.empty((n_steps, L, sh.K), dtype=torch.int32, device=dev)
     ws = stack.workspace(dev)
     comp = torch.cuda.current_stream()
     copy = torch.cuda.Stream()
-    done = [None] * n_steps
-    pool_idx = np.arange(len(pooled), dtype=np.int32)
-
-    def stage(t):
-        if t >= 2:
-            copy.wait_event(done[t - 2])  # slots of token t-2 may be reused only after it ran
-        pool.stage_layers(pool_idx, trace[t, pooled], copy_stream=copy)
-        ev = torch.cuda.Event()
-        ev.record(copy)
-        return ev
-
+    pool_idx = list(range(len(pooled)))
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_steps)]
     sampler = ClockSampler(local_rank)
-    ready = stage(0)
+    # the first token's experts: no head committed them (the prefill would leave them staged)
+    pool.stage_host(pool_idx, trace[0, pooled], 0, copy_stream=copy)
+    ev = torch.cuda.Event()
+    ev.record(copy)
+    comp.wait_event(ev)
     stats0 = None
-    for t in range(n_steps):
-        if t == args.warmup:
+    for t in range(W + K_):
+        if t == W:
             torch.cuda.synchronize()
             stats0 = (pool.stats.hits, pool.stats.misses, pool.stats.h2d_bytes)
             sampler.start()
-        comp.wait_event(ready)
         starts[t].record(comp)
-        stack.step(t, h0[t], incr[t], hout[t], ws, ids_out=ids[t], logit_bias=bias[t])
+        stack.step(t, h0[t], incr[t], hout[t], ws, ids_out=ids[t], logit_bias=bias[t], next_ids=nxt[t])
         ends[t].record(comp)
-        done[t] = ends[t]
-        if t + 1 < n_steps:
-            ready = stage(t + 1)
+        if t > 0:
+            # launch t is queued: stage its experts from what launch t-1 committed
+            pool.stage(pool_idx, nxt[t - 1], pooled, t, copy_stream=copy, after=ends[t - 1])
     torch.cuda.synchronize()
     sampler.stop()
-    status = B.e0_get_device_status(ws)
-    if status != 0:
-        raise RuntimeError("device status %d" % status)
-    W, K_ = args.warmup, args.steps
-    wall_ms = starts[W].elapsed_time(ends[n_steps - 1])
-    kern_ms = sum(starts[t].elapsed_time(ends[t]) for t in range(W, n_steps))
     hits = pool.stats.hits - stats0[0]
     misses = pool.stats.misses - stats0[1]
     h2d = pool.stats.h2d_bytes - stats0[2]
+    # the same pooled stack with each token's copies finished before its launch: the
+    # kernel time without waits on the ready words
+    for t in range(W + K_, n_steps):
+        pool.stage(pool_idx, nxt[t - 1], pooled, t, copy_stream=copy, after=ends[t - 1])
+        ev = torch.cuda.Event()
+        ev.record(copy)
+        comp.wait_event(ev)
+        starts[t].record(comp)
+        stack.step(t, h0[t], incr[t], hout[t], ws, ids_out=ids[t], logit_bias=bias[t], next_ids=nxt[t])
+        ends[t].record(comp)
+    torch.cuda.synchronize()
+    status = B.e0_get_device_status(ws)
+    if status != 0:
+        raise RuntimeError("device status %d" % status)
+    wall_ms = starts[W].elapsed_time(ends[W + K_ - 1])
+    kern_ms = sum(starts[t].elapsed_time(ends[t]) for t in range(W, W + K_))
+    nowait_ms = sum(starts[t].elapsed_time(ends[t]) for t in range(W + K_, n_steps)) / n_nowait
     # the routing really followed the trace
     got = ids.cpu().numpy()
     follow = float(np.mean([sorted(got[t, l]) == sorted(trace[t, l]) for t in range(n_steps) for l in range(L)]))
-    # trace statistics, LRU vs Belady hit rates (pooled layers, timed steps)
-    tr = trace[W:n_steps]
+    # trace statistics and the cache-policy study (pooled layers, timed steps)
+    tr = trace[W:W + K_]
     overlap = float(np.mean([len(set(tr[t, l]) & set(tr[t - 1, l])) / sh.K for t in range(1, len(tr)) for l in pooled]))
     cnt = np.zeros(sh.E)
     for l in pooled:
         cnt += np.bincount(tr[:, l].ravel(), minlength=sh.E)
     srt = np.sort(cnt)[::-1]
     coverage = float(srt[:int(round(0.525 * sh.E))].sum() / srt.sum())
-    lru = bel = 0
-    for l in pooled[:8]:  # Belady on 8 layers keeps the host simulation short
-        a, b = lru_belady_hits(tr[:, l], slots)
-        lru, bel = lru + a, bel + b
-    n8 = 8 * len(tr) * sh.K
+    study = CS.study([tr[:, l] for l in pooled[:8]], sh.E, cap)  # 8 layers keep the host replay short
     # host -> device bandwidth of this machine (pinned, one 1 GiB copy)
     probe = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
     dst = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
@@ -465,16 +436,20 @@ def run_slots(args, local_rank: int = 0):
         "vs_baseline": None,
         "dtype": "int4 weights x int16-quantised activations -> fp32 accumulate; bf16 in/out",
         "data": "synthetic (seeded weights; locality routing trace injected through the logit bias)",
-        "config": {"workload": f"40-layer stack, K={args.k}, experts of the {len(pooled)} prerouted layers in pinned "
-                               f"host memory, {slots} HBM slots per layer (LRU); next token staged on a side stream",
+        "config": {"workload": f"40-layer stack, K={args.k}, experts of the {len(pooled)} head-routed layers in "
+                               f"pinned host memory, {slots} HBM slots per layer (LRU); each launch's committed "
+                               "ids stage the next token while that token's launch waits per layer",
                    "l2": "inputs larger than L2", "parallelism": "1 GPU", "build_s": round(build_s, 1)},
-        "slots": {"hit_rate_lru": round(hits / max(1, hits + misses), 4),
-                  "hit_rate_lru_sim_8_layers": round(lru / n8, 4), "hit_rate_belady_sim_8_layers": round(bel / n8, 4),
+        "slots": {"hit_rate": round(hits / max(1, hits + misses), 4),
                   "h2d_bytes_per_step": int(per_step_h2d), "h2d_gbs_measured": round(h2d_gbs, 1),
-                  "stall_us_per_step": round((wall_ms - kern_ms) / K_ * 1e3, 1),
+                  "wall_us_per_step": round(ms * 1e3, 1),
                   "kernel_us_per_step": round(kern_ms / K_ * 1e3, 1),
+                  "kernel_us_per_step_copies_done_first": round(nowait_ms * 1e3, 1),
+                  "stall_us_per_step": round(ms * 1e3 - nowait_ms * 1e3, 1),
                   "bound_tok_s": round(1e3 / bound_ms, 1), "realised_overlap": round(overlap, 4),
-                  "coverage_top_52.5pct": round(coverage, 4), "trace_followed": round(follow, 4)},
+                  "coverage_top_52.5pct": round(coverage, 4), "trace_followed": round(follow, 4),
+                  "policy_study_8_layers": {k: (round(v["hit_rate"], 4) if isinstance(v, dict) else v)
+                                            for k, v in study.items()}},
         "e2e": None,
         "gpu_launches": K_,
         "clocks": sampler.summary(0, 0),
@@ -628,48 +603,50 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
 
 # ------------------------------------------------------------------ oracle timing
-def _oracle_sample_layers(K: int):
-    """Two sampled layers of the stack for oracle timing: one with a head (33 of 40
-    layers run one), one without."""
-    from oracle import model_inputs as OM
+def oracle_token_sampler(K: int):
+    """The oracle, as it stands, on whole decode tokens of the 40-layer stack: every
+    layer-step, the 33 heads and the 8 own-gate GEMVs of a token after the first.  One
+    untimed token draws and dequantises the weights it touches; the timed tokens then
+    keep that token's routing (adopted at every layer) so that they touch the same
+    experts and no input generation falls inside the timed region.  Returns (token(),
+    prep seconds)."""
+    import numpy as np
+    from oracle import layer as OL, model_inputs as OM
     from routing_predicted_experts_gb300 import synth as S
-    sh = S.LAYER35B(K)
-    lay_h = OM.layer(SEED, 7, sh, with_head=True)
-    lay_n = OM.layer(SEED, 39, sh, with_head=False)
-    return sh, lay_h, lay_n
+    t0 = time.time()
+    sh, L = S.LAYER35B(K), S.STACK_LAYERS
+    owners, pre = set(S.HEAD_OWNERS), set(S.PREROUTED)
+    layers = [OM.layer(SEED, l, sh, with_head=(l in owners)) for l in range(L)]
+    routers = [OM.router_weights(SEED, l, sh) for l in range(L)]
+    src = ["head" if l in pre else "gate" for l in range(L)]
+    h0 = OM.hidden(SEED, 0, sh.d)
+    incr = np.stack([OM.increment(SEED, 0, l, sh.d) for l in range(L)])
+    warm = OL.stack_token(h0, incr, layers, routers, src, K)
+    fixed = {l: rec["ids"] for l, rec in enumerate(warm["layers"])}
+
+    def token():
+        return OL.stack_token(h0, incr, layers, routers, src, K, zhat_prev=warm["zhat_next"], ids_prev=fixed,
+                              adopt=lambda l, z, ids: fixed[l])
+    return token, time.time() - t0
 
 
 def oracle_worker(K: int, budget_s: float, steps: int | None = None) -> dict:
-    """Time the oracle (as it stands) on the host: layer-steps of a sampled head layer and
-    a sampled head-less layer; a token is 33 of the former + 7 of the latter + 8 gates."""
-    import numpy as np
-    from oracle import layer as OL, model_inputs as OM, routing as OR
-    t_prep = time.time()
-    sh, lay_h, lay_n = _oracle_sample_layers(K)
-    R = OM.router_weights(SEED, 0, sh)
-    h = OM.hidden(SEED, 0, sh.d)
-    z = OM.supplied_logits(SEED, "cur", sh.E)
-    ids, _ = OR.softmax_topk(z, K)
-    for e in ids:  # draw and dequantise the sampled experts before timing
-        lay_h["expert"](int(e)); lay_n["expert"](int(e))
-    prep_s = time.time() - t_prep
-    th, tn, tr = [], [], []
+    """Time whole oracle tokens (single thread) until the budget or the step count."""
+    token, prep_s = oracle_token_sampler(K)
+    times = []
     t0 = time.time()
-    n = 0
     while True:
-        a = time.perf_counter(); OL.layer_step(h, lay_h, ids, z, ids, K); b = time.perf_counter()
-        OL.layer_step(h, lay_n, ids, z, None, K); c = time.perf_counter()
-        OL.router_logits(OL.rmsnorm(np.zeros(sh.d) + 1.0), R); d_ = time.perf_counter()
-        th.append(b - a); tn.append(c - b); tr.append(d_ - c)
-        n += 1
+        a = time.perf_counter()
+        token()
+        times.append(time.perf_counter() - a)
         if steps is not None:
-            if n >= steps:
+            if len(times) >= steps:
                 break
         elif time.time() - t0 >= budget_s:
             break
-    per_token = 33 * statistics.median(th) + 7 * statistics.median(tn) + 8 * statistics.median(tr)
-    return {"tok_s": 1.0 / per_token, "per_token_s": per_token, "reps": n, "prep_s": round(prep_s, 1),
-            "layer_head_s": statistics.median(th), "layer_nohead_s": statistics.median(tn)}
+    per_token = statistics.median(times)
+    return {"tok_s": 1.0 / per_token, "per_token_s": per_token, "reps": len(times), "prep_s": round(prep_s, 1),
+            "times": times}
 
 
 def cpu_baseline(K: int, budget_s: float = 10.0) -> dict:
@@ -693,33 +670,23 @@ def cpu_baseline(K: int, budget_s: float = 10.0) -> dict:
     except OSError:
         pass
     return {"value": round(j["tok_s"], 4), "unit": "tok/s", "cores": 1, "kind": "oracle",
-            "sample": f"fp64 numpy oracle, 1 thread: {j['reps']} repetitions of one head layer-step (layer 7) "
-                      f"+ one head-less layer-step (layer 39) + one gate GEMV of the 40-layer K={K} workload; "
-                      f"token time = 33 x head layer + 7 x head-less layer + 8 x gate "
-                      f"({j['per_token_s']:.3f} s/token); weights drawn and dequantised before timing "
-                      f"({j['prep_s']} s); host cpu: {cpu or 'unknown'}, nproc {os.cpu_count()}"}
+            "sample": f"fp64 numpy oracle, 1 thread: {j['reps']} whole decode tokens of the 40-layer K={K} stack "
+                      f"(40 layer-steps, 33 heads, 8 own-gate GEMVs each; median {j['per_token_s']:.3f} s/token); "
+                      f"weights drawn and dequantised by one untimed token first ({j['prep_s']} s); "
+                      f"host cpu: {cpu or 'unknown'}, nproc {os.cpu_count()}"}
 
 
 def run_reference(args) -> dict:
-    """Reference arm: the CPU oracle as it stands, on the host cores, same metric/config."""
-    env_cores = 1
-    j = None
-    per_step = []
-    import numpy as np  # noqa: F401
-    from oracle import layer as OL, model_inputs as OM, routing as OR
-    sh, lay_h, lay_n = _oracle_sample_layers(args.k)
-    h = OM.hidden(SEED, 0, sh.d)
-    z = OM.supplied_logits(SEED, "cur", sh.E)
-    ids, _ = OR.softmax_topk(z, args.k)
+    """Reference arm: the CPU oracle as it stands, on the host cores, same metric/config:
+    each step is one whole decode token of the stack (oracle_token_sampler)."""
+    token, prep_s = oracle_token_sampler(args.k)
     for _ in range(args.warmup):
-        OL.layer_step(h, lay_h, ids, z, ids, args.k)
+        token()
+    per_step = []
     for _ in range(args.steps):
         a = time.perf_counter()
-        OL.layer_step(h, lay_h, ids, z, ids, args.k)
-        b = time.perf_counter()
-        OL.layer_step(h, lay_n, ids, z, None, args.k)
-        c = time.perf_counter()
-        per_step.append(33 * (b - a) + 7 * (c - b))
+        token()
+        per_step.append(time.perf_counter() - a)
     tok_s = args.steps / sum(per_step)
     line = {
         "impl": "reference",
@@ -729,12 +696,12 @@ def run_reference(args) -> dict:
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"40-layer int4 MoE decode stack, 35B-A3B-class layers, K={args.k} "
                                "(CPU oracle, host cores)"},
-        "cpu_baseline": {"value": round(tok_s, 4), "unit": "tok/s", "cores": env_cores, "kind": "oracle",
-                         "sample": "each step: one head layer-step (layer 7) and one head-less layer-step "
-                                   "(layer 39) of the oracle; token time = 33 x + 7 x those"},
+        "cpu_baseline": {"value": round(tok_s, 4), "unit": "tok/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step one whole decode token of the oracle (40 layer-steps, 33 heads, "
+                                   f"8 own-gate GEMVs), single thread; weights drawn by one untimed token first "
+                                   f"({prep_s:.1f} s)"},
         "e2e": {"value": round(tok_s, 4), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
-    del j
     return line
 
 

@@ -112,6 +112,10 @@ typedef struct {
   int32_t n;
   const int16_t* slot_of;
   int64_t stride;
+  const uint32_t* ready;  /* nullable; decode stack only: a word (a slot pool's, see
+                             e0_slot_pool_view) that equals the token index once this
+                             token's experts and slot_of table are in place; the stack
+                             step waits for it (bounded) before reading either */
 } e0_experts;
 
 /* Unmerged recovery LoRA linear (§3.3): y = W x + (alpha/r) * B (A x).
@@ -144,11 +148,32 @@ typedef struct {
   const uint16_t* lres;
 } e0_prerouter;
 
+/* Routing families (Appendix A "Routing Math"). */
+enum {
+  E0_ROUTE_SOFTMAX_TOPK = 0,  /* ids = top-K of the logits; w = softmax over all E, picked,
+                                 renormalised (equal to the softmax of the picked logits) */
+  E0_ROUTE_SIGMOID_GROUP = 1  /* sigma = sigmoid(logits); a group's score is the sum of its
+                                 two largest sigma; the top topk_group of n_group groups
+                                 (contiguous blocks of E / n_group experts) survive; ids =
+                                 top-K of sigma within them; w = route_scale * sigma[ids] /
+                                 (sum sigma[ids] + 1e-20).  The page selects on "the biased
+                                 score" without printing the bias: an optional per-expert
+                                 score_bias is added to sigma for the group scores and the
+                                 top-K only. */
+};
+
 typedef struct {
   int32_t d;    /* hidden width: 256, 512, 1024 or 2048 */
   int32_t E;    /* routed experts, multiple of 8, <= 1024 */
   int32_t F;    /* expert width, multiple of 64 */
   int32_t K;    /* experts per token, 1..16 */
+  int32_t route;        /* routing family, E0_ROUTE_*; 0 (softmax-top-K) when zero-filled */
+  int32_t n_group;      /* sigmoid-group: groups (2 <= E / n_group, n_group <= 32) */
+  int32_t topk_group;   /* sigmoid-group: groups kept (topk_group * E / n_group >= K) */
+  float route_scale;    /* sigmoid-group: s */
+  const float* score_bias;  /* sigmoid-group: nullable device fp32 [E], the selection bias of
+                               the routing being chosen (single-layer calls; the decode
+                               stack takes it per layer from e0_layer.score_bias) */
 } e0_dims;
 
 /* Workspace for every engine call below; layers = 1 for single-layer calls. */
@@ -256,10 +281,17 @@ e0_status e0_moe_decode_layer_noalloc(const e0_dims* dims, const e0_experts* rou
                                       float* next_weights, e0_stream stream);
 
 /* --------------------------------------------------------------------------------
- * Decode stack: L layer-steps for one token in ONE launch (§3.2 "Two consumption
- * profiles": routing for layer l at token t is the prediction made by head l-1 at
- * token t-1, on layers whose previous layer owns a head; other layers, and every
- * layer at the first token, route with their own gate R·x).
+ * Decode stack: L layer-steps for one token in ONE launch.  Where a layer's routing
+ * comes from (route_src[l]):
+ *    1  the prediction head l-1 made at the previous token ("The Other Half of the
+ *       Memory Wall" §3.2 "Two consumption profiles", "Prediction-as-routing"); at the
+ *       first token such a layer routes with its own gate;
+ *    0  its own gate R_l x_l;
+ *   -N  route-ahead by N layers (the route-ahead notes of BigMoeOnEdge, "The idea"):
+ *       its own gate applied to the input of layer l - N at the same token, with the
+ *       combine weights taken from those logits (the prediction's own, as for a head);
+ *       needs l >= N.
+ * Every layer's gate logits get logit_bias[0][l] (e0_stack_step).
  * The stack object is library-owned (layer descriptors and the CTA work plan in
  * device memory); the weights it points to stay caller-owned and must outlive it.
  * ------------------------------------------------------------------------------ */
@@ -269,42 +301,69 @@ typedef struct {
   e0_qlora lora;                /* w.q == NULL -> none */
   e0_prerouter head;            /* lres == NULL -> no head on this layer */
   const uint16_t* router;       /* bf16 [E][d]; required on layers that may self-route */
+  const float* score_bias;      /* sigmoid-group routing: this layer's selection bias fp32
+                                   [E] (device), nullable */
 } e0_layer;
 
 typedef struct e0_stack e0_stack;
 
-/* layers: HOST array of L descriptors (copied). prerouted_from: HOST int8 [L],
- * 1 where layer l takes its routing from head l-1 after the first token. */
+/* layers: HOST array of L descriptors (copied).  route_src: HOST int8 [L] as above
+ * (NULL: every layer routes with its own gate). */
 e0_status e0_stack_create(e0_stack** out, const e0_dims* dims, const e0_layer* layers,
-                          int32_t L, const int8_t* prerouted_from);
+                          int32_t L, const int8_t* route_src);
 void e0_stack_destroy(e0_stack* stack);
 size_t e0_stack_workspace_size(const e0_stack* stack);
 
+/* Optional per-token outputs of e0_stack_step; every pointer is nullable device memory.
+ *   ids       int32 [L][K]: the routing each layer used at this token;
+ *   weights   fp32 [L][K]: its combine weights;
+ *   h_trace   bf16 [L][d]: each layer's input hidden state;
+ *   delta     fp32 [L][d]: each layer's delta (expert, shared and LoRA sum) before the
+ *             bf16 rounding of h_out;
+ *   logits    fp32 [2][L][E]: [0][l] the gate logits layer l routed by at this token
+ *             (own-gate and route-ahead layers), [1][l] the logits committed for layer
+ *             l at the next token (layers routed by the previous layer's head); both
+ *             include logit_bias; rows that do not apply are left untouched;
+ *   next_ids  int32 [L][K]: the routing committed for the next token (-1 on layers not
+ *             routed by a head), the device ids e0_stage_slots consumes. */
+typedef struct {
+  int32_t* ids;
+  float* weights;
+  uint16_t* h_trace;
+  float* delta;
+  float* logits;
+  int32_t* next_ids;
+} e0_stack_outputs;
+
 /* One decode token through all L layers.
- *   step: token index (0 = first token: every layer routes with its own gate).
+ *   step: token index (0 = first token: every layer routed by a head routes with its
+ *   own gate instead).  Pooled layers (e0_experts.ready set) wait for their ready word
+ *   to equal `step` (as uint32).
  *   h0: bf16 [d]; incr: bf16 [L][d] per-layer residual increments standing in for
  *   attention (h_l = bf16(h_out_{l-1} + incr_l), h_out_{-1} = h0);
- *   h_out: bf16 [d] output of the last layer.
- *   ids_out int32 [L][K], weights_out fp32 [L][K], h_trace bf16 [L][d]: nullable
- *   diagnostics (routing used per layer; each layer's input hidden state).
- *   logit_bias fp32 [2][L][E], nullable: [0][l] is added to layer l's own-gate logits
- *   at this token, [1][l] to the head logits that commit layer l's routing for the
- *   next token, before the top-K (a synthetic routing trace is injected this way: a
- *   large bias on the trace's ids makes the routing pick them). */
+ *   h_out: bf16 [d] output of the last layer.  outs: nullable (see e0_stack_outputs).
+ *   logit_bias fp32 [2][L][E], nullable: [0][l] is added to layer l's gate logits at
+ *   this token, [1][l] to the head logits that commit layer l's routing for the next
+ *   token, before the top-K (a synthetic routing trace is injected this way: a large
+ *   bias on the trace's ids makes the routing pick them). */
 e0_status e0_stack_step(e0_stack* stack, int32_t step, const uint16_t* h0,
-                        const uint16_t* incr, uint16_t* h_out, int32_t* ids_out,
-                        float* weights_out, uint16_t* h_trace, const float* logit_bias,
-                        void* workspace, size_t workspace_bytes, e0_stream stream);
+                        const uint16_t* incr, uint16_t* h_out, const e0_stack_outputs* outs,
+                        const float* logit_bias, void* workspace, size_t workspace_bytes,
+                        e0_stream stream);
 
 /* --------------------------------------------------------------------------------
- * Bounded HBM expert-slot pool (§3.1, §3.2: experts stay off the GPU and a bounded set
- * of slots holds the ones the routing needs; the prerouter's one-token lead is the
- * time to stage them).  Experts live in pinned host memory as one bundle per
- * (layer, expert): gate/up codes, scales, biases, down codes, scales, biases, at the
- * offsets e0_expert_bundle_bytes reports (layouts as in e0_experts).  Each layer owns
- * `slots` bundle slots in HBM, replaced least-recently-used; the experts of the
- * previous staging of a layer (the running token's) and the ones being staged are
- * never evicted, so 2K <= slots.
+ * Bounded HBM expert-slot pool (§3.1 "Executor paths", the staged path; §3.2
+ * "Motivation": experts stay off the GPU and a bounded set of slots holds the ones the
+ * routing needs; the prerouter's one-token lead is the time to stage them).  Experts
+ * live in pinned host memory as one bundle per (layer, expert): gate/up codes, scales,
+ * biases, down codes, scales, biases, at the offsets e0_expert_bundle_bytes reports
+ * (layouts as in e0_experts).  Each layer owns `slots` bundle slots in HBM, replaced
+ * least-recently-used; the experts of the previous staging of a layer and the ones
+ * being staged are never evicted, so 2K <= slots.  Each layer also has a ready word
+ * (e0_experts.ready of its view): a staging call writes its `tag` there after the
+ * layer's bundle copies and id -> slot table, all on the copy stream, so a decode-stack
+ * launch for token t (tag t) can start before the copies end and waits, layer by layer,
+ * only where it needs them.
  * ------------------------------------------------------------------------------ */
 typedef struct e0_slot_pool e0_slot_pool;
 typedef struct {
@@ -318,24 +377,38 @@ typedef struct {
  * offsets of the six tensors inside a bundle. */
 size_t e0_expert_bundle_bytes(const e0_dims* dims, size_t* offsets6);
 /* host_bundles: pinned host memory [layers][E][bundle_bytes], caller-owned, outliving
- * the pool.  The pool (slots and id -> slot tables) is library-owned. */
+ * the pool.  The pool (slots, id -> slot tables, ready words) is library-owned. */
 e0_status e0_slot_pool_create(e0_slot_pool** out, const e0_dims* dims, int32_t layers,
                               int32_t slots, const void* host_bundles, size_t bundle_bytes);
 void e0_slot_pool_destroy(e0_slot_pool* pool);
 /* The device view of a layer's slots, to pass as e0_layer.routed (n = slots, slot_of
- * the layer's id -> slot table, stride = bundle bytes). */
+ * the layer's id -> slot table, stride = bundle bytes, ready = its ready word). */
 e0_status e0_slot_pool_view(const e0_slot_pool* pool, int32_t layer, e0_experts* out);
-/* Make next_ids (HOST int32 [K]) resident in the layer's slots: copies of missing
- * bundles and the updated id -> slot table are queued on copy_stream, then `ready`
- * (nullable) is recorded there; launches that use these experts wait on it.  stats
- * (nullable) is accumulated into. */
-e0_status e0_stage_slots(e0_slot_pool* pool, int32_t layer, const int32_t* next_ids, int32_t K,
-                         e0_stream copy_stream, e0_event ready, e0_stage_stats* stats);
-/* The same for several layers in one call: layers HOST int32 [n_layers] (pool layer
- * indices), next_ids HOST int32 [n_layers][K]; `ready` is recorded once, after all. */
-e0_status e0_stage_slots_layers(e0_slot_pool* pool, const int32_t* layers, int32_t n_layers,
-                                const int32_t* next_ids, int32_t K, e0_stream copy_stream,
-                                e0_event ready, e0_stage_stats* stats);
+
+/* Stage the routing a decode-stack launch committed: next_ids is DEVICE int32 [*][K]
+ * (e0_stack_outputs.next_ids), rows HOST int32 [n_layers] gives the row of next_ids
+ * for each pool layer in layers (HOST int32 [n_layers]).  On copy_stream: wait for
+ * `after` (the launch that wrote next_ids; nullable only if the ids are already
+ * complete), copy the ids to the host, and block this thread until they arrive; then
+ * for each layer, in order: one copy per missing bundle, the id -> slot table, and
+ * `tag` into the layer's ready word.  Because the copies wait for `after`, no slot that
+ * launch (or an earlier one) reads is overwritten while it runs.  stats (nullable) is
+ * accumulated into.  On an error nothing of the failing layer is marked resident that
+ * was not copied, its ready word keeps its old value, and later calls stay valid. */
+e0_status e0_stage_slots(e0_slot_pool* pool, const int32_t* layers, int32_t n_layers,
+                         const int32_t* next_ids, const int32_t* rows, int32_t K, uint32_t tag,
+                         e0_stream copy_stream, e0_event after, e0_stage_stats* stats);
+/* The same with HOST ids [n_layers][K]: priming a pool before the first token (whose
+ * routing no head committed) or a routing the host already knows. */
+e0_status e0_stage_slots_host(e0_slot_pool* pool, const int32_t* layers, int32_t n_layers,
+                              const int32_t* ids, int32_t K, uint32_t tag, e0_stream copy_stream,
+                              e0_event after, e0_stage_stats* stats);
+/* The pool's own record of a layer's id -> slot table (HOST int16 [E], -1 = absent), as
+ * it will be on the device once the queued copies have run. */
+e0_status e0_slot_pool_resident(const e0_slot_pool* pool, int32_t layer, int16_t* slot_of_out);
+/* Tests: make the staging calls fail (as a failed cudaMemcpyAsync would, E0_ERR_CUDA)
+ * when they are about to queue their (n+1)-th bundle copy from now; n < 0 disarms. */
+e0_status e0_debug_fail_copies(e0_slot_pool* pool, int32_t n);
 
 /* --------------------------------------------------------------------------------
  * Input generation (not part of the method): the seeded counter-based generator

@@ -21,6 +21,12 @@ f64 = C.c_double
 sz = C.c_size_t
 
 E0_OK = 0
+E0_ERR_INVALID = -1
+E0_ERR_SHAPE = -2
+E0_ERR_CUDA = -3
+E0_ERR_UNSUPPORTED = -6
+E0_ROUTE_SOFTMAX_TOPK = 0
+E0_ROUTE_SIGMOID_GROUP = 1
 E0_LAYOUT_ROWS = 0
 E0_LAYOUT_COLSLAB = 1
 E0_DEV_TIMEOUT = 1
@@ -36,7 +42,7 @@ class e0_q4(C.Structure):
 
 
 class e0_experts(C.Structure):
-    _fields_ = [("gate_up", e0_q4), ("down", e0_q4), ("n", i32), ("slot_of", vp), ("stride", i64)]
+    _fields_ = [("gate_up", e0_q4), ("down", e0_q4), ("n", i32), ("slot_of", vp), ("stride", i64), ("ready", vp)]
 
 
 class e0_qlora(C.Structure):
@@ -49,7 +55,8 @@ class e0_prerouter(C.Structure):
 
 
 class e0_dims(C.Structure):
-    _fields_ = [("d", i32), ("E", i32), ("F", i32), ("K", i32)]
+    _fields_ = [("d", i32), ("E", i32), ("F", i32), ("K", i32), ("route", i32), ("n_group", i32),
+                ("topk_group", i32), ("route_scale", f32), ("score_bias", vp)]
 
 
 class e0_stage_stats(C.Structure):
@@ -58,7 +65,11 @@ class e0_stage_stats(C.Structure):
 
 class e0_layer(C.Structure):
     _fields_ = [("routed", e0_experts), ("shared", e0_experts), ("lora", e0_qlora), ("head", e0_prerouter),
-                ("router", vp)]
+                ("router", vp), ("score_bias", vp)]
+
+
+class e0_stack_outputs(C.Structure):
+    _fields_ = [("ids", vp), ("weights", vp), ("h_trace", vp), ("delta", vp), ("logits", vp), ("next_ids", vp)]
 
 
 P = C.POINTER
@@ -83,12 +94,14 @@ PROTOTYPES = {
     "e0_slot_pool_create": (i32, [P(vp), P(e0_dims), i32, i32, vp, sz]),
     "e0_slot_pool_destroy": (None, [vp]),
     "e0_slot_pool_view": (i32, [vp, i32, P(e0_experts)]),
-    "e0_stage_slots": (i32, [vp, i32, vp, i32, vp, vp, P(e0_stage_stats)]),
-    "e0_stage_slots_layers": (i32, [vp, vp, i32, vp, i32, vp, vp, P(e0_stage_stats)]),
+    "e0_stage_slots": (i32, [vp, vp, i32, vp, vp, i32, u32, vp, vp, P(e0_stage_stats)]),
+    "e0_stage_slots_host": (i32, [vp, vp, i32, vp, i32, u32, vp, vp, P(e0_stage_stats)]),
+    "e0_slot_pool_resident": (i32, [vp, i32, vp]),
+    "e0_debug_fail_copies": (i32, [vp, i32]),
     "e0_stack_create": (i32, [P(vp), P(e0_dims), P(e0_layer), i32, vp]),
     "e0_stack_destroy": (None, [vp]),
     "e0_stack_workspace_size": (sz, [vp]),
-    "e0_stack_step": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+    "e0_stack_step": (i32, [vp, i32, vp, vp, vp, P(e0_stack_outputs), vp, vp, sz, vp]),
     "e0_synth_normal": (i32, [vp, i64, u64, u32, i64, f64, i32, vp]),
     "e0_debug_inject_stall": (i32, [vp, u64, vp]),
     "e0_debug_trace": (i32, [vp, sz]),

@@ -27,6 +27,13 @@ def _p(t: Optional[torch.Tensor]) -> Optional[int]:
     return t.data_ptr()
 
 
+def _event(ev) -> Optional[int]:
+    """cudaEvent_t of a torch.cuda.Event (None -> NULL); the event must have been recorded."""
+    if ev is None:
+        return None
+    return int(ev.cuda_event)
+
+
 def _stream(stream=None) -> int:
     s = stream if stream is not None else torch.cuda.current_stream()
     return s.cuda_stream
@@ -84,8 +91,21 @@ class Prerouter:
                               _p(self.b2), _p(self.lres))
 
 
-def dims(d: int, E: int, F: int, K: int) -> L.e0_dims:
-    return L.e0_dims(d, E, F, K)
+def dims(d: int, E: int, F: int, K: int, family: Optional[dict] = None,
+         score_bias: Optional[torch.Tensor] = None) -> L.e0_dims:
+    """Layer dimensions and routing family: None = softmax-top-K, or a dict
+    {"kind": "sigmoid_group", "n_group", "topk_group", "scale"}; score_bias (device fp32
+    [E], sigmoid-group only) is the selection bias of the routing a single-layer call
+    chooses."""
+    dm = L.e0_dims(d, E, F, K)
+    if family is not None:
+        assert family["kind"] == "sigmoid_group"
+        dm.route = L.E0_ROUTE_SIGMOID_GROUP
+        dm.n_group = int(family["n_group"])
+        dm.topk_group = int(family["topk_group"])
+        dm.route_scale = float(family["scale"])
+        dm.score_bias = _p(score_bias)
+    return dm
 
 
 # ------------------------------------------------------------------ calls
@@ -209,13 +229,15 @@ def e0_qlinear_lora(lora: QLora, x: torch.Tensor, ws: torch.Tensor, y: Optional[
 class Stack:
     """Owns an e0_stack (layer descriptors + work plan on the device)."""
 
-    def __init__(self, dm: L.e0_dims, layers: list, prerouted: list[int], keepalive=None):
+    def __init__(self, dm: L.e0_dims, layers: list, route_src: list[int], keepalive=None):
+        """route_src[l]: 1 routed by head l-1 (after the first token), 0 own gate, -N
+        route-ahead by N layers."""
         self.dm = dm
         self.L = len(layers)
         arr = (L.e0_layer * self.L)()
         for i, ly in enumerate(layers):
             arr[i] = ly
-        pre = (C.c_int8 * self.L)(*prerouted)
+        pre = (C.c_int8 * self.L)(*route_src)
         h = C.c_void_p()
         check(lib().e0_stack_create(C.byref(h), C.byref(dm), arr, self.L, C.cast(pre, C.c_void_p)))
         self.handle = h
@@ -226,9 +248,16 @@ class Stack:
         return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
     def step(self, step: int, h0: torch.Tensor, incr: torch.Tensor, h_out: torch.Tensor, ws: torch.Tensor,
-             ids_out=None, w_out=None, h_trace=None, stream=None, logit_bias=None) -> None:
-        check(lib().e0_stack_step(self.handle, step, _p(h0), _p(incr), _p(h_out), _p(ids_out), _p(w_out),
-                                  _p(h_trace), _p(logit_bias), _p(ws), ws.numel(), _stream(stream)))
+             ids_out=None, w_out=None, h_trace=None, stream=None, logit_bias=None, delta=None, logits=None,
+             next_ids=None) -> None:
+        """One token; the optional outputs are e0_stack_outputs' (ids, weights, h_trace,
+        delta, logits [2][L][E], next_ids)."""
+        outs = None
+        if any(t is not None for t in (ids_out, w_out, h_trace, delta, logits, next_ids)):
+            outs = L.e0_stack_outputs(_p(ids_out), _p(w_out), _p(h_trace), _p(delta), _p(logits), _p(next_ids))
+        check(lib().e0_stack_step(self.handle, step, _p(h0), _p(incr), _p(h_out),
+                                  C.byref(outs) if outs is not None else None, _p(logit_bias), _p(ws), ws.numel(),
+                                  _stream(stream)))
 
     def close(self):
         if self.handle:
@@ -243,8 +272,9 @@ class Stack:
 
 
 def e0_layer_struct(routed: Experts, shared: Optional[Experts], lora: Optional[QLora], head: Optional[Prerouter],
-                    router: torch.Tensor) -> L.e0_layer:
+                    router: torch.Tensor, score_bias: Optional[torch.Tensor] = None) -> L.e0_layer:
     ly = L.e0_layer()
+    ly.score_bias = _p(score_bias)
     ly.routed = routed.c()
     if shared is not None:
         ly.shared = shared.c()
@@ -296,6 +326,7 @@ class SlotPool:
                                         total))
         self.handle = h
         self.bundles = bundles
+        self.E = dm.E
         self.stats = L.e0_stage_stats()
 
     def view(self, layer: int) -> _RawExperts:
@@ -303,19 +334,38 @@ class SlotPool:
         check(lib().e0_slot_pool_view(self.handle, layer, C.byref(ex)))
         return _RawExperts(ex)
 
-    def stage(self, layer: int, ids, copy_stream=None) -> None:
-        arr = (C.c_int32 * len(ids))(*[int(i) for i in ids])
-        check(lib().e0_stage_slots(self.handle, layer, C.cast(arr, C.c_void_p), len(ids), _stream(copy_stream), None,
-                                   C.byref(self.stats)))
-
-    def stage_layers(self, layers, ids, copy_stream=None) -> None:
-        """Stage ids [len(layers)][K] (host array) into the given pool layers in one call."""
+    def stage_host(self, layers, ids, tag: int, copy_stream=None, after=None) -> None:
+        """Stage HOST ids [len(layers)][K] into the given pool layers, then write `tag`
+        into their ready words (priming, or a routing the host knows)."""
         import numpy as np
         lay = np.ascontiguousarray(np.asarray(layers, dtype=np.int32))
         arr = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
-        check(lib().e0_stage_slots_layers(self.handle, C.c_void_p(lay.ctypes.data), len(lay),
-                                          C.c_void_p(arr.ctypes.data), arr.shape[-1], _stream(copy_stream), None,
-                                          C.byref(self.stats)))
+        check(lib().e0_stage_slots_host(self.handle, C.c_void_p(lay.ctypes.data), len(lay),
+                                        C.c_void_p(arr.ctypes.data), arr.shape[-1], tag & 0xFFFFFFFF,
+                                        _stream(copy_stream), _event(after), C.byref(self.stats)))
+
+    def stage(self, layers, next_ids: torch.Tensor, rows, tag: int, copy_stream=None, after=None) -> None:
+        """Stage the DEVICE ids a stack launch committed (next_ids int32 [*][K]; row rows[i]
+        for pool layer layers[i]) after event `after`, then write `tag` into the ready
+        words.  Blocks the calling thread until the ids have reached the host."""
+        import numpy as np
+        lay = np.ascontiguousarray(np.asarray(layers, dtype=np.int32))
+        rw = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
+        assert next_ids.dtype == torch.int32 and next_ids.is_cuda
+        check(lib().e0_stage_slots(self.handle, C.c_void_p(lay.ctypes.data), len(lay), _p(next_ids),
+                                   C.c_void_p(rw.ctypes.data), next_ids.shape[-1], tag & 0xFFFFFFFF,
+                                   _stream(copy_stream), _event(after), C.byref(self.stats)))
+
+    def resident(self, layer: int):
+        """The pool's own id -> slot table of a layer (int16 [E], -1 = absent)."""
+        import numpy as np
+        out = np.empty(self.E, dtype=np.int16)
+        check(lib().e0_slot_pool_resident(self.handle, layer, C.c_void_p(out.ctypes.data)))
+        return out
+
+    def fail_copies(self, n: int) -> None:
+        """Tests: make the (n+1)-th bundle copy from now fail as a failed copy call would."""
+        check(lib().e0_debug_fail_copies(self.handle, n))
 
     def close(self):
         if self.handle:

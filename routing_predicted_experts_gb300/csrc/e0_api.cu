@@ -54,15 +54,35 @@ e0_status device_ctas(int d, int* ncta) {
   return E0_OK;
 }
 
-e0_status check_dims(const e0_dims* dm) {
+}  // namespace
+
+// Shared with the other translation units (declared in e0_common.cuh).
+e0_status e0::check_dims(const e0_dims* dm) {
   E0_REQUIRE(dm, E0_ERR_INVALID, "dims is NULL");
   E0_REQUIRE(dm->d == 256 || dm->d == 512 || dm->d == 1024 || dm->d == 2048, E0_ERR_SHAPE,
              "d must be 256, 512, 1024 or 2048");
   E0_REQUIRE(dm->E >= 8 && dm->E <= EMAX && dm->E % 8 == 0, E0_ERR_SHAPE, "E must be a multiple of 8 in [8, 1024]");
   E0_REQUIRE(dm->F >= 64 && dm->F % 64 == 0 && dm->F <= 8192, E0_ERR_SHAPE, "F must be a multiple of 64");
   E0_REQUIRE(dm->K >= 1 && dm->K <= KMAX && dm->K <= dm->E, E0_ERR_SHAPE, "K must be in [1, min(16, E)]");
+  return e0::check_route(dm);
+}
+
+e0_status e0::check_route(const e0_dims* dm) {
+  if (dm->route == E0_ROUTE_SIGMOID_GROUP) {
+    E0_REQUIRE(dm->n_group >= 1 && dm->n_group <= 32 && dm->E % dm->n_group == 0 && dm->E / dm->n_group >= 2,
+               E0_ERR_SHAPE, "sigmoid-group routing: n_group must divide E into groups of >= 2, n_group <= 32");
+    E0_REQUIRE(dm->topk_group >= 1 && dm->topk_group <= dm->n_group &&
+                   dm->topk_group * (dm->E / dm->n_group) >= dm->K,
+               E0_ERR_SHAPE, "sigmoid-group routing: topk_group in [1, n_group] with topk_group * E/n_group >= K");
+    E0_REQUIRE(std::isfinite(dm->route_scale), E0_ERR_INVALID, "sigmoid-group routing: route_scale must be finite");
+  } else {
+    E0_REQUIRE(dm->route == E0_ROUTE_SOFTMAX_TOPK, E0_ERR_UNSUPPORTED, "unknown routing family");
+  }
   return E0_OK;
 }
+
+namespace {
+using e0::check_dims;
 
 // ------------------------------------------------------------------ planner
 struct PlanSpec {
@@ -346,6 +366,7 @@ e0_status fill_experts(const e0_experts* ex, const e0_dims* dm, bool routed, Lay
     L->gu_q = ex->gate_up.q; L->gu_s = ex->gate_up.scale; L->gu_b = ex->gate_up.bias;
     L->dn_q = ex->down.q; L->dn_s = ex->down.scale; L->dn_b = ex->down.bias;
     L->slot_of = ex->slot_of;
+    L->ready = ex->ready;
     L->n_routed = ex->n;
     E0_REQUIRE(ex->stride >= 0 && ex->stride % 16 == 0, E0_ERR_INVALID, "expert stride must be a multiple of 16");
     L->ex_stride = ex->stride;
@@ -402,6 +423,15 @@ void base_params(EngineParams& P, int d, int E, int F, int K, int L, int ncta, i
   P.timeout_ns = DEFAULT_TIMEOUT_NS;
   P.wl = ws_layout(E, L);
   P.trace = g_trace;
+}
+
+// The routing family of the call (dims are checked already).
+void set_route(EngineParams& P, const e0_dims* dm) {
+  P.route = dm->route;
+  P.n_group = dm->n_group;
+  P.topk_group = dm->topk_group;
+  P.route_scale = dm->route_scale;
+  P.score_bias = dm->score_bias;
 }
 
 void set_inline_plan(EngineParams& P, const CachedPlan& cp) {
@@ -500,6 +530,7 @@ extern "C" e0_status e0_moe_decode_layer(const e0_dims* dims, const e0_experts* 
 
   static thread_local EngineParams P;
   base_params(P, dims->d, dims->E, dims->F, dims->K, 1, ncta, MODE_LAYER);
+  set_route(P, dims);
   LayerDesc& L = P.inline_layer;
   PlanSpec ps;
   ps.d = dims->d; ps.E = dims->E; ps.F = dims->F; ps.K = dims->K;
@@ -632,7 +663,8 @@ struct e0_stack {
   e0_dims dims;
   int L;
   int ncta;
-  std::vector<int8_t> prerouted;
+  std::vector<int8_t> prerouted;   // 1: routed by head l-1 after the first token
+  uint64_t ahead_mask = 0;         // route-ahead layers
   LayerDesc* d_layers = nullptr;
   Unit* d_plan = nullptr;
   uint8_t* d_counts = nullptr;
@@ -641,8 +673,8 @@ struct e0_stack {
 };
 
 extern "C" e0_status e0_stack_create(e0_stack** out, const e0_dims* dims, const e0_layer* layers, int32_t L,
-                                     const int8_t* prerouted_from) {
-  E0_REQUIRE(out && layers && L >= 1 && L <= LMAX, E0_ERR_INVALID, "e0_stack_create: need 1..64 layers");
+                                     const int8_t* route_src) {
+  E0_REQUIRE(out && layers && L >= 1 && L <= LMAX, E0_ERR_INVALID, "e0_stack_create: need 1..48 layers");
   *out = nullptr;
   e0_status st = check_dims(dims);
   if (st) return st;
@@ -681,10 +713,18 @@ extern "C" e0_status e0_stack_create(e0_stack** out, const e0_dims* dims, const 
     E0_REQUIRE(ly.router && al16(ly.router), E0_ERR_INVALID,
                "every stack layer needs its own gate (used at the first token)");
     D.router = ly.router;
-    D.prerouted = prerouted_from ? prerouted_from[l] : 0;
+    D.score_bias = ly.score_bias;
+    D.gate_for = -1;
+    const int src = route_src ? route_src[l] : 0;
+    E0_REQUIRE(src <= 1, E0_ERR_INVALID, "route_src must be 1 (head), 0 (own gate) or -N (route-ahead by N)");
+    D.prerouted = src == 1 ? 1 : 0;
     if (D.prerouted) {
       E0_REQUIRE(l > 0 && layers[l - 1].head.lres, E0_ERR_INVALID,
                  "a prerouted layer needs a head on the previous layer");
+    }
+    if (src < 0) {
+      E0_REQUIRE(l + src >= 0, E0_ERR_INVALID, "route-ahead by N needs N layers before the layer");
+      D.ahead = -src;
     }
     const int kind = D.has_head ? KIND_MAIN : KIND_MAIN_NOHEAD;
     if (have_spec[kind]) {
@@ -711,6 +751,13 @@ extern "C" e0_status e0_stack_create(e0_stack** out, const e0_dims* dims, const 
       if (st) return st;
       n_crit = std::min(n_crit, nc);
     }
+  // route-ahead: the gate rows of layer l run on layer l - N's input (one target per layer)
+  for (int l = 0; l < L; ++l)
+    if (descs[l].ahead > 0) {
+      LayerDesc& src = descs[l - descs[l].ahead];
+      E0_REQUIRE(src.gate_for < 0, E0_ERR_INVALID, "two route-ahead layers read the same earlier layer");
+      src.gate_for = l;
+    }
   // the router rows of own-gate layers stay off the deferred CTAs
   st = build_plan(rs, ncta, units.data() + (size_t)KIND_ROUTER * ncta * MAXU,
                   counts.data() + (size_t)KIND_ROUTER * ncta, nullptr, nullptr, n_crit);
@@ -721,7 +768,10 @@ extern "C" e0_status e0_stack_create(e0_stack** out, const e0_dims* dims, const 
   s->L = L;
   s->ncta = ncta;
   s->prerouted.assign(L, 0);
-  for (int l = 0; l < L; ++l) s->prerouted[l] = descs[l].prerouted ? 1 : 0;
+  for (int l = 0; l < L; ++l) {
+    s->prerouted[l] = descs[l].prerouted ? 1 : 0;
+    if (descs[l].ahead > 0) s->ahead_mask |= 1ull << l;
+  }
   for (int k = 0; k < KINDS_MAX; ++k) {
     int nd = 0;
     for (int c = 0; c < ncta; ++c) nd += defer[(size_t)k * ncta + c];
@@ -758,9 +808,8 @@ extern "C" size_t e0_stack_workspace_size(const e0_stack* s) {
 }
 
 extern "C" e0_status e0_stack_step(e0_stack* s, int32_t step, const uint16_t* h0, const uint16_t* incr,
-                                   uint16_t* h_out, int32_t* ids_out, float* weights_out, uint16_t* h_trace,
-                                   const float* logit_bias, void* workspace, size_t workspace_bytes,
-                                   e0_stream stream) {
+                                   uint16_t* h_out, const e0_stack_outputs* outs, const float* logit_bias,
+                                   void* workspace, size_t workspace_bytes, e0_stream stream) {
   E0_REQUIRE(s && h0 && h_out, E0_ERR_INVALID, "e0_stack_step: NULL required argument");
   E0_REQUIRE(step >= 0, E0_ERR_INVALID, "step must be >= 0");
   e0_status st = check_ws(&s->dims, s->L, workspace, workspace_bytes);
@@ -768,6 +817,8 @@ extern "C" e0_status e0_stack_step(e0_stack* s, int32_t step, const uint16_t* h0
   E0_REQUIRE(al16(h0) && al16(h_out) && (!incr || al16(incr)), E0_ERR_INVALID, "hidden buffers must be 16-byte aligned");
   static thread_local EngineParams P;
   base_params(P, s->dims.d, s->dims.E, s->dims.F, s->dims.K, s->L, s->ncta, MODE_STACK);
+  set_route(P, &s->dims);
+  P.score_bias = nullptr;  // per layer in the stack
   P.layers = s->d_layers;
   P.plan = s->d_plan;
   P.plan_n = s->d_counts;
@@ -778,16 +829,26 @@ extern "C" e0_status e0_stack_step(e0_stack* s, int32_t step, const uint16_t* h0
   }
   P.kinds = KINDS_MAX;
   P.step = step;
-  uint64_t mask = 0;
+  // routed from gate logits: own-gate layers (and head-routed ones at the first token),
+  // whose gate rows run on their own input, and route-ahead layers, whose gate rows run
+  // N layers earlier
+  uint64_t own = 0;
   for (int l = 0; l < s->L; ++l)
-    if (step == 0 || !s->prerouted[l]) mask |= 1ull << l;
-  P.router_mask = mask;
+    if (!((s->ahead_mask >> l) & 1ull) && (step == 0 || !s->prerouted[l])) own |= 1ull << l;
+  P.gate_mask = own;
+  P.router_mask = own | s->ahead_mask;
   P.h_in = h0;
   P.incr = incr;
   P.h_out = h_out;
-  P.ids_trace = ids_out;
-  P.w_trace = weights_out;
-  P.h_trace = h_trace;
+  if (outs) {
+    P.ids_trace = outs->ids;
+    P.w_trace = outs->weights;
+    P.h_trace = outs->h_trace;
+    P.delta_trace = outs->delta;
+    P.delta_out = outs->delta ? outs->delta + (size_t)(s->L - 1) * s->dims.d : nullptr;
+    P.z_trace = outs->logits;
+    P.next_ids_out = outs->next_ids;
+  }
   P.logit_bias = logit_bias;
   P.ws = reinterpret_cast<uint8_t*>(workspace);
   E0_CHECK_CUDA(launch_engine(P, (cudaStream_t)stream));

@@ -14,6 +14,9 @@ namespace e0 {
 void set_error(const std::string& msg);
 e0_status fail(e0_status code, const std::string& msg);
 e0_status cuda_fail(cudaError_t err, const char* what);
+// Dimension and routing-family checks shared by every entry point.
+e0_status check_dims(const e0_dims* dm);
+e0_status check_route(const e0_dims* dm);  // the routing family's parameters only
 }  // namespace e0
 
 #define E0_CHECK_CUDA(call)                                        \
@@ -117,6 +120,13 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// System-scope acquire: for words written by a host-to-device copy on another stream.
+__device__ __forceinline__ uint32_t ld_acquire_sys_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
@@ -225,6 +235,61 @@ __device__ __forceinline__ void warp_topk_regs(const float (&z)[NPL], int E, int
       val = topk_key_value(hi);
     }
   }
+}
+
+// Warp maximum of a 64-bit key (two integer reductions: high word, then low word).
+__device__ __forceinline__ uint64_t warp_max_key(uint64_t k) {
+  const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(k >> 32));
+  const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(k >> 32) == hi ? (uint32_t)k : 0u);
+  return ((uint64_t)hi << 32) | lo;
+}
+
+// Sigmoid-group routing of one token ("The Other Half of the Memory Wall", Appendix A
+// "Sigmoid-group") from its logits z[0..E) (shared or global memory); every lane of the
+// warp calls.  sigma = 1/(1+e^-z); score = sigma + sbias (selection only); a group (a
+// contiguous block of E/n_group experts) scores the sum of its two best scores; the
+// topk_group best groups survive (ties to the lower group); ids = top-K of the scores
+// within them (descending, ties to the lower id); w = scale * sigma / (sum of the picked
+// sigma + 1e-20).  Lane k < K receives id k (-1 if none) and its final weight.
+__device__ __forceinline__ void sigmoid_group_route(const float* z, const float* sbias, int E, int K, int n_group,
+                                                    int topk_group, float scale, int lane, int& id_out,
+                                                    float& w_out) {
+  const int gs = E / n_group;
+  auto score = [&](int e) { return 1.0f / (1.0f + expf(-z[e])) + (sbias ? sbias[e] : 0.f); };
+  float gscore = -INFINITY;  // lane g < n_group: group g's score
+  for (int g = 0; g < n_group; ++g) {
+    uint64_t k1 = 0ull, k2 = 0ull;
+    for (int e = g * gs + lane; e < (g + 1) * gs; e += 32) k1 = max(k1, topk_key(score(e), e));
+    k1 = warp_max_key(k1);
+    for (int e = g * gs + lane; e < (g + 1) * gs; e += 32) {
+      const uint64_t k = topk_key(score(e), e);
+      if (k < k1) k2 = max(k2, k);
+    }
+    k2 = warp_max_key(k2);
+    if (lane == g) gscore = topk_key_value((uint32_t)(k1 >> 32)) + topk_key_value((uint32_t)(k2 >> 32));
+  }
+  int rank = 0;
+  for (int o = 0; o < 32; ++o) {
+    const float og = __shfl_sync(0xffffffffu, gscore, o);
+    if (o < n_group && (og > gscore || (og == gscore && o < lane))) ++rank;
+  }
+  const uint32_t keep = __ballot_sync(0xffffffffu, lane < n_group && rank < topk_group);
+  int id = -1;
+  uint64_t prev = ~0ull;
+  for (int k = 0; k < K; ++k) {
+    uint64_t m = 0ull;
+    for (int e = lane; e < E; e += 32)
+      if ((keep >> (e / gs)) & 1u) {
+        const uint64_t key = topk_key(score(e), e);
+        if (key < prev && key > m) m = key;
+      }
+    prev = warp_max_key(m);
+    if (lane == k && prev != 0ull) id = (int)(0xFFFFFFFFu - (uint32_t)prev);
+  }
+  const float sig = (lane < K && id >= 0) ? 1.0f / (1.0f + expf(-z[id])) : 0.f;
+  const float tot = warp_sum(sig);
+  id_out = id;
+  w_out = scale * sig / (tot + 1e-20f);
 }
 
 }  // namespace e0dev

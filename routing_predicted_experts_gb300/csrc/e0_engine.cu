@@ -37,8 +37,6 @@ struct Ctl {
   float red[NCW];
   uint32_t redm[NCW];
   float xscale;               // RMSNorm factor of the current layer input
-  int32_t f_ids[KMAX];        // finisher top-K
-  float f_vals[KMAX];
   volatile int32_t abort_flag;
   int32_t is_last;
   uint32_t epoch;
@@ -197,30 +195,50 @@ __device__ __forceinline__ int dot32(const uint4 q, const uint32_t* xp) {
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 __device__ __forceinline__ float gelu_f(float u) { return 0.5f * u * (1.0f + erff(u * 0.70710678118654752f)); }
 
-// ------------------------------------------------------------------ top-K (one warp)
-// Top-K of z[0..E) (shared memory), descending, ties to the lower index.  Writes
-// ids/vals (lane 0).  All 32 lanes must call.
-__device__ __noinline__ void warp_topk(const float* z, int E, int K, int lane, int32_t* ids, float* vals) {
-  uint32_t taken = 0;
-  uint64_t best = 0;
-  for (int e = lane, m = 0; e < E; e += 32, ++m) best = max(best, topk_key(z[e], e));
-  for (int k = 0; k < K; ++k) {
-    uint64_t m = best;
+// ------------------------------------------------------------------ routing (one warp)
+// Sigmoid-group routing (sigmoid_group_route in e0_common.cuh) with the family's
+// parameters; kept out of line: it is off the hot path.
+__device__ __noinline__ void route_sigmoid_group(const EngineParams& P, const float* z, const float* sbias, int lane,
+                                                 int& id_out, float& w_out) {
+  sigmoid_group_route(z, sbias, P.E, P.K, P.n_group, P.topk_group, P.route_scale, lane, id_out, w_out);
+}
+
+// Softmax-top-K of logits held in registers (lane holds z[lane + 32 j], j < NPL):
+// lane k < K receives id k (-1 if none) and its weight, the softmax over the picked.
+template <int NPL>
+__device__ __forceinline__ void softmax_topk_regs(const float (&z)[NPL], int E, int K, int lane, int& id, float& w) {
+  float val;
+  warp_topk_regs<NPL>(z, E, K, lane, id, val);
+  const float v0 = __shfl_sync(0xffffffffu, val, 0);
+  const float ex = (lane < K && id >= 0) ? expf(val - v0) : 0.f;
+  const float tot = warp_sum(ex);
+  w = tot > 0.f ? ex / tot : 0.f;
+}
+template <int NPL>
+__device__ __forceinline__ void softmax_topk_smem_n(const EngineParams& P, const float* z, int lane, int& id,
+                                                    float& w) {
+  float zv[NPL];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-    const int e = (int)(0xFFFFFFFFu - (uint32_t)m);
-    if (lane == 0) {
-      ids[k] = e;
-      vals[k] = z[e];
-    }
-    if ((e & 31) == lane) {
-      taken |= 1u << (e >> 5);
-      best = 0;
-      for (int e2 = lane, mm = 0; e2 < E; e2 += 32, ++mm)
-        if (!((taken >> mm) & 1u)) best = max(best, topk_key(z[e2], e2));
-    }
+  for (int j = 0; j < NPL; ++j) {
+    const int e = lane + 32 * j;
+    zv[j] = e < P.E ? z[e] : 0.f;
   }
-  __syncwarp();
+  softmax_topk_regs<NPL>(zv, P.E, P.K, lane, id, w);
+}
+
+// The routing of one token from its logits in shared memory z[0..E) by the family in P;
+// every lane of the warp calls.  Lane k < K receives id k (-1 if none) in descending
+// score order and its FINAL combine weight.
+__device__ __noinline__ void route_smem(const EngineParams& P, const float* z, const float* sbias, int lane, int& id,
+                                        float& w) {
+  if (P.route == ROUTE_SIGMOID_GROUP)
+    route_sigmoid_group(P, z, sbias, lane, id, w);
+  else if (P.E <= 256)
+    softmax_topk_smem_n<8>(P, z, lane, id, w);
+  else if (P.E <= 512)
+    softmax_topk_smem_n<16>(P, z, lane, id, w);
+  else
+    softmax_topk_smem_n<32>(P, z, lane, id, w);
 }
 
 // ------------------------------------------------------------------ producer
@@ -236,28 +254,55 @@ struct Prod {
   uint32_t par, p3, epoch;
 };
 
+// Stack: the routing warp routes layer l from gate logits (its own gate, or route-ahead
+// gate rows computed on an earlier layer's input) rather than from a committed route.
 __device__ __forceinline__ bool self_routes(const EngineParams& P, int l) {
   return P.mode == MODE_STACK && ((P.router_mask >> l) & 1ull);
 }
+// Stack: layer l's own gate rows run on its own input.
+__device__ __forceinline__ bool gate_here(const EngineParams& P, int l) {
+  return P.mode == MODE_STACK && ((P.gate_mask >> l) & 1ull);
+}
+
+__device__ __forceinline__ bool prod_keep_waiting(Prod& pr, uint64_t t0, uint32_t it);
+
+// Slot pools (stack): wait (bounded) until the layer's ready word says that this
+// token's experts and id -> slot table are in place.  The word is written by a copy on
+// the pool's copy stream after the bundles and the table, so seeing it makes them
+// visible too.  False after a timeout or an abort.
+__device__ __forceinline__ bool wait_slots_ready(Prod& pr, const LayerDesc& Ld) {
+  if (pr.P.mode != MODE_STACK || !Ld.ready) return true;
+  const uint32_t want = (uint32_t)pr.P.step;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    bool r = false;
+    if (pr.lane == 0) r = ld_acquire_sys_u32(Ld.ready) == want;
+    if (__shfl_sync(0xffffffffu, r ? 1 : 0, 0)) return true;
+    if (!prod_keep_waiting(pr, t0, it)) return false;
+  }
+}
 
 // Publish the routing of layer l in the route table.  Lane k (< K) brings id k
-// (-1 = none) and its unnormalised combine weight; ids are checked (range,
-// duplicates, slot table) and the weights renormalised over the ids that survive.
+// (-1 = none) and its combine weight; ids are checked (range, duplicates, slot table).
+// Softmax-top-K weights arrive unnormalised and are renormalised over the ids that
+// survive; sigmoid-group weights arrive final (their scale is not a normalisation).
 __device__ __forceinline__ void publish_route(Prod& pr, int l, int id, float w) {
   const EngineParams& P = pr.P;
   Ctl& C = pr.C;
   const LayerDesc& Ld = layer_at(P, l);
   const int lane = pr.lane, K = P.K;
+  const bool ready = wait_slots_ready(pr, Ld);
+  if (!ready) pr.ok = false;
   if (lane < K) C.rt_ids[l][lane] = (int16_t)id;
   __syncwarp();
-  bool v = lane < K && id >= 0 && id < P.E;
+  bool v = ready && lane < K && id >= 0 && id < P.E;
   if (lane < K)
     for (int j = 0; j < lane; ++j)
       if (C.rt_ids[l][j] == id) v = false;
-  if (lane < K && id != -1 && !v) raise_error(P, C, E0_DEV_BAD_ID);
+  if (ready && lane < K && id != -1 && !v) raise_error(P, C, E0_DEV_BAD_ID);
   int idx = v ? id : 0;
   if (v && Ld.slot_of) {
-    idx = Ld.slot_of[id];
+    idx = __ldcg(Ld.slot_of + id);
     if (idx < 0) {
       v = false;
       raise_error(P, C, E0_DEV_NOT_RESIDENT);
@@ -274,7 +319,7 @@ __device__ __forceinline__ void publish_route(Prod& pr, int l, int id, float w) 
   for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
   if (lane < K) {
     C.rt_idx[l][lane] = (int16_t)idx;
-    C.rt_w[l][lane] = (v && tot > 0.f) ? wv / tot : 0.f;
+    C.rt_w[l][lane] = P.route == ROUTE_SIGMOID_GROUP ? wv : ((v && tot > 0.f) ? wv / tot : 0.f);
   }
   if (lane == 0) C.rt_valid[l] = valid;
   if (P.mode == MODE_STACK && Ld.has_head) {
@@ -298,22 +343,6 @@ __device__ __forceinline__ void publish_route(Prod& pr, int l, int id, float w) 
   __syncwarp();
 }
 
-// Top-K of C.zbuf[0..E) (descending, ties to the lower id); lane k < K gets id k and
-// exp(z_k - z_max), the unnormalised softmax weight.
-__device__ __forceinline__ void topk_lane(Prod& pr, int& id, float& w) {
-  const EngineParams& P = pr.P;
-  Ctl& C = pr.C;
-  warp_topk(C.zbuf, P.E, P.K, pr.lane, C.f_ids, C.f_vals);  // lane 0 writes
-  __syncwarp();
-  id = -1;
-  w = 0.f;
-  if (pr.lane < P.K) {
-    id = C.f_ids[pr.lane];
-    w = expf(C.f_vals[pr.lane] - C.f_vals[0]);
-  }
-  __syncwarp();
-}
-
 // Kernel start: routing known at launch time (given ids, or the routes the previous
 // launch committed for this token) and the previous-token ids the heads one-hot.
 __device__ __forceinline__ void load_routes(Prod& pr) {
@@ -327,10 +356,16 @@ __device__ __forceinline__ void load_routes(Prod& pr) {
     if (P.ids_prev_in && lane < K) pid = P.ids_prev_in[lane];
     const bool inr = id >= 0 && id < P.E;
     if (P.logits_in && inr) z = P.logits_in[id];
-    float mx = inr ? z : -INFINITY;
+    float w;
+    if (P.route == ROUTE_SIGMOID_GROUP) {
+      const float sig = (P.logits_in && inr) ? 1.0f / (1.0f + expf(-z)) : 0.f;
+      w = P.route_scale * sig / (warp_sum(sig) + 1e-20f);
+    } else {
+      float mx = inr ? z : -INFINITY;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    const float w = (P.logits_in && inr) ? expf(z - mx) : 0.f;
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      w = (P.logits_in && inr) ? expf(z - mx) : 0.f;
+    }
     if (lane < K) C.rt_prev[0][lane] = (int16_t)pid;
     __syncwarp();
     bool pv = lane < K && pid >= 0 && pid < P.E;
@@ -464,11 +499,32 @@ __device__ __forceinline__ void self_route_regs(Prod& pr, int l) {
       return;
     }
   }
+  if (P.z_trace && blockIdx.x == 0) {
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+      const int e = pr.lane + 32 * j;
+      if (e < P.E) P.z_trace[(size_t)l * P.E + e] = zv[j];
+    }
+  }
   int id;
-  float val;
-  warp_topk_regs<NPL>(zv, P.E, P.K, pr.lane, id, val);
-  const float v0 = __shfl_sync(0xffffffffu, val, 0);
-  publish_route(pr, l, pr.lane < P.K ? id : -1, pr.lane < P.K && id >= 0 ? expf(val - v0) : 0.f);
+  float w;
+  if (P.route == ROUTE_SIGMOID_GROUP) {
+    // (the routing warp owns zbuf in the stack)
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+      const int e = pr.lane + 32 * j;
+      if (e < P.E) pr.C.zbuf[e] = zv[j];
+    }
+    __syncwarp();
+    route_sigmoid_group(P, pr.C.zbuf, layer_at(P, l).score_bias, pr.lane, id, w);
+    __syncwarp();
+  } else {
+    float val;
+    warp_topk_regs<NPL>(zv, P.E, P.K, pr.lane, id, val);
+    const float v0 = __shfl_sync(0xffffffffu, val, 0);
+    w = pr.lane < P.K && id >= 0 ? expf(val - v0) : 0.f;  // unnormalised: publish_route normalises
+  }
+  publish_route(pr, l, pr.lane < P.K ? id : -1, pr.lane < P.K && id >= 0 ? w : 0.f);
 }
 
 // A layer that routes with its own gate: wait until every gate logit of this launch
@@ -700,10 +756,15 @@ __device__ void producer(const EngineParams& P, Ctl& C, uint8_t* ring) {
   Prod pr{P, C, ring, 0u, true, (int)(threadIdx.x & 31), C.epoch & 1u, C.epoch % 3u, C.epoch};
   for (int l = 0; l < P.L && pr.ok; ++l) {
     const LayerDesc& Ld = layer_at(P, l);
-    if (self_routes(P, l)) {
+    // gate rows on this layer's input: its own gate, then the gate of the layer that
+    // routes ahead from here
+    const uint16_t* gates[2] = {gate_here(P, l) ? Ld.router : nullptr,
+                                P.mode == MODE_STACK && Ld.gate_for >= 0 ? layer_at(P, Ld.gate_for).router : nullptr};
+    for (int g = 0; g < 2; ++g) {
+      if (!gates[g]) continue;
       int nu;
       const Unit* us = units_of(P, KIND_ROUTER, blockIdx.x, nu);
-      for (int i = 0; i < nu; ++i) issue_bf_rows(pr, Ld.router, P.d, us[i].r0, us[i].r1);
+      for (int i = 0; i < nu; ++i) issue_bf_rows(pr, gates[g], P.d, us[i].r0, us[i].r1);
     }
     int nu;
     const Unit* us = units_of(P, P.plan ? Ld.plan_kind : 0, blockIdx.x, nu);
@@ -773,21 +834,24 @@ __device__ void router_warp(const EngineParams& P, Ctl& C) {
         }
         const float* z = zhat_ptr(P, pnext3, l - 1);
 #pragma unroll 8
-        for (int e = pr.lane; e < P.E; e += 32)
-          C.zbuf[e] = __ldcg(z + e) + (P.logit_bias ? P.logit_bias[((size_t)P.L + l) * P.E + e] : 0.f);
+        for (int e = pr.lane; e < P.E; e += 32) {
+          const float v = __ldcg(z + e) + (P.logit_bias ? P.logit_bias[((size_t)P.L + l) * P.E + e] : 0.f);
+          C.zbuf[e] = v;
+          if (P.z_trace) P.z_trace[((size_t)P.L + l) * P.E + e] = v;
+        }
         __syncwarp();
         int id;
         float w;
-        topk_lane(pr, id, w);
-        float tot = w;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        route_smem(P, C.zbuf, layer_at(P, l).score_bias, pr.lane, id, w);
         if (pr.lane < P.K) {
           rg_ids_ptr(P, pr.par ^ 1u, l)[pr.lane] = id;
-          rg_w_ptr(P, pr.par ^ 1u, l)[pr.lane] = w / tot;
+          rg_w_ptr(P, pr.par ^ 1u, l)[pr.lane] = w;
+          if (P.next_ids_out) P.next_ids_out[l * P.K + pr.lane] = id;
         }
         __syncwarp();
         if (pr.lane == 0) *rg_tag_ptr(P, pr.par ^ 1u, l) = pr.epoch + 1u;
+      } else if (P.next_ids_out && pr.lane < P.K) {
+        P.next_ids_out[l * P.K + pr.lane] = -1;  // no head commits this layer's routing
       }
     }
   }
@@ -1385,6 +1449,8 @@ __device__ __forceinline__ void layer_input(Cons& cs, int l, uint32_t par, const
       }
       if (P.mode == MODE_STACK && P.h_trace && blockIdx.x == 0)
         P.h_trace[(size_t)l * D + i] = f32_to_bf16_bits(h[k]);
+      if (P.mode == MODE_STACK && P.delta_trace && blockIdx.x == 0 && l > 0)
+        P.delta_trace[(size_t)(l - 1) * D + i] = a[k];
     }
   }
   if (tid == 0) C.xscale = scale;
@@ -1430,13 +1496,19 @@ __device__ void consumer(const EngineParams& P, Ctl& C, uint8_t* ring) {
     float* acc = acc_ptr(P, par, l);
     float* zh = zhat_ptr(P, pnext3, l);
     float* zr = reinterpret_cast<float*>(zr_ptr(P, par, l));  // tagged u64 words
-    const bool self_route = P.mode == MODE_STACK && ((P.router_mask >> l) & 1ull);
-    if (self_route) {
+    if (gate_here(P, l)) {
       // gate rows first: the routing warps pick this layer's experts from them
       int nu;
       const Unit* us = units_of(P, KIND_ROUTER, cta, nu);
       for (int i = 0; i < nu; ++i) consume_unit<D>(cs, Ld, us[i], l, acc, zh, zr);
       if (tid == 0) stamp(P, l, 8 + U_ROUTER);  // gate rows of this CTA published
+    }
+    if (P.mode == MODE_STACK && Ld.gate_for >= 0) {
+      // route-ahead: the gate rows of layer gate_for on this layer's input
+      float* zra = reinterpret_cast<float*>(zr_ptr(P, par, Ld.gate_for));
+      int nu;
+      const Unit* us = units_of(P, KIND_ROUTER, cta, nu);
+      for (int i = 0; i < nu; ++i) consume_unit<D>(cs, Ld, us[i], l, acc, zh, zra);
     }
     int nu;
     const Unit* us = units_of(P, P.plan ? Ld.plan_kind : 0, cta, nu);
@@ -1524,15 +1596,12 @@ __device__ void consumer(const EngineParams& P, Ctl& C, uint8_t* ring) {
   }
   cbar();
   if (want_next && cs.cw == 0) {
-    warp_topk(C.zbuf, P.E, P.K, cs.lane, C.f_ids, C.f_vals);
-    if (cs.lane == 0) {
-      const float mx = C.f_vals[0];
-      float s = 0.f;
-      for (int k = 0; k < P.K; ++k) s += expf(C.f_vals[k] - mx);
-      for (int k = 0; k < P.K; ++k) {
-        if (P.next_ids) P.next_ids[k] = C.f_ids[k];
-        if (P.next_w) P.next_w[k] = expf(C.f_vals[k] - mx) / s;
-      }
+    int id;
+    float w;
+    route_smem(P, C.zbuf, P.score_bias, cs.lane, id, w);
+    if (cs.lane < P.K) {
+      if (P.next_ids) P.next_ids[cs.lane] = id;
+      if (P.next_w) P.next_w[cs.lane] = w;
     }
   }
   cbar();

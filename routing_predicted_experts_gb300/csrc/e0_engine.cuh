@@ -47,7 +47,7 @@ constexpr int MAX_CTAS = 160;
 constexpr int HEAD_ROWS = 64;                 // max fc1 rows per U_HEAD unit
 constexpr int RANKS_MAX = 64;                 // max LoRA rank
 constexpr int KINDS_MAX = 3;
-constexpr int LMAX = 64;                      // layers per launch
+constexpr int LMAX = 48;                      // layers per launch
 constexpr float RMS_EPS = 1e-6f;
 
 constexpr uint16_t UF_LOCAL_V = 1;
@@ -109,8 +109,13 @@ struct LayerDesc {
   const uint16_t* lres;
   // own gate
   const uint16_t* router;
+  const float* score_bias;  // sigmoid-group routing: selection bias of this layer's routing (nullable)
+  const uint32_t* ready;    // stack, slot pools: word equal to the token index once this layer's
+                            // experts and slot_of table are in place (nullable)
   int32_t plan_kind;  // KIND_MAIN or KIND_MAIN_NOHEAD
   int32_t prerouted;  // 1: routing comes from the previous layer's head (after step 0)
+  int32_t ahead;      // N > 0: route-ahead, this layer's gate runs on layer (l - N)'s input
+  int32_t gate_for;   // stack: the layer whose route-ahead gate rows run on this layer's input, or -1
 };
 
 // Workspace: header, then parity-duplicated buffers so that one launch uses one half
@@ -139,10 +144,10 @@ struct WsLayout {
   size_t total;
 };
 
-__host__ __device__ inline size_t ws_align(size_t x) { return (x + 255) & ~size_t(255); }
+__host__ __device__ constexpr size_t ws_align(size_t x) { return (x + 255) & ~size_t(255); }
 
-__host__ __device__ inline WsLayout ws_layout(int E, int L) {
-  WsLayout w;
+__host__ __device__ constexpr WsLayout ws_layout(int E, int L) {
+  WsLayout w{};
   size_t o = 256;
   w.counters = o; o = ws_align(o + sizeof(uint32_t) * 2 * L * 4);
   w.acc = o;      o = ws_align(o + sizeof(float) * 2 * (size_t)L * OUTMAX);
@@ -158,10 +163,18 @@ __host__ __device__ inline WsLayout ws_layout(int E, int L) {
   return w;
 }
 
+enum RouteFamily : int32_t { ROUTE_SOFTMAX = 0, ROUTE_SIGMOID_GROUP = 1 };
+
 struct EngineParams {
   int32_t d, E, F, K, L, ncta, mode, norm, out_dim, kinds, step;
+  int32_t route;               // RouteFamily
+  int32_t n_group, topk_group; // sigmoid-group routing
+  float route_scale;
   uint32_t pad0;
-  uint64_t router_mask;        // stack: bit l set = layer l routes with its own gate
+  const float* score_bias;     // single-layer calls: selection bias of the routing being chosen
+  uint64_t router_mask;        // stack: bit l set = the routing warp routes layer l from its gate
+                               // logits (own gate, or route-ahead gate rows run N layers earlier)
+  uint64_t gate_mask;          // stack: bit l set = layer l's own gate rows run on its own input
   uint64_t timeout_ns;
   const LayerDesc* layers;     // stack: device array [L]; else nullptr (inline_layer)
   const Unit* plan;            // stack: device [kinds][ncta][MAXU]; else nullptr (inline)
@@ -186,6 +199,9 @@ struct EngineParams {
   int32_t* ids_trace;
   float* w_trace;
   uint16_t* h_trace;
+  float* delta_trace;          // stack, nullable: [L][d] each layer's delta (fp32)
+  float* z_trace;              // stack, nullable: [2][L][E] gate logits used / logits committed
+  int32_t* next_ids_out;       // stack, nullable: [L][K] routing committed for the next token
   int32_t accumulate;
   int32_t pad1;
   uint64_t* trace;             // nullable: [ncta][L][16] %globaltimer diagnostics: 0 layer start,

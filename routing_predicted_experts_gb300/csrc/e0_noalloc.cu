@@ -17,12 +17,15 @@
 // GPU share the array and race, so order them on one stream.
 #include <mutex>
 
-#include "e0_common.cuh"
+#include "e0_engine.cuh"
 
 namespace {
 
 constexpr size_t NOALLOC_SCRATCH_BYTES = 128 * 1024;  // upper bound on the workspace used
 constexpr int NOALLOC_MAX_DEVICES = 64;
+// every valid dims fits: the single-layer workspace grows only with E (<= EMAX)
+static_assert(e0eng::ws_layout(e0eng::EMAX, 1).total <= NOALLOC_SCRATCH_BYTES,
+              "the scratch array must hold the largest single-layer workspace");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
 
@@ -54,12 +57,17 @@ extern "C" e0_status e0_moe_decode_layer_noalloc(const e0_dims* dims, const e0_e
                                                  float* next_logits, int32_t* next_ids, float* next_weights,
                                                  e0_stream stream) {
   E0_REQUIRE(dims, E0_ERR_INVALID, "e0_moe_decode_layer_noalloc: dims is NULL");
+  // every argument check comes before anything is queued on the stream
+  e0_status st = e0::check_dims(dims);
+  if (st != E0_OK) return st;
+  E0_REQUIRE(routed && h_in && ids && logits && h_out, E0_ERR_INVALID,
+             "e0_moe_decode_layer_noalloc: NULL required argument");
   const size_t need = e0_workspace_size(dims, 1);
   E0_REQUIRE(need > 0, E0_ERR_SHAPE, "e0_moe_decode_layer_noalloc: unsupported dims");
   E0_REQUIRE(need <= NOALLOC_SCRATCH_BYTES, E0_ERR_NOMEM,
              "e0_moe_decode_layer_noalloc: these dims need a workspace larger than the built-in 128 KiB scratch");
   void* ws = nullptr;
-  e0_status st = noalloc_scratch(&ws);
+  st = noalloc_scratch(&ws);
   if (st != E0_OK) return st;
   E0_CHECK_CUDA(cudaMemsetAsync(ws, 0, need, (cudaStream_t)stream));
   return e0_moe_decode_layer(dims, routed, shared, lora, head, h_in, ids, logits, ids_prev, 1, h_out, delta_f32,

@@ -410,12 +410,37 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
 }
 
 // ------------------------------------------------------------------ small kernels
-// Routing: one warp per token, top-K of the logits and their renormalised softmax.
+// Routing family of a call ("The Other Half of the Memory Wall", Appendix A).
+struct RouteArgs {
+  int32_t family;              // E0_ROUTE_*
+  int32_t n_group, topk_group;
+  float scale;
+  const float* sbias;          // sigmoid-group selection bias [E] (nullable)
+};
+
+// Routing: one warp per token.  Softmax-top-K: top-K of the logits and their
+// renormalised softmax; sigmoid-group: sigmoid_group_route.
 template <int NPL>
-__global__ void route_kernel(const float* logits, int T, int E, int K, int32_t* ids, float* w, int32_t* ids_out,
-                             float* w_out) {
+__global__ void route_kernel(const float* logits, int T, int E, int K, RouteArgs ra, int32_t* ids, float* w,
+                             int32_t* ids_out, float* w_out) {
   const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (t >= T) return;
+  if (ra.family == E0_ROUTE_SIGMOID_GROUP) {
+    int id;
+    float wk;
+    sigmoid_group_route(logits + (size_t)t * E, ra.sbias, E, K, ra.n_group, ra.topk_group, ra.scale, lane, id, wk);
+    if (lane < K && id < 0) {  // NaN logits leave no id: contribute nothing through expert 0
+      id = 0;
+      wk = 0.f;
+    }
+    if (lane < K) {
+      ids[t * K + lane] = id;
+      w[t * K + lane] = wk;
+      if (ids_out) ids_out[t * K + lane] = id;
+      if (w_out) w_out[t * K + lane] = wk;
+    }
+    return;
+  }
   float z[NPL];
 #pragma unroll
   for (int j = 0; j < NPL; ++j) {
@@ -684,6 +709,10 @@ extern "C" e0_status e0_moe_prefill_layer(const e0_dims* dims, const e0_experts*
                                           e0_stream stream) {
   E0_REQUIRE(dims && routed && h_in && logits && h_out && workspace, E0_ERR_INVALID,
              "e0_moe_prefill_layer: NULL argument");
+  {
+    const e0_status cs = e0::check_route(dims);
+    if (cs != E0_OK) return cs;
+  }
   const int d = dims->d, E = dims->E, F = dims->F, K = dims->K;
   E0_REQUIRE(T >= 1 && T <= 65536 / (K > 0 ? K : 1), E0_ERR_SHAPE, "e0_moe_prefill_layer: T * K must be <= 65536");
   E0_REQUIRE(d % 256 == 0 && d >= 256 && (2 * F) % 256 == 0 && F % 64 == 0, E0_ERR_SHAPE,
@@ -731,12 +760,13 @@ extern "C" e0_status e0_moe_prefill_layer(const e0_dims* dims, const e0_experts*
 
   const int warps = 8;
   const int rb = (T + warps - 1) / warps;
+  const RouteArgs ra{dims->route, dims->n_group, dims->topk_group, dims->route_scale, dims->score_bias};
   if (E <= 256)
-    route_kernel<8><<<rb, 32 * warps, 0, st>>>(logits, T, E, K, ids, w, ids_out, weights_out);
+    route_kernel<8><<<rb, 32 * warps, 0, st>>>(logits, T, E, K, ra, ids, w, ids_out, weights_out);
   else if (E <= 512)
-    route_kernel<16><<<rb, 32 * warps, 0, st>>>(logits, T, E, K, ids, w, ids_out, weights_out);
+    route_kernel<16><<<rb, 32 * warps, 0, st>>>(logits, T, E, K, ra, ids, w, ids_out, weights_out);
   else
-    route_kernel<32><<<rb, 32 * warps, 0, st>>>(logits, T, E, K, ids, w, ids_out, weights_out);
+    route_kernel<32><<<rb, 32 * warps, 0, st>>>(logits, T, E, K, ra, ids, w, ids_out, weights_out);
   E0_CHECK_CUDA(cudaGetLastError());
   sort_kernel<<<1, 1024, 0, st>>>(ids, w, T, K, E, row_off, tile_off, inv, (int*)P(L.perm), (float*)P(L.wrow), one_row,
                                   one_tile);

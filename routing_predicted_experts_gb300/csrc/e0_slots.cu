@@ -7,7 +7,20 @@
 // expert) holding its six tensors; each layer owns S slots in HBM with the same bundle
 // layout, replaced least-recently-used.  The experts the running token uses and the
 // ones being staged are never evicted.  A miss is one asynchronous host-to-device copy
-// of the bundle on the caller's copy stream, followed by the layer's id -> slot table.
+// of the bundle on the caller's copy stream, followed by the layer's id -> slot table
+// and then the layer's ready word (the token the staging is for), which the decode
+// stack polls before it reads the layer's slots.  The routing that drives the copies
+// is the one a stack launch committed on the device; it comes to the host once, as a
+// small copy after that launch, and the bundle copies run while the next launch
+// (already queued) works through the layers before the pooled ones.
+//
+// Consistency: the pool's host record of which expert each slot holds changes only
+// for copies that were queued, and a layer's table is rewritten while it differs from
+// what the device last received; a ready word moves only after its layer's copies and
+// table are queued.  A failed call therefore leaves the record matching the device
+// once the queued copies have run, and a launch waiting for that layer times out (it
+// never reads a half-staged layer).
+#include <algorithm>
 #include <cstring>
 #include <vector>
 
@@ -23,15 +36,22 @@ struct e0_slot_pool {
   const uint8_t* host = nullptr;  // [L][E][bundle], pinned, caller-owned
   uint8_t* dev = nullptr;         // [L][S][bundle]
   int16_t* d_slot_of = nullptr;   // [L][E]
-  int16_t* h_snap = nullptr;      // pinned [L][2][E]: table snapshots for the copies
+  uint32_t* d_ready = nullptr;    // [L] tag of the last completed staging of each layer
+  uint8_t* h_snap = nullptr;      // pinned [L][2][snap]: id -> slot table (int16 [E]), then the tag
+  size_t snap = 0;                // bytes of one snapshot
   std::vector<cudaEvent_t> snap_done;  // [L][2]
+  int32_t* h_ids = nullptr;       // pinned landing buffer for committed device ids
+  size_t ids_cap = 0;             // its capacity in ids
+  cudaEvent_t ids_done = nullptr;
   std::vector<int> slot_id;       // [L][S] expert held by a slot, -1 = free
   std::vector<int> id_slot;       // [L][E]
   std::vector<uint64_t> stamp;    // [L][S] last use
   std::vector<int> cur;           // [L][KMAX] experts of the previous staging (in use by the running token)
   std::vector<int> ncur;          // [L]
   std::vector<int> flip;          // [L]
+  std::vector<uint8_t> dirty;     // [L] the device table differs from id_slot
   uint64_t clock = 0;
+  int fail_after = -1;            // tests: bundle copies left before an injected failure
 };
 
 namespace {
@@ -50,6 +70,8 @@ void bundle_layout(const e0_dims* dm, size_t off[6], size_t* total) {
   *total = o;
 }
 
+size_t table_bytes(int E) { return ((size_t)E * sizeof(int16_t) + 15) & ~size_t(15); }
+
 }  // namespace
 
 extern "C" size_t e0_expert_bundle_bytes(const e0_dims* dims, size_t* offsets6) {
@@ -63,10 +85,13 @@ extern "C" size_t e0_expert_bundle_bytes(const e0_dims* dims, size_t* offsets6) 
 extern "C" void e0_slot_pool_destroy(e0_slot_pool* p) {
   if (!p) return;
   for (cudaEvent_t e : p->snap_done)
-    if (e) cudaEventDestroy(e);
+    if (e) cudaEventSynchronize(e), cudaEventDestroy(e);
+  if (p->ids_done) cudaEventDestroy(p->ids_done);
   if (p->dev) cudaFree(p->dev);
   if (p->d_slot_of) cudaFree(p->d_slot_of);
+  if (p->d_ready) cudaFree(p->d_ready);
   if (p->h_snap) cudaFreeHost(p->h_snap);
+  if (p->h_ids) cudaFreeHost(p->h_ids);
   delete p;
 }
 
@@ -90,6 +115,7 @@ extern "C" e0_status e0_slot_pool_create(e0_slot_pool** out, const e0_dims* dims
   p->bundle = total;
   std::memcpy(p->off, off, sizeof(off));
   p->host = static_cast<const uint8_t*>(host_bundles);
+  p->snap = table_bytes(p->E) + 16;
   auto fail = [&](cudaError_t e, const char* what) {
     e0_slot_pool_destroy(p);
     return e0::cuda_fail(e, what);
@@ -100,19 +126,26 @@ extern "C" e0_status e0_slot_pool_create(e0_slot_pool** out, const e0_dims* dims
   if (e != cudaSuccess) return fail(e, "cudaMalloc(slot_of)");
   e = cudaMemset(p->d_slot_of, 0xFF, sizeof(int16_t) * (size_t)layers * p->E);  // -1: nothing resident
   if (e != cudaSuccess) return fail(e, "cudaMemset(slot_of)");
-  e = cudaHostAlloc(&p->h_snap, sizeof(int16_t) * (size_t)layers * 2 * p->E, cudaHostAllocDefault);
+  e = cudaMalloc(&p->d_ready, sizeof(uint32_t) * (size_t)layers);
+  if (e != cudaSuccess) return fail(e, "cudaMalloc(ready)");
+  e = cudaMemset(p->d_ready, 0xFF, sizeof(uint32_t) * (size_t)layers);  // no token staged yet
+  if (e != cudaSuccess) return fail(e, "cudaMemset(ready)");
+  e = cudaHostAlloc(&p->h_snap, p->snap * (size_t)layers * 2, cudaHostAllocDefault);
   if (e != cudaSuccess) return fail(e, "cudaHostAlloc(snapshots)");
   p->snap_done.assign((size_t)layers * 2, nullptr);
   for (auto& ev : p->snap_done) {
     e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
     if (e != cudaSuccess) return fail(e, "cudaEventCreate");
   }
+  e = cudaEventCreateWithFlags(&p->ids_done, cudaEventDisableTiming);
+  if (e != cudaSuccess) return fail(e, "cudaEventCreate");
   p->slot_id.assign((size_t)layers * slots, -1);
   p->id_slot.assign((size_t)layers * p->E, -1);
   p->stamp.assign((size_t)layers * slots, 0);
   p->cur.assign((size_t)layers * KMAX, -1);
   p->ncur.assign(layers, 0);
   p->flip.assign(layers, 0);
+  p->dirty.assign(layers, 0);
   e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return fail(e, "cudaDeviceSynchronize");
   *out = p;
@@ -132,61 +165,52 @@ extern "C" e0_status e0_slot_pool_view(const e0_slot_pool* p, int32_t layer, e0_
   out->n = p->S;
   out->slot_of = p->d_slot_of + (size_t)layer * p->E;
   out->stride = (int64_t)p->bundle;
+  out->ready = p->d_ready + layer;
+  return E0_OK;
+}
+
+extern "C" e0_status e0_slot_pool_resident(const e0_slot_pool* p, int32_t layer, int16_t* slot_of_out) {
+  E0_REQUIRE(p && slot_of_out, E0_ERR_INVALID, "e0_slot_pool_resident: NULL argument");
+  E0_REQUIRE(layer >= 0 && layer < p->L, E0_ERR_INVALID, "e0_slot_pool_resident: layer out of range");
+  for (int e = 0; e < p->E; ++e) slot_of_out[e] = (int16_t)p->id_slot[(size_t)layer * p->E + e];
+  return E0_OK;
+}
+
+extern "C" e0_status e0_debug_fail_copies(e0_slot_pool* p, int32_t n) {
+  E0_REQUIRE(p, E0_ERR_INVALID, "e0_debug_fail_copies: NULL pool");
+  p->fail_after = n < 0 ? -1 : n;
   return E0_OK;
 }
 
 namespace {
-e0_status stage_one(e0_slot_pool* p, int32_t layer, const int32_t* next_ids, int32_t K, cudaStream_t st,
-                    e0_stage_stats* stats);
-}  // namespace
 
-extern "C" e0_status e0_stage_slots(e0_slot_pool* p, int32_t layer, const int32_t* next_ids, int32_t K,
-                                    e0_stream copy_stream, e0_event ready, e0_stage_stats* stats) {
-  E0_REQUIRE(p && next_ids, E0_ERR_INVALID, "e0_stage_slots: NULL argument");
-  e0_status s = stage_one(p, layer, next_ids, K, (cudaStream_t)copy_stream, stats);
-  if (s != E0_OK) return s;
-  if (ready) E0_CHECK_CUDA(cudaEventRecord((cudaEvent_t)ready, (cudaStream_t)copy_stream));
-  return E0_OK;
-}
-
-extern "C" e0_status e0_stage_slots_layers(e0_slot_pool* p, const int32_t* layers, int32_t n_layers,
-                                           const int32_t* next_ids, int32_t K, e0_stream copy_stream, e0_event ready,
-                                           e0_stage_stats* stats) {
-  E0_REQUIRE(p && layers && next_ids && n_layers >= 0, E0_ERR_INVALID, "e0_stage_slots_layers: NULL argument");
-  for (int i = 0; i < n_layers; ++i) {
-    e0_status s = stage_one(p, layers[i], next_ids + (size_t)i * K, K, (cudaStream_t)copy_stream, stats);
-    if (s != E0_OK) return s;
-  }
-  if (ready) E0_CHECK_CUDA(cudaEventRecord((cudaEvent_t)ready, (cudaStream_t)copy_stream));
-  return E0_OK;
-}
-
-namespace {
-e0_status stage_one(e0_slot_pool* p, int32_t layer, const int32_t* next_ids, int32_t K, cudaStream_t st,
-                    e0_stage_stats* stats) {
+// Make ids[0..K) resident in pool layer `layer` and write `tag` into its ready word,
+// all queued on st.  Bookkeeping changes only for copies that were queued.
+e0_status stage_layer(e0_slot_pool* p, int32_t layer, const int32_t* ids, int32_t K, uint32_t tag, cudaStream_t st,
+                      e0_stage_stats* stats) {
   E0_REQUIRE(layer >= 0 && layer < p->L, E0_ERR_INVALID, "e0_stage_slots: layer out of range");
-  E0_REQUIRE(K >= 1 && K <= KMAX && 2 * K <= p->S, E0_ERR_SHAPE, "e0_stage_slots: K out of range");
   const int E = p->E, S = p->S;
+  for (int k = 0; k < K; ++k)
+    E0_REQUIRE(ids[k] >= 0 && ids[k] < E, E0_ERR_INVALID,
+               "e0_stage_slots: expert id out of range (a layer without committed routing?)");
   int* slot_id = &p->slot_id[(size_t)layer * S];
   int* id_slot = &p->id_slot[(size_t)layer * E];
   uint64_t* stamp = &p->stamp[(size_t)layer * S];
   const int* cur = &p->cur[(size_t)layer * KMAX];
   const int ncur = p->ncur[layer];
-  for (int k = 0; k < K; ++k)
-    E0_REQUIRE(next_ids[k] >= 0 && next_ids[k] < E, E0_ERR_INVALID, "e0_stage_slots: expert id out of range");
   auto pinned = [&](int id) {
     for (int k = 0; k < K; ++k)
-      if (next_ids[k] == id) return true;
+      if (ids[k] == id) return true;
     for (int k = 0; k < ncur; ++k)
       if (cur[k] == id) return true;
     return false;
   };
   e0_stage_stats s{};
-  bool changed = false;
-  for (int k = 0; k < K; ++k) {
-    const int id = next_ids[k];
+  e0_status result = E0_OK;
+  for (int k = 0; k < K && result == E0_OK; ++k) {
+    const int id = ids[k];
     bool dup = false;
-    for (int j = 0; j < k; ++j) dup = dup || next_ids[j] == id;
+    for (int j = 0; j < k; ++j) dup = dup || ids[j] == id;
     if (dup) continue;
     int slot = id_slot[id];
     if (slot >= 0) {
@@ -204,7 +228,24 @@ e0_status stage_one(e0_slot_pool* p, int32_t layer, const int32_t* next_ids, int
             victim = i;
           }
       }
-      E0_REQUIRE(victim >= 0, E0_ERR_UNSUPPORTED, "e0_stage_slots: every slot is pinned");
+      if (victim < 0) {
+        result = e0::fail(E0_ERR_UNSUPPORTED, "e0_stage_slots: every slot is pinned");
+        break;
+      }
+      cudaError_t err = cudaSuccess;
+      if (p->fail_after == 0) {
+        p->fail_after = -1;
+        err = cudaErrorInvalidValue;  // injected: as if the copy call had failed
+      } else {
+        if (p->fail_after > 0) --p->fail_after;
+        err = cudaMemcpyAsync(p->dev + ((size_t)layer * S + victim) * p->bundle,
+                              p->host + ((size_t)layer * E + id) * p->bundle, p->bundle, cudaMemcpyHostToDevice, st);
+      }
+      if (err != cudaSuccess) {
+        result = e0::cuda_fail(err, "cudaMemcpyAsync(expert bundle)");
+        break;
+      }
+      // the copy is queued: from here on the slot holds `id` for every later copy and launch
       if (slot_id[victim] >= 0) {
         id_slot[slot_id[victim]] = -1;
         ++s.evictions;
@@ -212,37 +253,87 @@ e0_status stage_one(e0_slot_pool* p, int32_t layer, const int32_t* next_ids, int
       slot_id[victim] = id;
       id_slot[id] = victim;
       slot = victim;
+      p->dirty[layer] = 1;
       ++s.misses;
       s.h2d_bytes += (int64_t)p->bundle;
-      E0_CHECK_CUDA(cudaMemcpyAsync(p->dev + ((size_t)layer * S + victim) * p->bundle,
-                                    p->host + ((size_t)layer * E + id) * p->bundle, p->bundle,
-                                    cudaMemcpyHostToDevice, st));
-      changed = true;
     }
     stamp[slot] = ++p->clock;
   }
-  if (changed) {
-    // the id -> slot table, from one of two pinned snapshots per layer (the one whose
-    // previous copy has finished)
-    const int f = p->flip[layer];
-    cudaEvent_t ev = p->snap_done[(size_t)layer * 2 + f];
-    E0_CHECK_CUDA(cudaEventSynchronize(ev));
-    int16_t* snap = p->h_snap + ((size_t)layer * 2 + f) * E;
-    for (int e = 0; e < E; ++e) snap[e] = (int16_t)id_slot[e];
-    E0_CHECK_CUDA(cudaMemcpyAsync(p->d_slot_of + (size_t)layer * E, snap, sizeof(int16_t) * E,
-                                  cudaMemcpyHostToDevice, st));
-    E0_CHECK_CUDA(cudaEventRecord(ev, st));
-    p->flip[layer] = f ^ 1;
-  }
-  int* cw = &p->cur[(size_t)layer * KMAX];
-  for (int k = 0; k < K; ++k) cw[k] = next_ids[k];
-  p->ncur[layer] = K;
   if (stats) {
     stats->hits += s.hits;
     stats->misses += s.misses;
     stats->evictions += s.evictions;
     stats->h2d_bytes += s.h2d_bytes;
   }
+  if (result != E0_OK) return result;
+  // the id -> slot table (while it differs from the device's) and the ready word, from
+  // one of two pinned snapshots per layer (the one whose previous copies have finished)
+  const int f = p->flip[layer];
+  cudaEvent_t ev = p->snap_done[(size_t)layer * 2 + f];
+  E0_CHECK_CUDA(cudaEventSynchronize(ev));
+  uint8_t* snap = p->h_snap + ((size_t)layer * 2 + f) * p->snap;
+  int16_t* table = reinterpret_cast<int16_t*>(snap);
+  uint32_t* tg = reinterpret_cast<uint32_t*>(snap + table_bytes(E));
+  if (p->dirty[layer]) {
+    for (int e = 0; e < E; ++e) table[e] = (int16_t)id_slot[e];
+    E0_CHECK_CUDA(cudaMemcpyAsync(p->d_slot_of + (size_t)layer * E, table, sizeof(int16_t) * E,
+                                  cudaMemcpyHostToDevice, st));
+    p->dirty[layer] = 0;
+  }
+  *tg = tag;
+  E0_CHECK_CUDA(cudaMemcpyAsync(p->d_ready + layer, tg, sizeof(uint32_t), cudaMemcpyHostToDevice, st));
+  E0_CHECK_CUDA(cudaEventRecord(ev, st));
+  p->flip[layer] = f ^ 1;
+  int* cw = &p->cur[(size_t)layer * KMAX];
+  for (int k = 0; k < K; ++k) cw[k] = ids[k];
+  p->ncur[layer] = K;
   return E0_OK;
 }
+
 }  // namespace
+
+extern "C" e0_status e0_stage_slots_host(e0_slot_pool* p, const int32_t* layers, int32_t n_layers,
+                                         const int32_t* ids, int32_t K, uint32_t tag, e0_stream copy_stream,
+                                         e0_event after, e0_stage_stats* stats) {
+  E0_REQUIRE(p && layers && ids && n_layers >= 0, E0_ERR_INVALID, "e0_stage_slots_host: NULL argument");
+  E0_REQUIRE(K >= 1 && K <= KMAX && 2 * K <= p->S, E0_ERR_SHAPE, "e0_stage_slots_host: K out of range");
+  const cudaStream_t st = (cudaStream_t)copy_stream;
+  if (after) E0_CHECK_CUDA(cudaStreamWaitEvent(st, (cudaEvent_t)after, 0));
+  for (int i = 0; i < n_layers; ++i) {
+    e0_status s = stage_layer(p, layers[i], ids + (size_t)i * K, K, tag, st, stats);
+    if (s != E0_OK) return s;
+  }
+  return E0_OK;
+}
+
+extern "C" e0_status e0_stage_slots(e0_slot_pool* p, const int32_t* layers, int32_t n_layers, const int32_t* next_ids,
+                                    const int32_t* rows, int32_t K, uint32_t tag, e0_stream copy_stream,
+                                    e0_event after, e0_stage_stats* stats) {
+  E0_REQUIRE(p && layers && rows && next_ids && n_layers >= 0, E0_ERR_INVALID, "e0_stage_slots: NULL argument");
+  E0_REQUIRE(K >= 1 && K <= KMAX && 2 * K <= p->S, E0_ERR_SHAPE, "e0_stage_slots: K out of range");
+  int nrows = 0;
+  for (int i = 0; i < n_layers; ++i) {
+    E0_REQUIRE(rows[i] >= 0 && rows[i] < 65536, E0_ERR_INVALID, "e0_stage_slots: row out of range");
+    nrows = std::max(nrows, rows[i] + 1);
+  }
+  if (n_layers == 0) return E0_OK;
+  const size_t need = (size_t)nrows * K;
+  if (need > p->ids_cap) {
+    // (every earlier call waited for its own landing copy, so the old buffer is idle)
+    if (p->h_ids) cudaFreeHost(p->h_ids);
+    p->h_ids = nullptr;
+    p->ids_cap = 0;
+    E0_CHECK_CUDA(cudaHostAlloc(&p->h_ids, need * sizeof(int32_t), cudaHostAllocDefault));
+    p->ids_cap = need;
+  }
+  const cudaStream_t st = (cudaStream_t)copy_stream;
+  if (after) E0_CHECK_CUDA(cudaStreamWaitEvent(st, (cudaEvent_t)after, 0));
+  E0_CHECK_CUDA(cudaMemcpyAsync(p->h_ids, next_ids, need * sizeof(int32_t), cudaMemcpyDeviceToHost, st));
+  E0_CHECK_CUDA(cudaEventRecord(p->ids_done, st));
+  E0_CHECK_CUDA(cudaEventSynchronize(p->ids_done));
+  for (int i = 0; i < n_layers; ++i) {
+    e0_status s = stage_layer(p, layers[i], p->h_ids + (size_t)rows[i] * K, K, tag, st, stats);
+    if (s != E0_OK) return s;
+  }
+  return E0_OK;
+}

@@ -68,15 +68,35 @@ def draws_u64(seed: int, stream: int, index: np.ndarray) -> np.ndarray:
 
 
 def normal_f32(seed: int, name: str, shape, sigma: float = 1.0, offset: int = 0) -> np.ndarray:
-    """Approximately N(0, sigma^2) fp32 tensor; element i uses draws 12*(offset+i)..+11."""
+    """Approximately N(0, sigma^2) fp32 tensor; element i uses draws 12*(offset+i)..+11.
+
+    Computed in chunks of elements (all twelve draws of a chunk at once, in place) so
+    that the temporaries stay in cache; the arithmetic is the module's definition."""
     n = int(np.prod(shape)) if len(shape) else 1
-    stream = stream_id(name)
-    idx = (np.arange(n, dtype=np.uint64) + np.uint64(offset)) * np.uint64(12)
-    s = np.zeros(n, dtype=np.int64)
-    for k in range(12):
-        s += (draws_u64(seed, stream, idx + np.uint64(k)) >> np.uint64(40)).astype(np.int64)
-    v = ((s - 6 * (1 << 24)).astype(np.float64) * np.float64(sigma)) * np.float64(2.0 ** -24)
-    return v.astype(np.float32).reshape(shape)
+    base = _base(seed, stream_id(name))
+    out = np.empty(n, dtype=np.float32)
+    k = np.arange(12, dtype=np.uint64)
+    chunk = 4096
+    with np.errstate(over="ignore"):
+        for c0 in range(0, n, chunk):
+            c1 = min(n, c0 + chunk)
+            i = np.arange(c0, c1, dtype=np.uint64) + np.uint64(offset)
+            z = i[:, None] * np.uint64(12) + k[None, :] + np.uint64(1)   # draw index + 1
+            z *= _G
+            z += base
+            t = z >> np.uint64(30)
+            z ^= t
+            z *= _M1
+            np.right_shift(z, np.uint64(27), out=t)
+            z ^= t
+            z *= _M2
+            np.right_shift(z, np.uint64(31), out=t)
+            z ^= t
+            z >>= np.uint64(40)                                         # 24-bit uniforms
+            s = z.sum(axis=1).astype(np.int64)
+            v = ((s - 6 * (1 << 24)).astype(np.float64) * np.float64(sigma)) * np.float64(2.0 ** -24)
+            out[c0:c1] = v.astype(np.float32)
+    return out.reshape(shape)
 
 
 def uniform_f64(seed: int, name: str, shape) -> np.ndarray:

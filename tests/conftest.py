@@ -27,3 +27,14 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    try:
+        from _common import REPORT
+    except Exception:  # pragma: no cover
+        return
+    if REPORT:
+        terminalreporter.write_sep("-", "parity report")
+        for line in REPORT:
+            terminalreporter.write_line(line)

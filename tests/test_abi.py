@@ -40,3 +40,17 @@ def test_host_side_argument_errors_without_gpu():
     st = lib.e0_moe_decode_layer(dm, None, None, None, None, None, None, None, None, 1, None, None, None, None,
                                  None, None, 0, None)
     assert st == -2  # d = 300 unsupported
+
+
+def test_routing_family_parameters_are_checked_without_gpu():
+    lib = _lib.lib()
+    bad_groups = _lib.e0_dims(256, 64, 128, 8, _lib.E0_ROUTE_SIGMOID_GROUP, 7, 4, 2.5, None)  # 7 does not divide 64
+    st = lib.e0_moe_decode_layer(bad_groups, None, None, None, None, None, None, None, None, 1, None, None, None, None,
+                                 None, None, 0, None)
+    assert st == _lib.E0_ERR_SHAPE
+    too_few = _lib.e0_dims(256, 64, 128, 8, _lib.E0_ROUTE_SIGMOID_GROUP, 8, 0, 2.5, None)  # no group kept
+    assert lib.e0_moe_decode_layer(too_few, None, None, None, None, None, None, None, None, 1, None, None, None, None,
+                                   None, None, 0, None) == _lib.E0_ERR_SHAPE
+    unknown = _lib.e0_dims(256, 64, 128, 8, 5, 0, 0, 0.0, None)
+    assert lib.e0_moe_decode_layer(unknown, None, None, None, None, None, None, None, None, 1, None, None, None, None,
+                                   None, None, 0, None) == _lib.E0_ERR_UNSUPPORTED

@@ -39,10 +39,9 @@ def test_bytes_per_token_decomposes():
     assert (b4, b8) == (652839424, 936495616)
 
 
-def _brute_hits(trace, slots, policy):
+def _brute_pool_hits(trace, slots):
     """Hits of the pool's rule written out directly: on a miss with a full pool, evict
-    among residents outside the current and previous sets the least recently used (LRU)
-    or the one whose next use is furthest (Belady)."""
+    among residents outside the current and previous sets the least recently used."""
     resident, last, hits, prev = set(), {}, 0, set()
     clock = 0
     for t, ids in enumerate(trace):
@@ -54,28 +53,21 @@ def _brute_hits(trace, slots, policy):
             else:
                 if len(resident) >= slots:
                     cand = sorted(r for r in resident if r not in pinned)
-                    if policy == "lru":
-                        victim = min(cand, key=lambda r: last[r])
-                    else:
-                        def nxt(r):
-                            return next((u for u in range(t + 1, len(trace)) if r in trace[u]), len(trace) + 1)
-                        victim = max(cand, key=nxt)
-                    resident.discard(victim)
+                    resident.discard(min(cand, key=lambda r: last[r]))
                 resident.add(e)
             last[e] = clock
         prev = set(ids)
     return hits
 
 
-def test_lru_and_belady_hit_counts():
+def test_pool_rule_hit_counts():
+    from routing_predicted_experts_gb300 import cachesim as CS
     rng = np.random.default_rng(3)
     for _ in range(20):
         E, K, T, slots = 10, 2, 30, 5
         trace = [list(rng.choice(E, K, replace=False)) for _ in range(T)]
-        lru, bel = bench.lru_belady_hits(trace, slots)
-        assert lru == _brute_hits(trace, slots, "lru")
-        assert bel >= lru  # the furthest-next-use eviction never does worse than LRU here
-    # a cyclic trace over slots + 1 experts: LRU misses every time after warm-up
+        assert CS.pool_lru_hits(trace, slots) == _brute_pool_hits(trace, slots)
+        assert CS.belady_hits(trace, slots) >= CS.lru_hits(trace, slots)
+    # a cyclic trace over c + 1 experts: LRU misses every time after warm-up, Belady does not
     trace = [[e] for e in itertools.islice(itertools.cycle(range(4)), 40)]
-    lru, bel = bench.lru_belady_hits(trace, 3)
-    assert lru == 0 and bel > 0
+    assert CS.lru_hits(trace, 3) == 0 and CS.belady_hits(trace, 3) > 0

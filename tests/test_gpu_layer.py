@@ -5,7 +5,7 @@ import pytest
 from oracle import bf16 as OB, layer as OL, model_inputs as OM, routing as OR
 from routing_predicted_experts_gb300 import synth as S
 
-from _common import bf16_dev, bf16_host, check_bf16_protocol, check_protocol, check_topk, to_dev
+from _common import bf16_dev, bf16_host, check_bf16_protocol, check_protocol, check_route, check_topk, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -154,3 +154,37 @@ def test_qlinear_lora_matches_oracle_and_accumulates():
     _, fb = B.e0_qlinear_lora(lob, bf16_dev(X), ws)
     torch.cuda.synchronize()
     assert np.allclose(f0.cpu().numpy(), fb.cpu().numpy(), rtol=0, atol=1e-6 * fb.abs().max().item())
+
+
+def test_layer_step_sigmoid_group_routing():
+    """Sigmoid-group routing (n = 8, G = 4, s = 2.5, K = 8) in a single layer-step: the
+    combine weights of the given ids are s * sigmoid / (sum + 1e-20), and the head's
+    prediction is turned into the next layer's ids by the same family, with a selection
+    bias that moves the choice but not the weights."""
+    import torch
+    from routing_predicted_experts_gb300 import binding as B, model as M
+    sh = S.LayerShape(d=256, E=64, F=128, K=8, H=64, r=4, alpha=8.0, shared=True)
+    seed = 9
+    lay = M.build_layer(seed, 0, sh)
+    h, zc, _, _ = _inputs(seed, sh)
+    bias = S.normal_f32(seed, "sg.bias", (sh.E,), 0.05)
+    fam = {"kind": "sigmoid_group", "n_group": 8, "topk_group": 4, "scale": 2.5}
+    famb = dict(fam, bias=bias.astype(np.float64))
+    ids, _ = OR.route(zc, sh.K, fam)
+    prev, _ = OR.route(OM.supplied_logits(seed, "prev", sh.E), sh.K, fam)
+    dm = B.dims(sh.d, sh.E, sh.F, sh.K, fam, score_bias=to_dev(bias, torch.float32))
+    ws = B.e0_workspace(dm)
+    out = B.e0_moe_decode_layer(dm, lay["routed"], lay["shared"], lay["lora"], lay["head"], bf16_dev(h)[None],
+                                to_dev(ids, torch.int32)[None], to_dev(zc, torch.float32)[None],
+                                to_dev(prev, torch.int32)[None], ws)
+    torch.cuda.synchronize()
+    assert B.e0_get_device_status(ws) == 0
+    ref = OL.layer_step(h, OM.layer(seed, 0, sh), ids, zc, prev, sh.K, fam, famb)
+    check_protocol(out["delta"][0].cpu().numpy(), ref["delta"], "delta")
+    zg = out["next_logits"][0].cpu().numpy().astype(np.float64)
+    check_protocol(zg, ref["next_logits"], "next_logits")
+    gi = out["next_ids"][0].cpu().numpy()
+    check_route(gi, ref["next_logits"], sh.K, "next_ids", famb)
+    w = out["next_weights"][0].cpu().numpy()
+    assert np.abs(w - OR.route_weights(zg, gi, fam)).max() <= 1e-5
+    assert abs(w.sum() - 2.5 * OR.sigmoid(zg[gi]).sum() / (OR.sigmoid(zg[gi]).sum() + 1e-20)) <= 1e-5

@@ -1,103 +1,100 @@
-"""Bounded expert-slot pool: a decode stack whose prerouted layers read their experts
-from a few HBM slots filled from pinned host memory must produce what the fully
-resident stack produces, on the same synthetic routing trace (injected through the
-logit bias), while the pool misses, evicts and hits as the trace dictates."""
+"""Bounded expert-slot pool: consistency of the pool's record, its device id -> slot table,
+its ready words and the bytes in its slots, including after a staging call whose bundle
+copy fails (injected on the host: the copy call reports an error, nothing runs wrong on
+the GPU).  The pooled decode stack itself is checked against the oracle in
+test_gpu_stack.py (staged from the routing the GPU commits)."""
 import numpy as np
 import pytest
 
 from routing_predicted_experts_gb300 import synth as S
 
-from oracle import bf16 as OB
-
-from _common import bf16_host, check_bf16_protocol
+from _common import dev_array
 
 pytestmark = pytest.mark.gpu
 
 
-def _lru_reference(trace_l, slots, K):
-    """Host LRU with the pool's pinning rule (previous and next sets never evicted):
-    hits and misses per step, to check the library's counters."""
-    resident, stamp, clock = [], {}, 0
-    hits = misses = 0
-    prev = []
-    for ids in trace_l:
-        pinned = set(ids) | set(prev)
-        for e in ids:
-            if e in resident:
-                hits += 1
-            else:
-                misses += 1
-                if len(resident) >= slots:
-                    victim = min((r for r in resident if r not in pinned), key=lambda r: stamp[r])
-                    resident.remove(victim)
-                resident.append(e)
-            clock += 1
-            stamp[e] = clock
-        prev = list(ids)
-    return hits, misses
-
-
-@pytest.mark.parametrize("slots", [8, 11])
-def test_pooled_stack_matches_resident_stack(slots):
-    import torch
+def _pool(slots=8):
     from routing_predicted_experts_gb300 import binding as B, model as M
-    sh, seed, L, steps = S.TINY, 5, 6, 12
-    owners = {1, 2, 3, 4}
-    pre = [1 if (l - 1) in owners else 0 for l in range(L)]
-    pooled = [l for l in range(L) if pre[l]]
+    sh = S.LayerShape(d=256, E=16, F=128, K=4, H=0, r=0, alpha=1.0, shared=False)
     dm = B.dims(sh.d, sh.E, sh.F, sh.K)
-    layers = [M.build_layer(seed, l, sh, with_head=(l in owners)) for l in range(L)]
-    dense = [B.e0_layer_struct(ly["routed"], ly["shared"], ly["lora"], ly["head"], ly["router"]) for ly in layers]
-    ref_stack = B.Stack(dm, dense, pre, keepalive=layers)
-    bundles = B.host_bundles(dm, [layers[l]["routed"] for l in pooled])
-    pool = B.SlotPool(dm, len(pooled), slots, bundles)
-    structs = []
-    for l, ly in enumerate(layers):
-        routed = pool.view(pooled.index(l)) if l in pooled else ly["routed"]
-        structs.append(B.e0_layer_struct(routed, ly["shared"], ly["lora"], ly["head"], ly["router"]))
-    pool_stack = B.Stack(dm, structs, pre, keepalive=(layers, pool))
-    trace = np.stack([S.locality_trace(seed, l, steps + 1, sh.E, sh.K) for l in range(L)], axis=1)  # [t][l][K]
-    ws_a, ws_b = ref_stack.workspace(), pool_stack.workspace()
-    copy = torch.cuda.Stream()
-    comp = torch.cuda.current_stream()
-    for t in range(steps):
-        bias = np.zeros((2, L, sh.E), dtype=np.float32)
-        for l in range(L):
-            bias[0, l, trace[t, l]] = 1e4      # own-gate routing at this token
-            bias[1, l, trace[t + 1, l]] = 1e4  # what the heads commit for the next token
-        bias_d = torch.from_numpy(bias).cuda()
-        for i, l in enumerate(pooled):
-            pool.stage(i, trace[t, l], copy_stream=copy)
-        ev = torch.cuda.Event()
-        ev.record(copy)
-        comp.wait_event(ev)
-        h0 = M.hidden(seed, t, sh.d)
-        incr = M.increments(seed, t, L, sh.d)
-        outs = []
-        for stack, ws in ((ref_stack, ws_a), (pool_stack, ws_b)):
-            h_out = torch.empty(sh.d, dtype=torch.int16, device="cuda")
-            ids = torch.empty((L, sh.K), dtype=torch.int32, device="cuda")
-            stack.step(t, h0, incr, h_out, ws, ids_out=ids, logit_bias=bias_d)
-            outs.append((h_out, ids))
-        torch.cuda.synchronize()
-        assert B.e0_get_device_status(ws_a) == 0 and B.e0_get_device_status(ws_b) == 0
-        for (h_out, ids) in outs:
-            got = ids.cpu().numpy()
-            for l in range(L):
-                assert sorted(got[l].tolist()) == sorted(trace[t, l].tolist()), (t, l)
-        # same experts and arithmetic; only the order of fp32 reductions may differ
-        check_bf16_protocol(bf16_host(outs[1][0]), bf16_host(outs[0][0]), f"h_out t{t}")
-        a = OB.bf16_to_f64(bf16_host(outs[0][0]))
-        b = OB.bf16_to_f64(bf16_host(outs[1][0]))
-        assert np.abs(a - b).max() <= 4 * 2.0 ** -8 * np.abs(a).max(), t
-    hits = misses = 0
-    for l in pooled:
-        h, m = _lru_reference(trace[:steps, l], slots, sh.K)
-        hits, misses = hits + h, misses + m
+    ly = M.build_layer(7, 0, sh, with_head=False, with_lora=False)
+    bundles = B.host_bundles(dm, [ly["routed"]])
+    return B, dm, sh, B.SlotPool(dm, 1, slots, bundles), bundles
+
+
+def _check_consistent(B, dm, pool, bundles, want_tag):
+    """Device table == the pool's record; every resident expert's bundle is byte-exact in
+    its slot; the ready word holds the last completed staging's tag."""
+    import torch
+    torch.cuda.synchronize()
+    total, offs = B.expert_bundle_layout(dm)
+    view = pool.view(0).c()
+    rec = pool.resident(0)
+    dev_tab = dev_array(view.slot_of, dm.E, torch.int16).cpu().numpy()
+    assert np.array_equal(dev_tab, rec), (dev_tab, rec)
+    base = view.gate_up.q - offs[0]
+    slots = dev_array(base, view.n * total, torch.uint8).cpu().numpy().reshape(view.n, total)
+    host = bundles[0].numpy()
+    for e in range(dm.E):
+        if rec[e] >= 0:
+            assert np.array_equal(slots[rec[e]], host[e]), e
+    assert len(set(int(s) for s in rec if s >= 0)) == int((rec >= 0).sum())  # one expert per slot
+    assert dev_array(view.ready, 1, torch.int32).cpu().numpy()[0] == want_tag
+
+
+def test_staging_fills_slots_and_ready_words():
+    B, dm, sh, pool, bundles = _pool()
+    pool.stage_host([0], [[0, 1, 2, 3]], 0)
+    _check_consistent(B, dm, pool, bundles, 0)
+    pool.stage_host([0], [[4, 5, 6, 7]], 1)
+    pool.stage_host([0], [[8, 9, 10, 11]], 2)   # evicts the least recently used: 0..3
+    _check_consistent(B, dm, pool, bundles, 2)
+    rec = pool.resident(0)
+    assert all(rec[e] >= 0 for e in range(4, 12)) and all(rec[e] < 0 for e in range(4))
     st = pool.stats
-    assert (st.hits, st.misses) == (hits, misses)
-    total, _ = B.expert_bundle_layout(dm)
-    assert st.h2d_bytes == misses * total
-    assert st.evictions > 0
-    pool_stack.close()
+    assert (st.hits, st.misses, st.evictions) == (0, 12, 4)
+    pool.close()
+
+
+def test_failed_bundle_copy_leaves_the_pool_consistent():
+    """The second bundle copy of a staging call fails: the call returns the copy error,
+    only the first miss counts as resident, the device table and the ready word keep
+    their previous state, and a retry completes the staging with every slot byte-exact."""
+    from routing_predicted_experts_gb300 import _lib
+    B, dm, sh, pool, bundles = _pool()
+    pool.stage_host([0], [[0, 1, 2, 3]], 0)
+    pool.stage_host([0], [[4, 5, 6, 7]], 1)
+    _check_consistent(B, dm, pool, bundles, 1)
+    before = pool.resident(0).copy()
+    pool.fail_copies(1)
+    with pytest.raises(_lib.E0Error) as ei:
+        pool.stage_host([0], [[8, 9, 10, 11]], 2)
+    assert ei.value.status == _lib.E0_ERR_CUDA
+    rec = pool.resident(0)
+    # 8 took the least recently used unpinned slot (expert 0's); 9..11 were never copied
+    assert rec[8] == before[0] and rec[0] < 0 and all(rec[e] < 0 for e in (9, 10, 11))
+    import torch
+    torch.cuda.synchronize()
+    view = pool.view(0).c()
+    assert dev_array(view.ready, 1, torch.int32).cpu().numpy()[0] == 1  # the layer was not released
+    assert np.array_equal(dev_array(view.slot_of, dm.E, torch.int16).cpu().numpy(), before)
+    pool.stage_host([0], [[8, 9, 10, 11]], 2)  # retry
+    _check_consistent(B, dm, pool, bundles, 2)
+    rec = pool.resident(0)
+    assert all(rec[e] >= 0 for e in range(4, 12))
+    st = pool.stats
+    assert (st.misses, st.hits) == (8 + 1 + 3, 1)
+    pool.close()
+
+
+def test_bad_ids_are_refused_before_any_copy():
+    from routing_predicted_experts_gb300 import _lib
+    B, dm, sh, pool, bundles = _pool()
+    pool.stage_host([0], [[0, 1, 2, 3]], 0)
+    before = pool.resident(0).copy()
+    with pytest.raises(_lib.E0Error) as ei:
+        pool.stage_host([0], [[4, 5, 16, 7]], 1)
+    assert ei.value.status == _lib.E0_ERR_INVALID
+    assert np.array_equal(pool.resident(0), before)
+    _check_consistent(B, dm, pool, bundles, 0)
     pool.close()

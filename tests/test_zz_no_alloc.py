@@ -55,13 +55,19 @@ def test_noalloc_matches_workspace_entry_point_twice():
         check_protocol(OB.bf16_to_f64(ho), OB.bf16_to_f64(hr), f"h_out call {call}")
 
 
-def test_noalloc_rejects_dims_beyond_its_scratch():
+def test_noalloc_checks_arguments_before_queueing_anything():
+    """Every valid dims fits the built-in scratch (its workspace grows only with E, and
+    E = 1024 still fits); unsupported dims and missing pointers are refused with the
+    shape / invalid-argument status before anything is queued on the stream."""
     import torch  # noqa: F401
     from routing_predicted_experts_gb300 import _lib, binding as B
     lib = _lib.lib()
-    dm = B.dims(2048, 1024, 512, 4)  # workspace needed for E = 1024 still fits
+    dm = B.dims(2048, 1024, 512, 4)
     assert lib.e0_workspace_size(C.byref(dm), 1) <= 128 * 1024
     bad = B.dims(300, 256, 512, 4)
     st = lib.e0_moe_decode_layer_noalloc(C.byref(bad), None, None, None, None, None, None, None, None, None, None,
                                          None, None, None, None)
-    assert st != 0
+    assert st == _lib.E0_ERR_SHAPE, st
+    st = lib.e0_moe_decode_layer_noalloc(C.byref(dm), None, None, None, None, None, None, None, None, None, None,
+                                         None, None, None, None)
+    assert st == _lib.E0_ERR_INVALID, st
