@@ -113,9 +113,11 @@ typedef struct {
   const int16_t* slot_of;
   int64_t stride;
   const uint32_t* ready;  /* nullable; decode stack only: a word (a slot pool's, see
-                             e0_slot_pool_view) that equals the token index once this
+                             e0_slot_pool_view) that reaches the token index once this
                              token's experts and slot_of table are in place; the stack
-                             step waits for it (bounded) before reading either */
+                             step waits for it (bounded) before reading either.  With
+                             ready set, slot_of holds two tables [2][E], used by tokens
+                             of even and odd index */
 } e0_experts;
 
 /* Unmerged recovery LoRA linear (§3.3): y = W x + (alpha/r) * B (A x).
@@ -192,6 +194,8 @@ e0_status e0_get_device_status(const void* workspace, uint32_t* status_out, e0_s
  *   logit_bias: fp32 [E] added to the logits before top-K (nullable).
  *   logits_out fp32 [T][E]; ids_out int32 [T][K] (descending, ties -> lower id);
  *   weights_out fp32 [T][K] renormalised softmax over ids_out (nullable).
+ *   T > 1 (at most 16) reads each head weight row once for all tokens; the workspace
+ *   must then be 256-byte aligned and hold e0_decode_workspace_size(dims, T, 0, H).
  * ------------------------------------------------------------------------------ */
 e0_status e0_prerouter_forward(const e0_prerouter* head, int32_t d, int32_t E,
                                const uint16_t* h, const int32_t* ids_cur,
@@ -220,10 +224,19 @@ e0_status e0_qlinear_lora(const e0_qlora* lora, int32_t in, const uint16_t* x, i
  *   this layer used at the previous token; only read by the head).
  *   delta_f32 fp32 [T][d] nullable.  If head != NULL the call also commits the next
  *   layer's routing for the next token: next_logits fp32 [T][E], next_ids int32
- *   [T][K], next_weights fp32 [T][K] (nullable).
- *   T == 1 runs the streaming GEMV engine; T > 1 runs the tokens one after another
- *   through the same engine.
+ *   [T][K], next_weights fp32 [T][K] (nullable).  The weights follow dims->route.
+ *   T == 1 runs the streaming GEMV engine (workspace: e0_workspace_size(dims, 1)).
+ *   2 <= T <= 16 (several tokens of a batch) reads every weight once for all tokens:
+ *   the experts on the grouped tensor-core path of e0_moe_prefill_layer (each expert
+ *   any token picked, once; fp16 products, fp32 accumulation), the head with each
+ *   weight row dotted with every token's hidden state; the routed stack must hold all
+ *   E experts (no slot pool), d and 2F multiples of 256; workspace:
+ *   e0_decode_workspace_size(dims, T, lora_out, H) bytes, 256-byte aligned.
  * ------------------------------------------------------------------------------ */
+/* Workspace bytes of e0_moe_decode_layer for T tokens (lora_out: the LoRA output width,
+ * 0 without LoRA; H: the head's fc1 width, 0 without a head).  T == 1 gives
+ * e0_workspace_size(dims, 1). */
+size_t e0_decode_workspace_size(const e0_dims* dims, int32_t T, int32_t lora_out, int32_t H);
 e0_status e0_moe_decode_layer(const e0_dims* dims, const e0_experts* routed,
                               const e0_experts* shared, const e0_qlora* lora,
                               const e0_prerouter* head, const uint16_t* h_in,
@@ -325,7 +338,10 @@ size_t e0_stack_workspace_size(const e0_stack* stack);
  *             l at the next token (layers routed by the previous layer's head); both
  *             include logit_bias; rows that do not apply are left untouched;
  *   next_ids  int32 [L][K]: the routing committed for the next token (-1 on layers not
- *             routed by a head), the device ids e0_stage_slots consumes. */
+ *             routed by a head), the device ids e0_stage_slots consumes;
+ *   commit_box  e0_commit_box_device() of a commit box: each head-routed layer's committed
+ *             ids are also written there, as soon as its head is done, for
+ *             e0_stage_slots_committed to stage while the launch goes on. */
 typedef struct {
   int32_t* ids;
   float* weights;
@@ -333,6 +349,7 @@ typedef struct {
   float* delta;
   float* logits;
   int32_t* next_ids;
+  void* commit_box;
 } e0_stack_outputs;
 
 /* One decode token through all L layers.
@@ -382,7 +399,8 @@ e0_status e0_slot_pool_create(e0_slot_pool** out, const e0_dims* dims, int32_t l
                               int32_t slots, const void* host_bundles, size_t bundle_bytes);
 void e0_slot_pool_destroy(e0_slot_pool* pool);
 /* The device view of a layer's slots, to pass as e0_layer.routed (n = slots, slot_of
- * the layer's id -> slot table, stride = bundle bytes, ready = its ready word). */
+ * the layer's two id -> slot tables, int16 [2][E], for tokens of even and odd index,
+ * stride = bundle bytes, ready = its ready word). */
 e0_status e0_slot_pool_view(const e0_slot_pool* pool, int32_t layer, e0_experts* out);
 
 /* Stage the routing a decode-stack launch committed: next_ids is DEVICE int32 [*][K]
@@ -403,6 +421,24 @@ e0_status e0_stage_slots(e0_slot_pool* pool, const int32_t* layers, int32_t n_la
 e0_status e0_stage_slots_host(e0_slot_pool* pool, const int32_t* layers, int32_t n_layers,
                               const int32_t* ids, int32_t K, uint32_t tag, e0_stream copy_stream,
                               e0_event after, e0_stage_stats* stats);
+/* Staging from the routing while it is being committed.  A commit box is pinned,
+ * host-mapped memory (library-owned) that a decode-stack launch for token t writes,
+ * layer by layer, as each head finishes: the ids committed for token t + 1 and then the
+ * tag t + 1 (two halves, by the tag's parity).  e0_stage_slots_committed waits on the
+ * host (polling, bounded by timeout_ns; E0_ERR_TIMEOUT after) for each pool layer's row
+ * (rows HOST int32 [n_layers]: the stack layer of each pool layer) to carry `tag`, then
+ * stages it exactly as e0_stage_slots does.  Call it right after queueing launch `tag`
+ * behind launch `tag` - 1: the copies of token `tag` then overlap launch `tag` - 1, and
+ * launch `tag` waits only for the layers whose copies are still in flight.  Safe while
+ * launch `tag` - 1 runs: its experts are pinned in the pool and each layer keeps two
+ * id -> slot tables, for even and odd tokens. */
+typedef struct e0_commit_box e0_commit_box;
+e0_status e0_commit_box_create(e0_commit_box** out, int32_t layers);
+void e0_commit_box_destroy(e0_commit_box* box);
+void* e0_commit_box_device(const e0_commit_box* box);
+e0_status e0_stage_slots_committed(e0_slot_pool* pool, const e0_commit_box* box, const int32_t* layers,
+                                   const int32_t* rows, int32_t n_layers, int32_t K, uint32_t tag,
+                                   e0_stream copy_stream, uint64_t timeout_ns, e0_stage_stats* stats);
 /* The pool's own record of a layer's id -> slot table (HOST int16 [E], -1 = absent), as
  * it will be on the device once the queued copies have run. */
 e0_status e0_slot_pool_resident(const e0_slot_pool* pool, int32_t layer, int16_t* slot_of_out);

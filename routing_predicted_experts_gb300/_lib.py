@@ -69,7 +69,8 @@ class e0_layer(C.Structure):
 
 
 class e0_stack_outputs(C.Structure):
-    _fields_ = [("ids", vp), ("weights", vp), ("h_trace", vp), ("delta", vp), ("logits", vp), ("next_ids", vp)]
+    _fields_ = [("ids", vp), ("weights", vp), ("h_trace", vp), ("delta", vp), ("logits", vp), ("next_ids", vp),
+                ("commit_box", vp)]
 
 
 P = C.POINTER
@@ -88,6 +89,7 @@ PROTOTYPES = {
     "e0_moe_decode_layer_noalloc": (i32, [P(e0_dims), P(e0_experts), P(e0_experts), P(e0_qlora), P(e0_prerouter),
                                           vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
     "e0_prefill_workspace_size": (sz, [P(e0_dims), i32, i32]),
+    "e0_decode_workspace_size": (sz, [P(e0_dims), i32, i32, i32]),
     "e0_moe_prefill_layer": (i32, [P(e0_dims), P(e0_experts), P(e0_experts), P(e0_qlora), vp, vp, i32, vp, vp, vp,
                                    vp, vp, sz, vp]),
     "e0_expert_bundle_bytes": (sz, [P(e0_dims), vp]),
@@ -97,6 +99,10 @@ PROTOTYPES = {
     "e0_stage_slots": (i32, [vp, vp, i32, vp, vp, i32, u32, vp, vp, P(e0_stage_stats)]),
     "e0_stage_slots_host": (i32, [vp, vp, i32, vp, i32, u32, vp, vp, P(e0_stage_stats)]),
     "e0_slot_pool_resident": (i32, [vp, i32, vp]),
+    "e0_commit_box_create": (i32, [P(vp), i32]),
+    "e0_commit_box_destroy": (None, [vp]),
+    "e0_commit_box_device": (vp, [vp]),
+    "e0_stage_slots_committed": (i32, [vp, vp, vp, vp, i32, i32, u32, vp, u64, P(e0_stage_stats)]),
     "e0_debug_fail_copies": (i32, [vp, i32]),
     "e0_stack_create": (i32, [P(vp), P(e0_dims), P(e0_layer), i32, vp]),
     "e0_stack_destroy": (None, [vp]),

@@ -105,6 +105,7 @@ def dims(d: int, E: int, F: int, K: int, family: Optional[dict] = None,
         dm.topk_group = int(family["topk_group"])
         dm.route_scale = float(family["scale"])
         dm.score_bias = _p(score_bias)
+        dm._keepalive = score_bias  # the struct holds only the address
     return dm
 
 
@@ -125,6 +126,12 @@ def e0_pack_int4(w: torch.Tensor, layout: int = L.E0_LAYOUT_ROWS, out: Optional[
     check(lib().e0_pack_int4(_p(w.contiguous()), b, rows, cols, 64, layout, _p(out.q), _p(out.scale),
                              _p(out.bias), _stream(stream)))
     return out
+
+
+def e0_decode_workspace(dm: L.e0_dims, T: int, lora_out: int = 0, H: int = 0, device=None) -> torch.Tensor:
+    """Zeroed workspace of e0_moe_decode_layer / e0_prerouter_forward for T tokens."""
+    n = lib().e0_decode_workspace_size(C.byref(dm), T, lora_out, H)
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
 
 def e0_workspace(dm: L.e0_dims, layers: int = 1, device=None) -> torch.Tensor:
@@ -249,12 +256,13 @@ class Stack:
 
     def step(self, step: int, h0: torch.Tensor, incr: torch.Tensor, h_out: torch.Tensor, ws: torch.Tensor,
              ids_out=None, w_out=None, h_trace=None, stream=None, logit_bias=None, delta=None, logits=None,
-             next_ids=None) -> None:
+             next_ids=None, commit_box=None) -> None:
         """One token; the optional outputs are e0_stack_outputs' (ids, weights, h_trace,
-        delta, logits [2][L][E], next_ids)."""
+        delta, logits [2][L][E], next_ids, commit_box: a CommitBox)."""
         outs = None
-        if any(t is not None for t in (ids_out, w_out, h_trace, delta, logits, next_ids)):
-            outs = L.e0_stack_outputs(_p(ids_out), _p(w_out), _p(h_trace), _p(delta), _p(logits), _p(next_ids))
+        if any(t is not None for t in (ids_out, w_out, h_trace, delta, logits, next_ids, commit_box)):
+            outs = L.e0_stack_outputs(_p(ids_out), _p(w_out), _p(h_trace), _p(delta), _p(logits), _p(next_ids),
+                                      commit_box.device if commit_box is not None else None)
         check(lib().e0_stack_step(self.handle, step, _p(h0), _p(incr), _p(h_out),
                                   C.byref(outs) if outs is not None else None, _p(logit_bias), _p(ws), ws.numel(),
                                   _stream(stream)))
@@ -327,6 +335,7 @@ class SlotPool:
         self.handle = h
         self.bundles = bundles
         self.E = dm.E
+        self.K = dm.K
         self.stats = L.e0_stage_stats()
 
     def view(self, layer: int) -> _RawExperts:
@@ -356,6 +365,18 @@ class SlotPool:
                                    C.c_void_p(rw.ctypes.data), next_ids.shape[-1], tag & 0xFFFFFFFF,
                                    _stream(copy_stream), _event(after), C.byref(self.stats)))
 
+    def stage_committed(self, box: "CommitBox", layers, rows, tag: int, copy_stream=None,
+                        timeout_ns: int = 2_000_000_000) -> None:
+        """Stage token `tag` from the commit box as the running launch commits each layer
+        (rows[i]: the stack layer of pool layer layers[i]); returns when every layer's
+        copies are queued."""
+        import numpy as np
+        lay = np.ascontiguousarray(np.asarray(layers, dtype=np.int32))
+        rw = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
+        check(lib().e0_stage_slots_committed(self.handle, box.handle, C.c_void_p(lay.ctypes.data),
+                                             C.c_void_p(rw.ctypes.data), len(lay), self.K, tag & 0xFFFFFFFF,
+                                             _stream(copy_stream), timeout_ns, C.byref(self.stats)))
+
     def resident(self, layer: int):
         """The pool's own id -> slot table of a layer (int16 [E], -1 = absent)."""
         import numpy as np
@@ -370,6 +391,28 @@ class SlotPool:
     def close(self):
         if self.handle:
             lib().e0_slot_pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class CommitBox:
+    """Owns an e0_commit_box: pinned host-mapped memory a stack launch writes each
+    head-routed layer's committed ids into as soon as its head is done."""
+
+    def __init__(self, layers: int):
+        h = C.c_void_p()
+        check(lib().e0_commit_box_create(C.byref(h), layers))
+        self.handle = h
+        self.device = lib().e0_commit_box_device(h)
+
+    def close(self):
+        if self.handle:
+            lib().e0_commit_box_destroy(self.handle)
             self.handle = None
 
     def __del__(self):

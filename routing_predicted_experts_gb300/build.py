@@ -11,7 +11,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libe0.so")
-SOURCES = ["e0_engine.cu", "e0_api.cu", "e0_pack.cu", "e0_noalloc.cu", "e0_prefill.cu", "e0_slots.cu"]
+SOURCES = ["e0_engine.cu", "e0_api.cu", "e0_pack.cu", "e0_noalloc.cu", "e0_prefill.cu", "e0_slots.cu",
+           "e0_multitok.cu"]
 HEADERS = ["e0_common.cuh", "e0_engine.cuh", "e0_tc.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2"]

@@ -520,6 +520,27 @@ extern "C" e0_status e0_moe_decode_layer(const e0_dims* dims, const e0_experts* 
   E0_REQUIRE(routed && h_in && ids && logits && h_out, E0_ERR_INVALID, "e0_moe_decode_layer: NULL required argument");
   E0_REQUIRE(T >= 0, E0_ERR_INVALID, "T must be >= 0");
   if (T == 0) return E0_OK;
+  if (T > 1) {
+    // several tokens: each weight read once for all of them (grouped tensor-core experts,
+    // multi-token head)
+    E0_REQUIRE(T <= 16, E0_ERR_SHAPE, "e0_moe_decode_layer: T must be <= 16");
+    const bool has_head = head && head->lres;
+    E0_REQUIRE(!has_head || next_logits || next_ids, E0_ERR_INVALID, "a head needs next_logits or next_ids");
+    const int lora_out = lora && lora->w.q ? lora->out : 0;
+    const int H = has_head ? head->H : 0;
+    E0_REQUIRE(workspace && al16(workspace) && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0,
+               E0_ERR_INVALID, "workspace must be 256-byte aligned");
+    E0_REQUIRE(workspace_bytes >= e0_decode_workspace_size(dims, T, lora_out, H), E0_ERR_NOMEM,
+               "workspace smaller than e0_decode_workspace_size(dims, T, lora_out, H)");
+    const size_t pf = (e0_prefill_workspace_size(dims, T, lora_out) + 255) & ~size_t(255);
+    st = e0pf_grouped_layer(dims, routed, shared, lora, h_in, logits, ids, T, h_out, delta_f32, nullptr, nullptr,
+                            workspace, pf, stream);
+    if (st) return st;
+    if (!has_head) return E0_OK;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    return e0mt_head(head, dims, h_in, ids, ids_prev, T, nullptr, next_logits, next_ids, next_weights, ws + pf,
+                     workspace_bytes - pf, reinterpret_cast<uint32_t*>(ws + 4), stream);
+  }
   st = check_ws(dims, 1, workspace, workspace_bytes);
   if (st) return st;
   E0_REQUIRE(al16(h_in) && al16(h_out) && (!delta_f32 || al16(delta_f32)), E0_ERR_INVALID,
@@ -590,6 +611,17 @@ extern "C" e0_status e0_prerouter_forward(const e0_prerouter* head, int32_t d, i
   if (T == 0) return E0_OK;
   st = check_ws(&dm, 1, workspace, workspace_bytes);
   if (st) return st;
+  if (T > 1) {
+    // several tokens: each head weight row read once for all of them
+    E0_REQUIRE(T <= 16, E0_ERR_SHAPE, "e0_prerouter_forward: T must be <= 16");
+    E0_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, E0_ERR_INVALID,
+               "workspace must be 256-byte aligned");
+    E0_REQUIRE(workspace_bytes >= 256 + e0mt_head_scratch(&dm, T, head->H), E0_ERR_NOMEM,
+               "workspace smaller than e0_decode_workspace_size(dims, T, 0, H)");
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    return e0mt_head(head, &dm, h, ids_cur, ids_prev, T, logit_bias, logits_out, ids_out, weights_out, ws + 256,
+                     workspace_bytes - 256, reinterpret_cast<uint32_t*>(ws + 4), stream);
+  }
   int ncta;
   st = device_ctas(d, &ncta);
   if (st) return st;
@@ -848,6 +880,7 @@ extern "C" e0_status e0_stack_step(e0_stack* s, int32_t step, const uint16_t* h0
     P.delta_out = outs->delta ? outs->delta + (size_t)(s->L - 1) * s->dims.d : nullptr;
     P.z_trace = outs->logits;
     P.next_ids_out = outs->next_ids;
+    P.commit_box = static_cast<uint32_t*>(outs->commit_box);
   }
   P.logit_bias = logit_bias;
   P.ws = reinterpret_cast<uint8_t*>(workspace);

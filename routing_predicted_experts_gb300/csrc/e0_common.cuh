@@ -33,6 +33,14 @@ e0_status check_route(const e0_dims* dm);  // the routing family's parameters on
 // ------------------------------------------------------------------ device helpers
 namespace e0dev {
 
+// Routing family of a call ("The Other Half of the Memory Wall", Appendix A).
+struct RouteArgs {
+  int32_t family;              // E0_ROUTE_*
+  int32_t n_group, topk_group;
+  float scale;
+  const float* sbias;          // sigmoid-group selection bias [E] (nullable)
+};
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -293,3 +301,17 @@ __device__ __forceinline__ void sigmoid_group_route(const float* z, const float*
 }
 
 }  // namespace e0dev
+
+// Host launchers shared between translation units.
+cudaError_t e0pf_route_topk(const float* logits, int T, int E, int K, const e0dev::RouteArgs& ra, int32_t* ids,
+                            float* w, cudaStream_t st);
+e0_status e0pf_grouped_layer(const e0_dims* dims, const e0_experts* routed, const e0_experts* shared,
+                             const e0_qlora* lora, const uint16_t* h_in, const float* logits,
+                             const int32_t* given_ids, int32_t T, uint16_t* h_out, float* delta_f32,
+                             int32_t* ids_out, float* weights_out, void* workspace, size_t workspace_bytes,
+                             e0_stream stream);
+e0_status e0mt_head(const e0_prerouter* head, const e0_dims* dims, const uint16_t* h, const int32_t* ids_cur,
+                    const int32_t* ids_prev, int32_t T, const float* logit_bias, float* logits_out,
+                    int32_t* ids_out, float* weights_out, void* scratch, size_t scratch_bytes, uint32_t* status,
+                    e0_stream stream);
+size_t e0mt_head_scratch(const e0_dims* dims, int32_t T, int32_t H);

@@ -269,14 +269,17 @@ __device__ __forceinline__ bool prod_keep_waiting(Prod& pr, uint64_t t0, uint32_
 // Slot pools (stack): wait (bounded) until the layer's ready word says that this
 // token's experts and id -> slot table are in place.  The word is written by a copy on
 // the pool's copy stream after the bundles and the table, so seeing it makes them
-// visible too.  False after a timeout or an abort.
+// visible too.  A pool keeps two tables per layer, for even and odd tokens, so that the
+// next token's can be written while this token runs.  False after a timeout or an abort.
 __device__ __forceinline__ bool wait_slots_ready(Prod& pr, const LayerDesc& Ld) {
   if (pr.P.mode != MODE_STACK || !Ld.ready) return true;
   const uint32_t want = (uint32_t)pr.P.step;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     bool r = false;
-    if (pr.lane == 0) r = ld_acquire_sys_u32(Ld.ready) == want;
+    // staged for this token or a later one (the next token's staging may already have
+    // finished: it leaves this token's table half and slots alone)
+    if (pr.lane == 0) r = (int32_t)(ld_acquire_sys_u32(Ld.ready) - want) >= 0;
     if (__shfl_sync(0xffffffffu, r ? 1 : 0, 0)) return true;
     if (!prod_keep_waiting(pr, t0, it)) return false;
   }
@@ -302,7 +305,8 @@ __device__ __forceinline__ void publish_route(Prod& pr, int l, int id, float w) 
   if (ready && lane < K && id != -1 && !v) raise_error(P, C, E0_DEV_BAD_ID);
   int idx = v ? id : 0;
   if (v && Ld.slot_of) {
-    idx = __ldcg(Ld.slot_of + id);
+    const int half = (P.mode == MODE_STACK && Ld.ready) ? (P.step & 1) * P.E : 0;
+    idx = __ldcg(Ld.slot_of + half + id);
     if (idx < 0) {
       v = false;
       raise_error(P, C, E0_DEV_NOT_RESIDENT);
@@ -788,31 +792,17 @@ __device__ void producer(const EngineParams& P, Ctl& C, uint8_t* ring) {
   }
 }
 
-// Routing warp: publishes every layer's route in the route table (routes known at
-// launch, then the layers that route with their own gate as their gate logits
-// complete) and, in the stack, the bookkeeping for the next token.
-__device__ void router_warp(const EngineParams& P, Ctl& C) {
-  Prod pr{P, C, nullptr, 0u, true, (int)(threadIdx.x & 31), C.epoch & 1u, C.epoch % 3u, C.epoch};
-  // The leading layers that route with their own gate and have no head need nothing
-  // from the staged routes: publish theirs first and stage the rest afterwards (the
-  // staging takes several microseconds; a head's layer needs its previous-token ids).
-  if (P.mode == MODE_STACK)
-    for (int l = 0; l < P.L && pr.ok && self_routes(P, l) && !layer_at(P, l).has_head; ++l)
-      compute_self_route(pr, l);
-  load_routes(pr);
-  if (P.mode == MODE_STACK)
-    for (int l = 0; l < P.L && pr.ok; ++l) {
-      if (self_routes(P, l))
-        compute_self_route(pr, l);
-      else
-        publish_staged_route(pr, l);
-    }
-  // Stack bookkeeping, one CTA per layer: record the ids each layer used (the heads'
-  // previous-token one-hot at the next step) and commit the next token's routing of
-  // every prerouted layer: the top-K of the logits the previous layer's head produced.
-  if (P.mode == MODE_STACK) {
+// Stack bookkeeping of this CTA's layers in [l0, l1) (layer l on CTA l % ncta): record
+// the ids each layer used (the heads' previous-token one-hot at the next step) and commit
+// the next token's routing of every head-routed layer: the top-K of the logits the
+// previous layer's head produced.
+__device__ __forceinline__ void stack_bookkeeping(Prod& pr, int l0, int l1) {
+  const EngineParams& P = pr.P;
+  Ctl& C = pr.C;
+  {
     const uint32_t pnext3 = (pr.epoch + 1) % 3u;
     for (int l = blockIdx.x; l < P.L && pr.ok; l += P.ncta) {
+      if (l < l0 || l >= l1) continue;
       compute_self_route(pr, l);
       if (!pr.ok) break;
       if (pr.lane < P.K) {
@@ -848,12 +838,54 @@ __device__ void router_warp(const EngineParams& P, Ctl& C) {
           rg_w_ptr(P, pr.par ^ 1u, l)[pr.lane] = w;
           if (P.next_ids_out) P.next_ids_out[l * P.K + pr.lane] = id;
         }
+        if (P.commit_box) {
+          // the committed ids, then the token they are for, into host-mapped memory: the
+          // host can stage this layer's experts while the launch goes on
+          uint32_t* box = P.commit_box + ((size_t)((P.step + 1) & 1) * P.L + l) * (KMAX + 1);
+          if (pr.lane < P.K) box[1 + pr.lane] = (uint32_t)id;
+          __syncwarp();
+          if (pr.lane == 0) {
+            __threadfence_system();
+            *reinterpret_cast<volatile uint32_t*>(box) = (uint32_t)(P.step + 1);
+          }
+        }
         __syncwarp();
         if (pr.lane == 0) *rg_tag_ptr(P, pr.par ^ 1u, l) = pr.epoch + 1u;
       } else if (P.next_ids_out && pr.lane < P.K) {
         P.next_ids_out[l * P.K + pr.lane] = -1;  // no head commits this layer's routing
       }
     }
+  }
+}
+
+// Routing warp: publishes every layer's route in the route table (routes known at
+// launch, then the layers that route with their own gate as their gate logits
+// complete) and, in the stack, the bookkeeping for the next token.
+__device__ void router_warp(const EngineParams& P, Ctl& C) {
+  Prod pr{P, C, nullptr, 0u, true, (int)(threadIdx.x & 31), C.epoch & 1u, C.epoch % 3u, C.epoch};
+  // The leading layers that route with their own gate and have no head need nothing
+  // from the staged routes: publish theirs first and stage the rest afterwards (the
+  // staging takes several microseconds; a head's layer needs its previous-token ids).
+  if (P.mode == MODE_STACK)
+    for (int l = 0; l < P.L && pr.ok && self_routes(P, l) && !layer_at(P, l).has_head; ++l)
+      compute_self_route(pr, l);
+  load_routes(pr);
+  if (P.mode == MODE_STACK) {
+    // routes up to the last layer not routed from gate logits, then this CTA's
+    // bookkeeping of those layers (a committed route leaves as soon as its head is done,
+    // while the launch goes on), then the trailing gate-routed layers and theirs
+    int lc = 0;
+    for (int l = 0; l < P.L; ++l)
+      if (!self_routes(P, l)) lc = l + 1;
+    for (int l = 0; l < lc && pr.ok; ++l) {
+      if (self_routes(P, l))
+        compute_self_route(pr, l);
+      else
+        publish_staged_route(pr, l);
+    }
+    stack_bookkeeping(pr, 0, lc);
+    for (int l = lc; l < P.L && pr.ok; ++l) compute_self_route(pr, l);
+    stack_bookkeeping(pr, lc, P.L);
   }
   // After an abort, mark every route published so that no consumer waits on one.
   if (pr.lane == 0 && !pr.ok)

@@ -202,6 +202,8 @@ struct EngineParams {
   float* delta_trace;          // stack, nullable: [L][d] each layer's delta (fp32)
   float* z_trace;              // stack, nullable: [2][L][E] gate logits used / logits committed
   int32_t* next_ids_out;       // stack, nullable: [L][K] routing committed for the next token
+  uint32_t* commit_box;        // stack, nullable: host-mapped [2][L][KMAX + 1]: per layer the token
+                               // index the committed ids are for (word 0), then the ids
   int32_t accumulate;
   int32_t pad1;
   uint64_t* trace;             // nullable: [ncta][L][16] %globaltimer diagnostics: 0 layer start,

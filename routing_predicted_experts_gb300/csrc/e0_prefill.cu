@@ -410,14 +410,6 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
 }
 
 // ------------------------------------------------------------------ small kernels
-// Routing family of a call ("The Other Half of the Memory Wall", Appendix A).
-struct RouteArgs {
-  int32_t family;              // E0_ROUTE_*
-  int32_t n_group, topk_group;
-  float scale;
-  const float* sbias;          // sigmoid-group selection bias [E] (nullable)
-};
-
 // Routing: one warp per token.  Softmax-top-K: top-K of the logits and their
 // renormalised softmax; sigmoid-group: sigmoid_group_route.
 template <int NPL>
@@ -462,6 +454,42 @@ __global__ void route_kernel(const float* logits, int T, int E, int K, RouteArgs
     w[t * K + lane] = ex / tot;
     if (ids_out) ids_out[t * K + lane] = id;
     if (w_out) w_out[t * K + lane] = ex / tot;
+  }
+}
+
+// Committed routing (decode of several tokens): one warp per token takes the given ids
+// and the family's combine weights of the token's logits over them: the softmax over
+// the picked logits, or scale * sigmoid / (sum + 1e-20).  An id outside [0, E) or
+// repeated is reported (E0_DEV_BAD_ID) and contributes nothing through expert 0.
+__global__ void route_given_kernel(const float* logits, const int32_t* given, int T, int E, int K, RouteArgs ra,
+                                   int32_t* ids, float* w, int32_t* ids_out, float* w_out, uint32_t* status) {
+  const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (t >= T) return;
+  int id = lane < K ? given[(size_t)t * K + lane] : -1;
+  bool v = lane < K && id >= 0 && id < E;
+  for (int j = 0; j < K; ++j) {
+    const int o = __shfl_sync(0xffffffffu, id, j);
+    if (j < lane && o == id) v = false;
+  }
+  if (lane < K && !v) atomicOr(status, (uint32_t)E0_DEV_BAD_ID);
+  const float z = v ? logits[(size_t)t * E + id] : 0.f;
+  float wk;
+  if (ra.family == E0_ROUTE_SIGMOID_GROUP) {
+    const float sig = v ? 1.0f / (1.0f + expf(-z)) : 0.f;
+    wk = ra.scale * sig / (warp_sum(sig) + 1e-20f);
+  } else {
+    float mx = v ? z : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float ex = v ? expf(z - mx) : 0.f;
+    const float tot = warp_sum(ex);
+    wk = tot > 0.f ? ex / tot : 0.f;
+  }
+  if (lane < K) {
+    ids[t * K + lane] = v ? id : 0;
+    w[t * K + lane] = v ? wk : 0.f;
+    if (ids_out) ids_out[t * K + lane] = v ? id : -1;
+    if (w_out) w_out[t * K + lane] = v ? wk : 0.f;
   }
 }
 
@@ -702,11 +730,14 @@ extern "C" size_t e0_prefill_workspace_size(const e0_dims* dims, int32_t T, int3
       .total;
 }
 
-extern "C" e0_status e0_moe_prefill_layer(const e0_dims* dims, const e0_experts* routed, const e0_experts* shared,
-                                          const e0_qlora* lora, const uint16_t* h_in, const float* logits,
-                                          int32_t T, uint16_t* h_out, float* delta_f32, int32_t* ids_out,
-                                          float* weights_out, void* workspace, size_t workspace_bytes,
-                                          e0_stream stream) {
+// The grouped (tensor-core) MoE layer for T tokens: routed by the top-K of `logits`, or,
+// when given_ids is set, by those committed ids with the combine weights of `logits`.
+// Also the multi-token decode path of e0_moe_decode_layer.
+e0_status e0pf_grouped_layer(const e0_dims* dims, const e0_experts* routed, const e0_experts* shared,
+                             const e0_qlora* lora, const uint16_t* h_in, const float* logits,
+                             const int32_t* given_ids, int32_t T, uint16_t* h_out, float* delta_f32,
+                             int32_t* ids_out, float* weights_out, void* workspace, size_t workspace_bytes,
+                             e0_stream stream) {
   E0_REQUIRE(dims && routed && h_in && logits && h_out && workspace, E0_ERR_INVALID,
              "e0_moe_prefill_layer: NULL argument");
   {
@@ -761,7 +792,10 @@ extern "C" e0_status e0_moe_prefill_layer(const e0_dims* dims, const e0_experts*
   const int warps = 8;
   const int rb = (T + warps - 1) / warps;
   const RouteArgs ra{dims->route, dims->n_group, dims->topk_group, dims->route_scale, dims->score_bias};
-  if (E <= 256)
+  if (given_ids)
+    route_given_kernel<<<rb, 32 * warps, 0, st>>>(logits, given_ids, T, E, K, ra, ids, w, ids_out, weights_out,
+                                                  status);
+  else if (E <= 256)
     route_kernel<8><<<rb, 32 * warps, 0, st>>>(logits, T, E, K, ra, ids, w, ids_out, weights_out);
   else if (E <= 512)
     route_kernel<16><<<rb, 32 * warps, 0, st>>>(logits, T, E, K, ra, ids, w, ids_out, weights_out);
@@ -817,4 +851,27 @@ extern "C" e0_status e0_moe_prefill_layer(const e0_dims* dims, const e0_experts*
   combine_kernel<<<T, 256, 0, st>>>(h_in, d, K, inv, yslot, ys, yl, h_out, delta_f32);
   E0_CHECK_CUDA(cudaGetLastError());
   return E0_OK;
+}
+
+extern "C" e0_status e0_moe_prefill_layer(const e0_dims* dims, const e0_experts* routed, const e0_experts* shared,
+                                          const e0_qlora* lora, const uint16_t* h_in, const float* logits,
+                                          int32_t T, uint16_t* h_out, float* delta_f32, int32_t* ids_out,
+                                          float* weights_out, void* workspace, size_t workspace_bytes,
+                                          e0_stream stream) {
+  return e0pf_grouped_layer(dims, routed, shared, lora, h_in, logits, nullptr, T, h_out, delta_f32, ids_out,
+                            weights_out, workspace, workspace_bytes, stream);
+}
+
+// Top-K routing of T tokens' logits by the family (one warp per token), for the other
+// translation units.
+cudaError_t e0pf_route_topk(const float* logits, int T, int E, int K, const RouteArgs& ra, int32_t* ids, float* w,
+                            cudaStream_t st) {
+  const int warps = 8, rb = (T + warps - 1) / warps;
+  if (E <= 256)
+    route_kernel<8><<<rb, 32 * warps, 0, st>>>(logits, T, E, K, ra, ids, w, nullptr, nullptr);
+  else if (E <= 512)
+    route_kernel<16><<<rb, 32 * warps, 0, st>>>(logits, T, E, K, ra, ids, w, nullptr, nullptr);
+  else
+    route_kernel<32><<<rb, 32 * warps, 0, st>>>(logits, T, E, K, ra, ids, w, nullptr, nullptr);
+  return cudaGetLastError();
 }

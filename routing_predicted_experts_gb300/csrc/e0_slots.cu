@@ -17,10 +17,14 @@
 // Consistency: the pool's host record of which expert each slot holds changes only
 // for copies that were queued, and a layer's table is rewritten while it differs from
 // what the device last received; a ready word moves only after its layer's copies and
-// table are queued.  A failed call therefore leaves the record matching the device
+// table are queued.  Each layer has two tables, for tokens of even and odd index, so
+// that the next token's staging never rewrites the table the running token reads, and
+// the LRU never evicts the running token's experts (the previous staging's).  A failed call therefore leaves the record matching the device
 // once the queued copies have run, and a launch waiting for that layer times out (it
 // never reads a half-staged layer).
 #include <algorithm>
+#include <atomic>
+#include <chrono>
 #include <cstring>
 #include <vector>
 
@@ -35,7 +39,7 @@ struct e0_slot_pool {
   size_t off[6] = {};
   const uint8_t* host = nullptr;  // [L][E][bundle], pinned, caller-owned
   uint8_t* dev = nullptr;         // [L][S][bundle]
-  int16_t* d_slot_of = nullptr;   // [L][E]
+  int16_t* d_slot_of = nullptr;   // [L][2][E]: tables for tokens of even and odd index
   uint32_t* d_ready = nullptr;    // [L] tag of the last completed staging of each layer
   uint8_t* h_snap = nullptr;      // pinned [L][2][snap]: id -> slot table (int16 [E]), then the tag
   size_t snap = 0;                // bytes of one snapshot
@@ -49,9 +53,17 @@ struct e0_slot_pool {
   std::vector<int> cur;           // [L][KMAX] experts of the previous staging (in use by the running token)
   std::vector<int> ncur;          // [L]
   std::vector<int> flip;          // [L]
-  std::vector<uint8_t> dirty;     // [L] the device table differs from id_slot
+  std::vector<uint8_t> dirty;     // [L][2] the device table of that parity differs from id_slot
   uint64_t clock = 0;
   int fail_after = -1;            // tests: bundle copies left before an injected failure
+  // the copies of a staging call are spread over a few streams of the pool's own (layer l
+  // on stream l % NCS), forked from and joined back into the caller's copy stream: each
+  // copy operation has a fixed cost, and independent streams let several copy engines
+  // take them at once
+  static constexpr int NCS = 4;
+  cudaStream_t cs[NCS] = {};
+  cudaEvent_t fork_ev = nullptr;
+  cudaEvent_t join_ev[NCS] = {};
 };
 
 namespace {
@@ -87,6 +99,11 @@ extern "C" void e0_slot_pool_destroy(e0_slot_pool* p) {
   for (cudaEvent_t e : p->snap_done)
     if (e) cudaEventSynchronize(e), cudaEventDestroy(e);
   if (p->ids_done) cudaEventDestroy(p->ids_done);
+  for (int i = 0; i < e0_slot_pool::NCS; ++i) {
+    if (p->cs[i]) cudaStreamSynchronize(p->cs[i]), cudaStreamDestroy(p->cs[i]);
+    if (p->join_ev[i]) cudaEventDestroy(p->join_ev[i]);
+  }
+  if (p->fork_ev) cudaEventDestroy(p->fork_ev);
   if (p->dev) cudaFree(p->dev);
   if (p->d_slot_of) cudaFree(p->d_slot_of);
   if (p->d_ready) cudaFree(p->d_ready);
@@ -122,9 +139,9 @@ extern "C" e0_status e0_slot_pool_create(e0_slot_pool** out, const e0_dims* dims
   };
   cudaError_t e = cudaMalloc(&p->dev, (size_t)layers * slots * total);
   if (e != cudaSuccess) return fail(e, "cudaMalloc(slots)");
-  e = cudaMalloc(&p->d_slot_of, sizeof(int16_t) * (size_t)layers * p->E);
+  e = cudaMalloc(&p->d_slot_of, sizeof(int16_t) * (size_t)layers * 2 * p->E);
   if (e != cudaSuccess) return fail(e, "cudaMalloc(slot_of)");
-  e = cudaMemset(p->d_slot_of, 0xFF, sizeof(int16_t) * (size_t)layers * p->E);  // -1: nothing resident
+  e = cudaMemset(p->d_slot_of, 0xFF, sizeof(int16_t) * (size_t)layers * 2 * p->E);  // -1: nothing resident
   if (e != cudaSuccess) return fail(e, "cudaMemset(slot_of)");
   e = cudaMalloc(&p->d_ready, sizeof(uint32_t) * (size_t)layers);
   if (e != cudaSuccess) return fail(e, "cudaMalloc(ready)");
@@ -139,13 +156,21 @@ extern "C" e0_status e0_slot_pool_create(e0_slot_pool** out, const e0_dims* dims
   }
   e = cudaEventCreateWithFlags(&p->ids_done, cudaEventDisableTiming);
   if (e != cudaSuccess) return fail(e, "cudaEventCreate");
+  e = cudaEventCreateWithFlags(&p->fork_ev, cudaEventDisableTiming);
+  if (e != cudaSuccess) return fail(e, "cudaEventCreate");
+  for (int i = 0; i < e0_slot_pool::NCS; ++i) {
+    e = cudaStreamCreateWithFlags(&p->cs[i], cudaStreamNonBlocking);
+    if (e != cudaSuccess) return fail(e, "cudaStreamCreate");
+    e = cudaEventCreateWithFlags(&p->join_ev[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) return fail(e, "cudaEventCreate");
+  }
   p->slot_id.assign((size_t)layers * slots, -1);
   p->id_slot.assign((size_t)layers * p->E, -1);
   p->stamp.assign((size_t)layers * slots, 0);
   p->cur.assign((size_t)layers * KMAX, -1);
   p->ncur.assign(layers, 0);
   p->flip.assign(layers, 0);
-  p->dirty.assign(layers, 0);
+  p->dirty.assign((size_t)layers * 2, 0);
   e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return fail(e, "cudaDeviceSynchronize");
   *out = p;
@@ -163,7 +188,7 @@ extern "C" e0_status e0_slot_pool_view(const e0_slot_pool* p, int32_t layer, e0_
   out->down.scale = reinterpret_cast<const uint16_t*>(base + p->off[4]);
   out->down.bias = reinterpret_cast<const uint16_t*>(base + p->off[5]);
   out->n = p->S;
-  out->slot_of = p->d_slot_of + (size_t)layer * p->E;
+  out->slot_of = p->d_slot_of + (size_t)layer * 2 * p->E;
   out->stride = (int64_t)p->bundle;
   out->ready = p->d_ready + layer;
   return E0_OK;
@@ -184,11 +209,28 @@ extern "C" e0_status e0_debug_fail_copies(e0_slot_pool* p, int32_t n) {
 
 namespace {
 
+// The pool's streams start after everything queued on st so far.
+e0_status fork(e0_slot_pool* p, cudaStream_t st) {
+  E0_CHECK_CUDA(cudaEventRecord(p->fork_ev, st));
+  for (int i = 0; i < e0_slot_pool::NCS; ++i) E0_CHECK_CUDA(cudaStreamWaitEvent(p->cs[i], p->fork_ev, 0));
+  return E0_OK;
+}
+// st continues after everything queued on the pool's streams.
+e0_status join(e0_slot_pool* p, cudaStream_t st) {
+  for (int i = 0; i < e0_slot_pool::NCS; ++i) {
+    E0_CHECK_CUDA(cudaEventRecord(p->join_ev[i], p->cs[i]));
+    E0_CHECK_CUDA(cudaStreamWaitEvent(st, p->join_ev[i], 0));
+  }
+  return E0_OK;
+}
+
 // Make ids[0..K) resident in pool layer `layer` and write `tag` into its ready word,
-// all queued on st.  Bookkeeping changes only for copies that were queued.
-e0_status stage_layer(e0_slot_pool* p, int32_t layer, const int32_t* ids, int32_t K, uint32_t tag, cudaStream_t st,
+// all queued on one of the pool's streams (layer % NCS).  Bookkeeping changes only for
+// copies that were queued.
+e0_status stage_layer(e0_slot_pool* p, int32_t layer, const int32_t* ids, int32_t K, uint32_t tag,
                       e0_stage_stats* stats) {
   E0_REQUIRE(layer >= 0 && layer < p->L, E0_ERR_INVALID, "e0_stage_slots: layer out of range");
+  const cudaStream_t st = p->cs[layer % e0_slot_pool::NCS];
   const int E = p->E, S = p->S;
   for (int k = 0; k < K; ++k)
     E0_REQUIRE(ids[k] >= 0 && ids[k] < E, E0_ERR_INVALID,
@@ -253,7 +295,7 @@ e0_status stage_layer(e0_slot_pool* p, int32_t layer, const int32_t* ids, int32_
       slot_id[victim] = id;
       id_slot[id] = victim;
       slot = victim;
-      p->dirty[layer] = 1;
+      p->dirty[(size_t)layer * 2] = p->dirty[(size_t)layer * 2 + 1] = 1;
       ++s.misses;
       s.h2d_bytes += (int64_t)p->bundle;
     }
@@ -266,19 +308,21 @@ e0_status stage_layer(e0_slot_pool* p, int32_t layer, const int32_t* ids, int32_
     stats->h2d_bytes += s.h2d_bytes;
   }
   if (result != E0_OK) return result;
-  // the id -> slot table (while it differs from the device's) and the ready word, from
-  // one of two pinned snapshots per layer (the one whose previous copies have finished)
+  // the id -> slot table of the tag's parity (while it differs from the device's) and the
+  // ready word, from one of two pinned snapshots per layer (the one whose previous copies
+  // have finished); the other parity's table stays as the running token reads it
+  const int half = (int)(tag & 1u);
   const int f = p->flip[layer];
   cudaEvent_t ev = p->snap_done[(size_t)layer * 2 + f];
   E0_CHECK_CUDA(cudaEventSynchronize(ev));
   uint8_t* snap = p->h_snap + ((size_t)layer * 2 + f) * p->snap;
   int16_t* table = reinterpret_cast<int16_t*>(snap);
   uint32_t* tg = reinterpret_cast<uint32_t*>(snap + table_bytes(E));
-  if (p->dirty[layer]) {
+  if (p->dirty[(size_t)layer * 2 + half]) {
     for (int e = 0; e < E; ++e) table[e] = (int16_t)id_slot[e];
-    E0_CHECK_CUDA(cudaMemcpyAsync(p->d_slot_of + (size_t)layer * E, table, sizeof(int16_t) * E,
+    E0_CHECK_CUDA(cudaMemcpyAsync(p->d_slot_of + ((size_t)layer * 2 + half) * E, table, sizeof(int16_t) * E,
                                   cudaMemcpyHostToDevice, st));
-    p->dirty[layer] = 0;
+    p->dirty[(size_t)layer * 2 + half] = 0;
   }
   *tg = tag;
   E0_CHECK_CUDA(cudaMemcpyAsync(p->d_ready + layer, tg, sizeof(uint32_t), cudaMemcpyHostToDevice, st));
@@ -299,11 +343,10 @@ extern "C" e0_status e0_stage_slots_host(e0_slot_pool* p, const int32_t* layers,
   E0_REQUIRE(K >= 1 && K <= KMAX && 2 * K <= p->S, E0_ERR_SHAPE, "e0_stage_slots_host: K out of range");
   const cudaStream_t st = (cudaStream_t)copy_stream;
   if (after) E0_CHECK_CUDA(cudaStreamWaitEvent(st, (cudaEvent_t)after, 0));
-  for (int i = 0; i < n_layers; ++i) {
-    e0_status s = stage_layer(p, layers[i], ids + (size_t)i * K, K, tag, st, stats);
-    if (s != E0_OK) return s;
-  }
-  return E0_OK;
+  e0_status s = fork(p, st);
+  for (int i = 0; i < n_layers && s == E0_OK; ++i) s = stage_layer(p, layers[i], ids + (size_t)i * K, K, tag, stats);
+  const e0_status j = join(p, st);
+  return s != E0_OK ? s : j;
 }
 
 extern "C" e0_status e0_stage_slots(e0_slot_pool* p, const int32_t* layers, int32_t n_layers, const int32_t* next_ids,
@@ -331,9 +374,72 @@ extern "C" e0_status e0_stage_slots(e0_slot_pool* p, const int32_t* layers, int3
   E0_CHECK_CUDA(cudaMemcpyAsync(p->h_ids, next_ids, need * sizeof(int32_t), cudaMemcpyDeviceToHost, st));
   E0_CHECK_CUDA(cudaEventRecord(p->ids_done, st));
   E0_CHECK_CUDA(cudaEventSynchronize(p->ids_done));
-  for (int i = 0; i < n_layers; ++i) {
-    e0_status s = stage_layer(p, layers[i], p->h_ids + (size_t)rows[i] * K, K, tag, st, stats);
-    if (s != E0_OK) return s;
+  e0_status s = fork(p, st);
+  for (int i = 0; i < n_layers && s == E0_OK; ++i)
+    s = stage_layer(p, layers[i], p->h_ids + (size_t)rows[i] * K, K, tag, stats);
+  const e0_status j = join(p, st);
+  return s != E0_OK ? s : j;
+}
+
+// ------------------------------------------------------------------ commit box
+struct e0_commit_box {
+  int L = 0;
+  uint32_t* host = nullptr;  // pinned, mapped: [2][L][KMAX + 1]
+  uint32_t* dev = nullptr;   // the same memory as the device addresses it
+};
+
+extern "C" void e0_commit_box_destroy(e0_commit_box* b) {
+  if (!b) return;
+  if (b->host) cudaFreeHost(b->host);
+  delete b;
+}
+
+extern "C" e0_status e0_commit_box_create(e0_commit_box** out, int32_t layers) {
+  E0_REQUIRE(out && layers >= 1 && layers <= LMAX, E0_ERR_INVALID, "e0_commit_box_create: need 1..48 layers");
+  *out = nullptr;
+  e0_commit_box* b = new e0_commit_box;
+  b->L = layers;
+  const size_t words = (size_t)2 * layers * (KMAX + 1);
+  cudaError_t e = cudaHostAlloc(&b->host, words * sizeof(uint32_t), cudaHostAllocMapped);
+  if (e == cudaSuccess) e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&b->dev), b->host, 0);
+  if (e != cudaSuccess) {
+    e0_commit_box_destroy(b);
+    return e0::cuda_fail(e, "e0_commit_box_create");
   }
+  for (size_t i = 0; i < words; ++i) b->host[i] = 0xFFFFFFFFu;  // no token committed yet
+  *out = b;
   return E0_OK;
+}
+
+extern "C" void* e0_commit_box_device(const e0_commit_box* b) { return b ? b->dev : nullptr; }
+
+extern "C" e0_status e0_stage_slots_committed(e0_slot_pool* p, const e0_commit_box* box, const int32_t* layers,
+                                              const int32_t* rows, int32_t n_layers, int32_t K, uint32_t tag,
+                                              e0_stream copy_stream, uint64_t timeout_ns, e0_stage_stats* stats) {
+  E0_REQUIRE(p && box && layers && rows && n_layers >= 0, E0_ERR_INVALID, "e0_stage_slots_committed: NULL argument");
+  E0_REQUIRE(K >= 1 && K <= KMAX && 2 * K <= p->S, E0_ERR_SHAPE, "e0_stage_slots_committed: K out of range");
+  for (int i = 0; i < n_layers; ++i)
+    E0_REQUIRE(rows[i] >= 0 && rows[i] < box->L, E0_ERR_INVALID, "e0_stage_slots_committed: row out of range");
+  const cudaStream_t st = (cudaStream_t)copy_stream;
+  const auto t0 = std::chrono::steady_clock::now();
+  e0_status s = fork(p, st);
+  for (int i = 0; i < n_layers && s == E0_OK; ++i) {
+    const volatile uint32_t* row = box->host + ((size_t)(tag & 1u) * box->L + rows[i]) * (KMAX + 1);
+    // the launch writes the ids, then (after a system-scope fence) the tag
+    for (uint32_t it = 0; row[0] != tag; ++it) {
+      if ((it & 255u) == 0 &&
+          (uint64_t)std::chrono::duration_cast<std::chrono::nanoseconds>(std::chrono::steady_clock::now() - t0)
+                  .count() > timeout_ns)
+      {
+        join(p, st);
+        return e0::fail(E0_ERR_TIMEOUT, "e0_stage_slots_committed: the launch did not commit this layer in time");
+      }
+    }
+    std::atomic_thread_fence(std::memory_order_acquire);
+    int32_t ids[KMAX];
+    for (int k = 0; k < K; ++k) ids[k] = (int32_t)row[1 + k];
+    s = stage_layer(p, layers[i], ids, K, tag, stats);
+  }
+  const e0_status j = join(p, st);
+  return s != E0_OK ? s : j;
 }

@@ -98,7 +98,7 @@ class DevView:
     """A device array given by raw pointer, readable by torch.as_tensor (tests only)."""
 
     def __init__(self, ptr, n, typestr):
-        self.__cuda_array_interface__ = {"shape": (n,), "typestr": typestr, "data": (int(ptr), True),
+        self.__cuda_array_interface__ = {"shape": (n,), "typestr": typestr, "data": (int(ptr), False),
                                          "version": 2}
 
 

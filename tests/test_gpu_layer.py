@@ -172,7 +172,8 @@ def test_layer_step_sigmoid_group_routing():
     famb = dict(fam, bias=bias.astype(np.float64))
     ids, _ = OR.route(zc, sh.K, fam)
     prev, _ = OR.route(OM.supplied_logits(seed, "prev", sh.E), sh.K, fam)
-    dm = B.dims(sh.d, sh.E, sh.F, sh.K, fam, score_bias=to_dev(bias, torch.float32))
+    bias_dev = to_dev(bias, torch.float32)
+    dm = B.dims(sh.d, sh.E, sh.F, sh.K, fam, score_bias=bias_dev)
     ws = B.e0_workspace(dm)
     out = B.e0_moe_decode_layer(dm, lay["routed"], lay["shared"], lay["lora"], lay["head"], bf16_dev(h)[None],
                                 to_dev(ids, torch.int32)[None], to_dev(zc, torch.float32)[None],

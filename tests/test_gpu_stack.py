@@ -82,53 +82,58 @@ def run_lockstep(seed, sh, L, head_owners, steps, route_src=None, check_layers=N
     # step-0 routing of pooled layers is forced (logit bias) onto known ids, which prime the
     # pool: the first token's routing is not committed by any head
     prime = {l: np.arange(K, dtype=np.int32) + (l % max(1, E // K - 1)) * K for l in pooled}
-    zhat_prev, ids_prev, prev_next, prev_logits1 = {}, {}, None, None
-    ambiguous = decisions = 0
-    staged = {l: [] for l in pooled}
-    end_prev = None
-    free = {"zhat": {}, "ids": {}}  # the free-running oracle's state (drift)
+    # ---- every launch (and, for a pool, the staging of each next token) is queued first,
+    # the way a decode loop runs: token t's experts are staged from the ids launch t-1
+    # commits, layer by layer, while launch t-1 still runs and launch t waits for them
+    box = B.CommitBox(L) if pool else None
+    runs = []
     for t in range(steps):
-        h0 = M.hidden(seed, t, d)
-        incr = M.increments(seed, t, L, d)
-        h_out = torch.empty(d, dtype=torch.int16, device="cuda")
-        ids_t = torch.empty((L, K), dtype=torch.int32, device="cuda")
-        w_t = torch.empty((L, K), dtype=torch.float32, device="cuda")
-        h_tr = torch.empty((L, d), dtype=torch.int16, device="cuda")
-        dl_t = torch.empty((L, d), dtype=torch.float32, device="cuda")
-        zl_t = torch.zeros((2, L, E), dtype=torch.float32, device="cuda")
-        nx_t = torch.empty((L, K), dtype=torch.int32, device="cuda")
-        bias = None
+        run = {"h0": M.hidden(seed, t, d), "incr": M.increments(seed, t, L, d),
+               "h_out": torch.empty(d, dtype=torch.int16, device="cuda"),
+               "ids": torch.empty((L, K), dtype=torch.int32, device="cuda"),
+               "w": torch.empty((L, K), dtype=torch.float32, device="cuda"),
+               "h_tr": torch.empty((L, d), dtype=torch.int16, device="cuda"),
+               "delta": torch.empty((L, d), dtype=torch.float32, device="cuda"),
+               "logits": torch.zeros((2, L, E), dtype=torch.float32, device="cuda"),
+               "next": torch.empty((L, K), dtype=torch.int32, device="cuda"), "bias": None}
         if pool and t == 0:
             b = np.zeros((2, L, E), dtype=np.float32)
             for l in pooled:
                 b[0, l, prime[l]] = 1e4
-            bias = torch.from_numpy(b).cuda()
+            run["bias"] = torch.from_numpy(b).cuda()
             pool.stage_host(list(range(len(pooled))), np.stack([prime[l] for l in pooled]), 0, copy_stream=copy)
-            for l in pooled:
-                staged[l].append(prime[l].tolist())
             ev = torch.cuda.Event()
             ev.record(copy)
             comp.wait_event(ev)  # (t = 0 only; later launches wait on the ready words)
-        stack.step(t, h0, incr, h_out, ws, ids_out=ids_t, w_out=w_t, h_trace=h_tr, logit_bias=bias, delta=dl_t,
-                   logits=zl_t, next_ids=nx_t)
-        end = torch.cuda.Event()
-        end.record(comp)
+        stack.step(t, run["h0"], run["incr"], run["h_out"], ws, ids_out=run["ids"], w_out=run["w"],
+                   h_trace=run["h_tr"], logit_bias=run["bias"], delta=run["delta"], logits=run["logits"],
+                   next_ids=run["next"], commit_box=box)
         if pool and t > 0:
-            # launch t is queued already: stage its experts from the ids launch t-1 committed
-            pool.stage(list(range(len(pooled))), prev_next, pooled, t, copy_stream=copy, after=end_prev)
-        torch.cuda.synchronize()
-        assert B.e0_get_device_status(ws) == 0, (label, t)
-        H, I, W = bf16_host(h_tr), ids_t.cpu().numpy(), w_t.cpu().numpy()
-        DL, ZL, NX = dl_t.cpu().numpy(), zl_t.cpu().numpy(), nx_t.cpu().numpy()
+            pool.stage_committed(box, list(range(len(pooled))), pooled, t, copy_stream=copy)
+        runs.append(run)
+    torch.cuda.synchronize()
+    assert B.e0_get_device_status(ws) == 0, label
+    if pool:
+        for i, l in enumerate(pooled):
+            view = pool.view(i).c()
+            dev_tab = dev_array(view.slot_of, 2 * E, torch.int16).cpu().numpy().reshape(2, E)
+            assert np.array_equal(dev_tab[(steps - 1) & 1], pool.resident(i)), (label, l)
+            assert dev_array(view.ready, 1, torch.int32).cpu().numpy()[0] == steps - 1
+        box.close()
+
+    zhat_prev, ids_prev, prev_next, prev_logits1 = {}, {}, None, None
+    ambiguous = decisions = 0
+    staged = {l: [prime[l].tolist()] for l in pooled}
+    free = {"zhat": {}, "ids": {}}  # the free-running oracle's state (drift)
+    for t in range(steps):
+        run = runs[t]
+        h0, incr, h_out, bias = run["h0"], run["incr"], run["h_out"], run["bias"]
+        H, I, W = bf16_host(run["h_tr"]), run["ids"].cpu().numpy(), run["w"].cpu().numpy()
+        DL, ZL, NX = run["delta"].cpu().numpy(), run["logits"].cpu().numpy(), run["next"].cpu().numpy()
         inc = bf16_host(incr)
-        if pool:
-            for i, l in enumerate(pooled):
-                if t > 0:
-                    staged[l].append(I[l].tolist())
-                view = pool.view(i).c()
-                dev_tab = dev_array(view.slot_of, E, torch.int16).cpu().numpy()
-                assert np.array_equal(dev_tab, pool.resident(i)), (label, t, l)
-                assert dev_array(view.ready, 1, torch.int32).cpu().numpy()[0] == t
+        if pool and t > 0:
+            for l in pooled:
+                staged[l].append(I[l].tolist())
         bias_np = bias.cpu().numpy() if bias is not None else None
         zhat_now = {}
         xs = {}
@@ -169,7 +174,7 @@ def run_lockstep(seed, sh, L, head_owners, steps, route_src=None, check_layers=N
             w_ref = OR.route_weights(zg, gi, family)
             assert np.abs(W[l] - w_ref).max() <= 1e-5, (label, t, l, W[l], w_ref)
             if headed:
-                assert np.array_equal(I[l], prev_next[l].cpu().numpy()), (label, t, l)
+                assert np.array_equal(I[l], prev_next[l]), (label, t, l)
             prev = ids_prev.get(l) if t > 0 else None
             ref = OL.layer_step(H[l], olay(l), gi, z, prev, K, family, family)
             check_protocol(DL[l], ref["delta"], f"{label} delta t{t} l{l}")
@@ -198,9 +203,8 @@ def run_lockstep(seed, sh, L, head_owners, steps, route_src=None, check_layers=N
             check_protocol(got, ref, f"{label} free-running h_out t{t}")
         zhat_prev = zhat_now
         ids_prev = {l: I[l].copy() for l in range(L)}
-        prev_next = nx_t
+        prev_next = NX
         prev_logits1 = ZL[1].copy()
-        end_prev = end
     REPORT.append(f"{label}: {decisions} routing decisions checked over {steps} steps, {ambiguous} ambiguous "
                   f"(gap <= 1e-3) adopted from the GPU")
     if pool:
