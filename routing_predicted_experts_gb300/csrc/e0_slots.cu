@@ -41,9 +41,9 @@ struct e0_slot_pool {
   uint8_t* dev = nullptr;         // [L][S][bundle]
   int16_t* d_slot_of = nullptr;   // [L][2][E]: tables for tokens of even and odd index
   uint32_t* d_ready = nullptr;    // [L] tag of the last completed staging of each layer
-  uint8_t* h_snap = nullptr;      // pinned [L][2][snap]: id -> slot table (int16 [E]), then the tag
-  size_t snap = 0;                // bytes of one snapshot
-  std::vector<cudaEvent_t> snap_done;  // [L][2]
+  int16_t* h_tab = nullptr;       // pinned [2][L][E]: table snapshots, by the tag's parity
+  uint32_t* h_tag = nullptr;      // pinned [2][L]: ready-word snapshots, by the tag's parity
+  cudaEvent_t snap_done[2] = {};  // the copies that last read each half of the snapshots
   int32_t* h_ids = nullptr;       // pinned landing buffer for committed device ids
   size_t ids_cap = 0;             // its capacity in ids
   cudaEvent_t ids_done = nullptr;
@@ -52,19 +52,15 @@ struct e0_slot_pool {
   std::vector<uint64_t> stamp;    // [L][S] last use
   std::vector<int> cur;           // [L][KMAX] experts of the previous staging (in use by the running token)
   std::vector<int> ncur;          // [L]
-  std::vector<int> flip;          // [L]
   std::vector<uint8_t> dirty;     // [L][2] the device table of that parity differs from id_slot
   uint64_t clock = 0;
   int fail_after = -1;            // tests: bundle copies left before an injected failure
-  // the copies of a staging call are spread over a few streams of the pool's own (layer l
-  // on stream l % NCS), forked from and joined back into the caller's copy stream: each
-  // copy operation has a fixed cost, and independent streams let several copy engines
-  // take them at once
-  static constexpr int NCS = 4;
-  cudaStream_t cs[NCS] = {};
-  cudaEvent_t fork_ev = nullptr;
-  cudaEvent_t join_ev[NCS] = {};
 };
+
+// Layers whose tables and ready words go out together, in one 2-D table copy and one
+// ready-word copy: each copy operation has a fixed cost of several microseconds, which
+// per layer would exceed the bundle copies themselves.
+constexpr int GROUP_LAYERS = 8;
 
 namespace {
 
@@ -82,8 +78,6 @@ void bundle_layout(const e0_dims* dm, size_t off[6], size_t* total) {
   *total = o;
 }
 
-size_t table_bytes(int E) { return ((size_t)E * sizeof(int16_t) + 15) & ~size_t(15); }
-
 }  // namespace
 
 extern "C" size_t e0_expert_bundle_bytes(const e0_dims* dims, size_t* offsets6) {
@@ -99,15 +93,11 @@ extern "C" void e0_slot_pool_destroy(e0_slot_pool* p) {
   for (cudaEvent_t e : p->snap_done)
     if (e) cudaEventSynchronize(e), cudaEventDestroy(e);
   if (p->ids_done) cudaEventDestroy(p->ids_done);
-  for (int i = 0; i < e0_slot_pool::NCS; ++i) {
-    if (p->cs[i]) cudaStreamSynchronize(p->cs[i]), cudaStreamDestroy(p->cs[i]);
-    if (p->join_ev[i]) cudaEventDestroy(p->join_ev[i]);
-  }
-  if (p->fork_ev) cudaEventDestroy(p->fork_ev);
   if (p->dev) cudaFree(p->dev);
   if (p->d_slot_of) cudaFree(p->d_slot_of);
   if (p->d_ready) cudaFree(p->d_ready);
-  if (p->h_snap) cudaFreeHost(p->h_snap);
+  if (p->h_tab) cudaFreeHost(p->h_tab);
+  if (p->h_tag) cudaFreeHost(p->h_tag);
   if (p->h_ids) cudaFreeHost(p->h_ids);
   delete p;
 }
@@ -132,7 +122,6 @@ extern "C" e0_status e0_slot_pool_create(e0_slot_pool** out, const e0_dims* dims
   p->bundle = total;
   std::memcpy(p->off, off, sizeof(off));
   p->host = static_cast<const uint8_t*>(host_bundles);
-  p->snap = table_bytes(p->E) + 16;
   auto fail = [&](cudaError_t e, const char* what) {
     e0_slot_pool_destroy(p);
     return e0::cuda_fail(e, what);
@@ -147,29 +136,21 @@ extern "C" e0_status e0_slot_pool_create(e0_slot_pool** out, const e0_dims* dims
   if (e != cudaSuccess) return fail(e, "cudaMalloc(ready)");
   e = cudaMemset(p->d_ready, 0xFF, sizeof(uint32_t) * (size_t)layers);  // no token staged yet
   if (e != cudaSuccess) return fail(e, "cudaMemset(ready)");
-  e = cudaHostAlloc(&p->h_snap, p->snap * (size_t)layers * 2, cudaHostAllocDefault);
-  if (e != cudaSuccess) return fail(e, "cudaHostAlloc(snapshots)");
-  p->snap_done.assign((size_t)layers * 2, nullptr);
+  e = cudaHostAlloc(&p->h_tab, sizeof(int16_t) * 2 * (size_t)layers * p->E, cudaHostAllocDefault);
+  if (e != cudaSuccess) return fail(e, "cudaHostAlloc(table snapshots)");
+  e = cudaHostAlloc(&p->h_tag, sizeof(uint32_t) * 2 * (size_t)layers, cudaHostAllocDefault);
+  if (e != cudaSuccess) return fail(e, "cudaHostAlloc(ready snapshots)");
   for (auto& ev : p->snap_done) {
     e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
     if (e != cudaSuccess) return fail(e, "cudaEventCreate");
   }
   e = cudaEventCreateWithFlags(&p->ids_done, cudaEventDisableTiming);
   if (e != cudaSuccess) return fail(e, "cudaEventCreate");
-  e = cudaEventCreateWithFlags(&p->fork_ev, cudaEventDisableTiming);
-  if (e != cudaSuccess) return fail(e, "cudaEventCreate");
-  for (int i = 0; i < e0_slot_pool::NCS; ++i) {
-    e = cudaStreamCreateWithFlags(&p->cs[i], cudaStreamNonBlocking);
-    if (e != cudaSuccess) return fail(e, "cudaStreamCreate");
-    e = cudaEventCreateWithFlags(&p->join_ev[i], cudaEventDisableTiming);
-    if (e != cudaSuccess) return fail(e, "cudaEventCreate");
-  }
   p->slot_id.assign((size_t)layers * slots, -1);
   p->id_slot.assign((size_t)layers * p->E, -1);
   p->stamp.assign((size_t)layers * slots, 0);
   p->cur.assign((size_t)layers * KMAX, -1);
   p->ncur.assign(layers, 0);
-  p->flip.assign(layers, 0);
   p->dirty.assign((size_t)layers * 2, 0);
   e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return fail(e, "cudaDeviceSynchronize");
@@ -209,28 +190,12 @@ extern "C" e0_status e0_debug_fail_copies(e0_slot_pool* p, int32_t n) {
 
 namespace {
 
-// The pool's streams start after everything queued on st so far.
-e0_status fork(e0_slot_pool* p, cudaStream_t st) {
-  E0_CHECK_CUDA(cudaEventRecord(p->fork_ev, st));
-  for (int i = 0; i < e0_slot_pool::NCS; ++i) E0_CHECK_CUDA(cudaStreamWaitEvent(p->cs[i], p->fork_ev, 0));
-  return E0_OK;
-}
-// st continues after everything queued on the pool's streams.
-e0_status join(e0_slot_pool* p, cudaStream_t st) {
-  for (int i = 0; i < e0_slot_pool::NCS; ++i) {
-    E0_CHECK_CUDA(cudaEventRecord(p->join_ev[i], p->cs[i]));
-    E0_CHECK_CUDA(cudaStreamWaitEvent(st, p->join_ev[i], 0));
-  }
-  return E0_OK;
-}
-
-// Make ids[0..K) resident in pool layer `layer` and write `tag` into its ready word,
-// all queued on one of the pool's streams (layer % NCS).  Bookkeeping changes only for
-// copies that were queued.
-e0_status stage_layer(e0_slot_pool* p, int32_t layer, const int32_t* ids, int32_t K, uint32_t tag,
-                      e0_stage_stats* stats) {
+// Make ids[0..K) resident in pool layer `layer`: the LRU picks the slots, one copy per
+// missing bundle is queued on st.  The bookkeeping changes only for copies that were
+// queued; the layer's tables are marked as differing from the record.
+e0_status stage_bundles(e0_slot_pool* p, int32_t layer, const int32_t* ids, int32_t K, cudaStream_t st,
+                        e0_stage_stats* stats) {
   E0_REQUIRE(layer >= 0 && layer < p->L, E0_ERR_INVALID, "e0_stage_slots: layer out of range");
-  const cudaStream_t st = p->cs[layer % e0_slot_pool::NCS];
   const int E = p->E, S = p->S;
   for (int k = 0; k < K; ++k)
     E0_REQUIRE(ids[k] >= 0 && ids[k] < E, E0_ERR_INVALID,
@@ -308,29 +273,59 @@ e0_status stage_layer(e0_slot_pool* p, int32_t layer, const int32_t* ids, int32_
     stats->h2d_bytes += s.h2d_bytes;
   }
   if (result != E0_OK) return result;
-  // the id -> slot table of the tag's parity (while it differs from the device's) and the
-  // ready word, from one of two pinned snapshots per layer (the one whose previous copies
-  // have finished); the other parity's table stays as the running token reads it
-  const int half = (int)(tag & 1u);
-  const int f = p->flip[layer];
-  cudaEvent_t ev = p->snap_done[(size_t)layer * 2 + f];
-  E0_CHECK_CUDA(cudaEventSynchronize(ev));
-  uint8_t* snap = p->h_snap + ((size_t)layer * 2 + f) * p->snap;
-  int16_t* table = reinterpret_cast<int16_t*>(snap);
-  uint32_t* tg = reinterpret_cast<uint32_t*>(snap + table_bytes(E));
-  if (p->dirty[(size_t)layer * 2 + half]) {
-    for (int e = 0; e < E; ++e) table[e] = (int16_t)id_slot[e];
-    E0_CHECK_CUDA(cudaMemcpyAsync(p->d_slot_of + ((size_t)layer * 2 + half) * E, table, sizeof(int16_t) * E,
-                                  cudaMemcpyHostToDevice, st));
-    p->dirty[(size_t)layer * 2 + half] = 0;
-  }
-  *tg = tag;
-  E0_CHECK_CUDA(cudaMemcpyAsync(p->d_ready + layer, tg, sizeof(uint32_t), cudaMemcpyHostToDevice, st));
-  E0_CHECK_CUDA(cudaEventRecord(ev, st));
-  p->flip[layer] = f ^ 1;
   int* cw = &p->cur[(size_t)layer * KMAX];
   for (int k = 0; k < K; ++k) cw[k] = ids[k];
   p->ncur[layer] = K;
+  return E0_OK;
+}
+
+// Queue, after the bundles of pool layers [l0, l1), their tables of the tag's parity
+// (one 2-D copy, when any differs from the record) and then `tag` into their ready words
+// (one copy), from the tag's half of the pinned snapshots.
+e0_status flush_group(e0_slot_pool* p, int l0, int l1, uint32_t tag, cudaStream_t st) {
+  if (l1 <= l0) return E0_OK;
+  const int E = p->E, half = (int)(tag & 1u);
+  bool any = false;
+  for (int l = l0; l < l1; ++l) any = any || p->dirty[(size_t)l * 2 + half];
+  if (any) {
+    int16_t* snap = p->h_tab + ((size_t)half * p->L + l0) * E;
+    for (int l = l0; l < l1; ++l)
+      for (int e = 0; e < E; ++e) snap[(size_t)(l - l0) * E + e] = (int16_t)p->id_slot[(size_t)l * E + e];
+    E0_CHECK_CUDA(cudaMemcpy2DAsync(p->d_slot_of + ((size_t)l0 * 2 + half) * E, sizeof(int16_t) * 2 * E, snap,
+                                    sizeof(int16_t) * E, sizeof(int16_t) * E, l1 - l0, cudaMemcpyHostToDevice, st));
+    for (int l = l0; l < l1; ++l) p->dirty[(size_t)l * 2 + half] = 0;
+  }
+  uint32_t* tg = p->h_tag + (size_t)half * p->L;
+  for (int l = l0; l < l1; ++l) tg[l] = tag;
+  E0_CHECK_CUDA(cudaMemcpyAsync(p->d_ready + l0, tg + l0, sizeof(uint32_t) * (l1 - l0), cudaMemcpyHostToDevice, st));
+  return E0_OK;
+}
+
+// One staging call: the layers in order, their small copies grouped over runs of
+// consecutive pool layers (at most GROUP_LAYERS).  ids_of(i) returns pool layer
+// layers[i]'s ids (or nullptr with an error status set); the tag's snapshot half is
+// free once the call two tags back has been copied out.
+template <class IdsOf>
+e0_status stage_call(e0_slot_pool* p, const int32_t* layers, int32_t n, int32_t K, uint32_t tag, cudaStream_t st,
+                     e0_stage_stats* stats, IdsOf ids_of) {
+  for (int i = 0; i < n; ++i)
+    E0_REQUIRE(layers[i] >= 0 && layers[i] < p->L, E0_ERR_INVALID, "e0_stage_slots: layer out of range");
+  E0_CHECK_CUDA(cudaEventSynchronize(p->snap_done[tag & 1u]));
+  int g0 = 0;  // first index of the current group
+  for (int i = 0; i < n; ++i) {
+    e0_status err = E0_OK;
+    const int32_t* ids = ids_of(i, err);
+    if (err != E0_OK) return err;
+    e0_status s = stage_bundles(p, layers[i], ids, K, st, stats);
+    if (s != E0_OK) return s;
+    const bool last = i + 1 == n || layers[i + 1] != layers[i] + 1 || i + 1 - g0 == GROUP_LAYERS;
+    if (last) {
+      s = flush_group(p, layers[g0], layers[i] + 1, tag, st);
+      if (s != E0_OK) return s;
+      g0 = i + 1;
+    }
+  }
+  E0_CHECK_CUDA(cudaEventRecord(p->snap_done[tag & 1u], st));
   return E0_OK;
 }
 
@@ -343,10 +338,8 @@ extern "C" e0_status e0_stage_slots_host(e0_slot_pool* p, const int32_t* layers,
   E0_REQUIRE(K >= 1 && K <= KMAX && 2 * K <= p->S, E0_ERR_SHAPE, "e0_stage_slots_host: K out of range");
   const cudaStream_t st = (cudaStream_t)copy_stream;
   if (after) E0_CHECK_CUDA(cudaStreamWaitEvent(st, (cudaEvent_t)after, 0));
-  e0_status s = fork(p, st);
-  for (int i = 0; i < n_layers && s == E0_OK; ++i) s = stage_layer(p, layers[i], ids + (size_t)i * K, K, tag, stats);
-  const e0_status j = join(p, st);
-  return s != E0_OK ? s : j;
+  return stage_call(p, layers, n_layers, K, tag, st, stats,
+                    [&](int i, e0_status&) { return ids + (size_t)i * K; });
 }
 
 extern "C" e0_status e0_stage_slots(e0_slot_pool* p, const int32_t* layers, int32_t n_layers, const int32_t* next_ids,
@@ -374,11 +367,8 @@ extern "C" e0_status e0_stage_slots(e0_slot_pool* p, const int32_t* layers, int3
   E0_CHECK_CUDA(cudaMemcpyAsync(p->h_ids, next_ids, need * sizeof(int32_t), cudaMemcpyDeviceToHost, st));
   E0_CHECK_CUDA(cudaEventRecord(p->ids_done, st));
   E0_CHECK_CUDA(cudaEventSynchronize(p->ids_done));
-  e0_status s = fork(p, st);
-  for (int i = 0; i < n_layers && s == E0_OK; ++i)
-    s = stage_layer(p, layers[i], p->h_ids + (size_t)rows[i] * K, K, tag, stats);
-  const e0_status j = join(p, st);
-  return s != E0_OK ? s : j;
+  return stage_call(p, layers, n_layers, K, tag, st, stats,
+                    [&](int i, e0_status&) { return p->h_ids + (size_t)rows[i] * K; });
 }
 
 // ------------------------------------------------------------------ commit box
@@ -422,24 +412,20 @@ extern "C" e0_status e0_stage_slots_committed(e0_slot_pool* p, const e0_commit_b
     E0_REQUIRE(rows[i] >= 0 && rows[i] < box->L, E0_ERR_INVALID, "e0_stage_slots_committed: row out of range");
   const cudaStream_t st = (cudaStream_t)copy_stream;
   const auto t0 = std::chrono::steady_clock::now();
-  e0_status s = fork(p, st);
-  for (int i = 0; i < n_layers && s == E0_OK; ++i) {
+  int32_t ids[KMAX];
+  return stage_call(p, layers, n_layers, K, tag, st, stats, [&](int i, e0_status& err) -> const int32_t* {
     const volatile uint32_t* row = box->host + ((size_t)(tag & 1u) * box->L + rows[i]) * (KMAX + 1);
     // the launch writes the ids, then (after a system-scope fence) the tag
     for (uint32_t it = 0; row[0] != tag; ++it) {
       if ((it & 255u) == 0 &&
           (uint64_t)std::chrono::duration_cast<std::chrono::nanoseconds>(std::chrono::steady_clock::now() - t0)
-                  .count() > timeout_ns)
-      {
-        join(p, st);
-        return e0::fail(E0_ERR_TIMEOUT, "e0_stage_slots_committed: the launch did not commit this layer in time");
+                  .count() > timeout_ns) {
+        err = e0::fail(E0_ERR_TIMEOUT, "e0_stage_slots_committed: the launch did not commit this layer in time");
+        return nullptr;
       }
     }
     std::atomic_thread_fence(std::memory_order_acquire);
-    int32_t ids[KMAX];
     for (int k = 0; k < K; ++k) ids[k] = (int32_t)row[1 + k];
-    s = stage_layer(p, layers[i], ids, K, tag, stats);
-  }
-  const e0_status j = join(p, st);
-  return s != E0_OK ? s : j;
+    return ids;
+  });
 }
