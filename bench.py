@@ -467,6 +467,154 @@ def run_slots(args, local_rank: int = 0):
     }
 
 
+ROUTE_AHEAD_METRIC = ("decode tok/s with training-free route-ahead routing (40-layer int4 MoE stack, K=4) and "
+                      "the committed selection's agreement with each layer's own gate")
+
+
+def run_route_ahead(args, local_rank: int = 0):
+    """The 40-layer stack with route-ahead N (no heads): layer l >= N ranks its own gate on
+    the input of layer l - N at the same token, so every layer's experts are known N
+    layers early; layers 0..N-1 route with their own gate.  Reports tok/s and the share of
+    committed slots that the layer's own gate on its own input would also pick (the size
+    of the perturbation, as the route-ahead notes report it)."""
+    import numpy as np
+    import torch
+    from routing_predicted_experts_gb300 import binding as B, model as M, synth as S
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    N, L = args.ahead, S.STACK_LAYERS
+    sh = S.LAYER35B(args.k)
+    t_build = time.time()
+    layers = [M.build_layer(SEED, l, sh, with_head=False, device=dev) for l in range(L)]
+    structs = [B.e0_layer_struct(ly["routed"], ly["shared"], ly["lora"], None, ly["router"]) for ly in layers]
+    src = [0 if l < N else -N for l in range(L)]
+    dm = B.dims(sh.d, sh.E, sh.F, sh.K)
+    stack = B.Stack(dm, structs, src, keepalive=layers)
+    build_s = time.time() - t_build
+    n_steps = args.warmup + args.steps
+    h0 = torch.empty((n_steps, sh.d), dtype=torch.int16, device=dev)
+    incr = torch.empty((n_steps, L, sh.d), dtype=torch.int16, device=dev)
+    B.e0_synth_normal(h0, SEED, S.stream_id("bench.h0"), 0, 1.0)
+    B.e0_synth_normal(incr, SEED, S.stream_id("bench.incr"), 0, 1.0)
+    h_out = torch.empty((n_steps, sh.d), dtype=torch.int16, device=dev)
+    ws = stack.workspace(dev)
+    stream = torch.cuda.current_stream()
+    for t in range(args.warmup):
+        stack.step(t, h0[t], incr[t], h_out[t], ws)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for t in range(args.warmup, n_steps):
+        stack.step(t, h0[t], incr[t], h_out[t], ws)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sampler.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    assert B.e0_get_device_status(ws) == 0
+    # agreement: a sample of tokens, each layer's own gate on its own input (the GPU's
+    # plain linear router: a head with only its linear residual) against the committed ids
+    n_agree = n_slots = 0
+    d_out = torch.empty((L, sh.K), dtype=torch.int32, device=dev)
+    h_tr = torch.empty((L, sh.d), dtype=torch.int16, device=dev)
+    ws1 = B.e0_workspace(dm, device=dev)
+    for t in range(min(32, n_steps)):
+        stack.step(n_steps + t, h0[t], incr[t], h_out[t], ws, ids_out=d_out, h_trace=h_tr)
+        own = []
+        for l in range(N, L):
+            gate = B.Prerouter(0, None, None, None, None, None, None, layers[l]["router"])
+            _, ids, _ = B.e0_prerouter_forward(gate, sh.d, sh.E, sh.K, h_tr[l:l + 1], None, None, ws1)
+            own.append(ids[0])
+        own = torch.stack(own).cpu().numpy()
+        com = d_out[N:].cpu().numpy()
+        for a, b in zip(com, own):
+            n_agree += len(set(a.tolist()) & set(b.tolist()))
+            n_slots += sh.K
+    torch.cuda.synchronize()
+    assert B.e0_get_device_status(ws) == 0 and B.e0_get_device_status(ws1) == 0
+    bpt = algorithmic_bytes_per_token(K=args.k, L=L, heads=0, routers=L)
+    peak, peak_kind = _peaks()
+    stack.close()
+    return {
+        "metric": ROUTE_AHEAD_METRIC if args.k == 4 else ROUTE_AHEAD_METRIC.replace("K=4", f"K={args.k}"),
+        "value": round(1e3 / ms, 1), "unit": "tok/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int4 weights x int16-quantised activations -> fp32 accumulate; bf16 in/out",
+        "data": "synthetic (seeded N(0,0.02) weights packed int4 g64; N(0,1) hidden states and per-layer increments)",
+        "config": {"workload": f"40-layer int4 MoE decode stack, 35B-A3B-class layers without heads, route-ahead "
+                               f"N={N}: layers {N}..39 rank their own gate on the input {N} layers earlier",
+                   "l2": "inputs larger than L2", "parallelism": "1 GPU", "bytes_per_token": bpt,
+                   "build_s": round(build_s, 1)},
+        "route_ahead": {"N": N, "agreement_with_own_gate": round(n_agree / max(1, n_slots), 4),
+                        "slots_compared": n_slots},
+        "roofline": {"bound": "hbm", "achieved": round(bpt / (ms / 1e3) / 1e9, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(bpt / (ms / 1e3) / 1e9 / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
+                     "traffic": None},
+        "e2e": None, "gpu_launches": args.steps, "clocks": sampler.summary(0, 0),
+    }
+
+
+MULTI_METRIC = "decode tok/s of one 35B-A3B-class layer-step with T tokens per call (K=4, head, shared, LoRA)"
+
+
+def run_multitoken(args, local_rank: int = 0):
+    """One layer-step for T = 1, 2, 4, 8, 16 tokens per call: each weight is read once per
+    call, so the bytes per token fall with T."""
+    import numpy as np
+    import torch
+    from routing_predicted_experts_gb300 import binding as B, model as M, synth as S
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    sh = S.LAYER35B(args.k)
+    lay = M.build_layer(SEED, 0, sh, device=dev)
+    dm = B.dims(sh.d, sh.E, sh.F, sh.K)
+    q4 = lambda rows, cols: rows * cols // 2 + rows * (cols // 64) * 4
+    expert = q4(2 * sh.F, sh.d) + q4(sh.d, sh.F)
+    lora = q4(sh.d, sh.d) + 2 * 2 * sh.r * sh.d
+    head = 2 * sh.H * sh.d + 2 * sh.H + 2 * sh.E * sh.H + 2 * sh.E + 2 * sh.E * sh.d
+    rows = []
+    for T in (1, 2, 4, 8, 16):
+        H = torch.empty((T, sh.d), dtype=torch.int16, device=dev)
+        B.e0_synth_normal(H, SEED, S.stream_id(f"bench.mt.h{T}"), 0, 1.0)
+        Z = torch.empty((T, sh.E), dtype=torch.float32, device=dev)
+        B.e0_synth_normal(Z, SEED, S.stream_id(f"bench.mt.z{T}"), 0, 1.0)
+        ids = torch.topk(Z, sh.K, dim=1).indices.to(torch.int32).contiguous()
+        prev = torch.roll(ids, 1, 0).contiguous()
+        ws = B.e0_decode_workspace(dm, T, lay["lora"].out, sh.H, device=dev)
+        run = lambda: B.e0_moe_decode_layer(dm, lay["routed"], lay["shared"], lay["lora"], lay["head"], H, ids, Z,
+                                            prev, ws, want_delta=False)
+        for _ in range(args.warmup):
+            run()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n = 200
+        e0.record()
+        for _ in range(n):
+            run()
+        e1.record()
+        torch.cuda.synchronize()
+        assert B.e0_get_device_status(ws) == 0
+        us = e0.elapsed_time(e1) / n * 1e3
+        distinct = len(set(ids.cpu().numpy().ravel().tolist()))
+        nbytes = distinct * expert + expert + lora + head + 2 * 2 * sh.H * distinct
+        rows.append({"T": T, "us_per_call": round(us, 2), "tok_s": round(T / (us / 1e6), 1),
+                     "distinct_experts": distinct, "weight_mb_per_token": round(nbytes / T / 1e6, 3),
+                     "hbm_gbs": round(nbytes / (us / 1e6) / 1e9, 1)})
+    best = max(rows, key=lambda r: r["tok_s"])
+    return {
+        "metric": MULTI_METRIC, "value": best["tok_s"], "unit": "tok/s", "n_gpus": 1, "steps": 200,
+        "warmup": args.warmup, "ms_per_step": round(best["us_per_call"] / 1e3, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "T=1: int4 x int16 -> fp32; T>1: int4 dequantised to fp16 on tensor cores, fp32 accumulate",
+        "data": "synthetic (seeded weights, N(0,1) hidden states and logits)",
+        "config": {"workload": "one 35B-A3B-class layer-step (d=2048, E=256, F=512, K=4, head H=1024, shared, "
+                               "LoRA r=16), T tokens per call", "l2": "weights 30 MB per call (< L2: warm-cache)",
+                   "parallelism": "1 GPU"},
+        "per_T": rows, "e2e": None, "gpu_launches": None,
+    }
+
+
 def run_ours(args, rank: int, world: int, local_rank: int):
     import torch
     from routing_predicted_experts_gb300 import binding as B, synth as S
@@ -728,9 +876,11 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--oracle-worker", action="store_true")
     ap.add_argument("--trace", default=None, help="write per-CTA per-layer timer stamps of 4 extra steps (.npy)")
-    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "slots"],
+    ap.add_argument("--ahead", type=int, default=2, help="route-ahead depth N (workload route-ahead)")
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "slots", "route-ahead", "multitoken"],
                     help="decode: the 40-layer stack (the headline); prefill: a T=512 chunk through one layer; "
-                         "slots: the stack with host-resident experts and a bounded HBM slot pool")
+                         "slots: the stack with host-resident experts and a bounded HBM slot pool; route-ahead: "
+                         "the stack routed by route-ahead N (--ahead); multitoken: one layer-step, T = 1..16")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -754,9 +904,10 @@ def main():
 
     if args.workload == "slots" and args.steps > 512:
         args.steps = 512  # the slot-pool workload is 512 decode steps
-    if args.workload in ("prefill", "slots"):
+    if args.workload in ("prefill", "slots", "route-ahead", "multitoken"):
         if rank == 0:
-            run = run_prefill if args.workload == "prefill" else run_slots
+            run = {"prefill": run_prefill, "slots": run_slots, "route-ahead": run_route_ahead,
+                   "multitoken": run_multitoken}[args.workload]
             print(json.dumps(run(args, local_rank)))
         return
 

@@ -17,7 +17,7 @@ struct Ctl {
   float res[DMAX];            // residual h of the layer, fp32 (exact bf16 values); x = res * xscale
   uint4 xq[4][DMAX / 32];     // x as int16: xq[t][c] = group t (of 4) of chunk c, stored [0,2,4,6,1,3,5,7]
                               // (group-major, so that lanes reading consecutive chunks hit distinct banks)
-  float xinv[DMAX / 32];      // per 32-element chunk: dequant step of xq (one step for all of x)
+  float xinv[DMAX / 32];      // per 32-element chunk: dequant step of xq (max |x| of the chunk / 32767)
   float xsum[DMAX / 32];      // per 32-element chunk: sum of the dequantised chunk
   float abuf[2][64];          // gate/up row values of the last two expert slabs (rows 2j, 2j + 1 = gate, up of j)
   uint4 aqw[NCW][4];          // per warp: the activations quantised to int16 in the dot32 order
@@ -35,7 +35,6 @@ struct Ctl {
   uint32_t rt_pvalid[LMAX];
   volatile int32_t rt_ready[LMAX];
   float red[NCW];
-  uint32_t redm[NCW];
   float xscale;               // RMSNorm factor of the current layer input
   volatile int32_t abort_flag;
   int32_t is_last;
@@ -1393,11 +1392,11 @@ __device__ __forceinline__ void consume_unit(Cons& cs, const LayerDesc& Ld, cons
 }
 
 // Build the layer input: residual h (fp32 of bf16 values), the RMSNorm factor, and
-// the int16 copy of x = h * factor used by the int4 rows.  One quantisation step,
-// max|x| / 32767, serves the whole vector, so the only block-wide reduction is the
-// one that the norm needs anyway (sum of squares and max |h| together).  Thread t
+// the int16 copy of x = h * factor used by the int4 rows, with one quantisation step
+// per 32-element chunk (max |x| of the chunk / 32767), so the only block-wide
+// reduction is the one that the norm needs anyway (the sum of squares).  Thread t
 // owns elements t + NCT*k: warp w owns the whole 32-element chunks w + NCW*k, whose
-// sums come from one integer warp reduction.  inc[] holds this thread's residual
+// maxima and sums come from warp reductions.  inc[] holds this thread's residual
 // increments, loaded before the dependency wait.
 template <int D>
 __device__ __forceinline__ void layer_input(Cons& cs, int l, uint32_t par, const float* inc) {
@@ -1406,7 +1405,7 @@ __device__ __forceinline__ void layer_input(Cons& cs, int l, uint32_t par, const
   const int tid = cs.tid;
   constexpr int PER = (D + NCT - 1) / NCT;
   float h[PER];
-  float ss = 0.f, mx = 0.f;
+  float ss = 0.f;
   const float* accp = (P.mode == MODE_STACK && l > 0) ? acc_ptr(P, par, l - 1) : nullptr;
   float a[PER];
 #pragma unroll
@@ -1429,34 +1428,32 @@ __device__ __forceinline__ void layer_input(Cons& cs, int l, uint32_t par, const
       h[k] = v;
       C.res[i] = v;
       ss += v * v;
-      mx = fmaxf(mx, fabsf(v));
     }
   }
   ss = warp_sum(ss);
-  const uint32_t mb = __reduce_max_sync(0xffffffffu, __float_as_uint(mx));
-  if (cs.lane == 0) {
-    C.red[cs.cw] = ss;
-    C.redm[cs.cw] = mb;
-  }
+  if (cs.lane == 0) C.red[cs.cw] = ss;
+  // the largest |h| of each 32-element chunk (a warp owns whole chunks)
+  uint32_t cm[PER];
+#pragma unroll
+  for (int k = 0; k < PER; ++k)
+    cm[k] = (tid - cs.lane) + NCT * k < D ? __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h[k]))) : 0u;
   cbar();
   float tot = 0.f;
-  uint32_t mxb = 0u;
 #pragma unroll
-  for (int w = 0; w < NCW; ++w) {
-    tot += C.red[w];
-    mxb = max(mxb, C.redm[w]);
-  }
-  // (the quantisation step needs no correctly rounded division: any step near
-  // max|x| / 32767 works, the codes are clamped and each is scaled back by the same inv)
+  for (int w = 0; w < NCW; ++w) tot += C.red[w];
   const float scale = P.norm ? rsqrtf(tot * (1.0f / (float)D) + RMS_EPS) : 1.0f;
-  const float xmax = __uint_as_float(mxb) * scale;
-  const float r = xmax > 0.f ? __fdividef(32767.0f, xmax) : 0.f;
-  const float inv = xmax * (1.0f / 32767.0f);
   int16_t* xq16 = reinterpret_cast<int16_t*>(C.xq);
-  // independent chunks: codes first, then their stores and sums, so the steps overlap
+  // one quantisation step per 32-element chunk, max|x of the chunk| / 32767, so that an
+  // outlier costs resolution only within its own chunk.  (The step needs no correctly
+  // rounded division: the codes are clamped and scaled back by the same inv.)
+  // Independent chunks: codes first, then their stores and sums, so the steps overlap.
   int q[PER], sq[PER];
+  float inv[PER];
 #pragma unroll
   for (int k = 0; k < PER; ++k) {
+    const float xmax = __uint_as_float(cm[k]) * scale;
+    const float r = xmax > 0.f ? __fdividef(32767.0f, xmax) : 0.f;
+    inv[k] = xmax * (1.0f / 32767.0f);
     const int v = __float2int_rn(h[k] * scale * r);
     q[k] = v > 32767 ? 32767 : (v < -32767 ? -32767 : v);
   }
@@ -1476,8 +1473,8 @@ __device__ __forceinline__ void layer_input(Cons& cs, int l, uint32_t par, const
     const int i = tid + NCT * k;
     if (i < D) {
       if (cs.lane == 0) {
-        C.xinv[i >> 5] = inv;
-        C.xsum[i >> 5] = (float)sq[k] * inv;
+        C.xinv[i >> 5] = inv[k];
+        C.xsum[i >> 5] = (float)sq[k] * inv[k];
       }
       if (P.mode == MODE_STACK && P.h_trace && blockIdx.x == 0)
         P.h_trace[(size_t)l * D + i] = f32_to_bf16_bits(h[k]);

@@ -189,3 +189,31 @@ def test_layer_step_sigmoid_group_routing():
     w = out["next_weights"][0].cpu().numpy()
     assert np.abs(w - OR.route_weights(zg, gi, fam)).max() <= 1e-5
     assert abs(w.sum() - 2.5 * OR.sigmoid(zg[gi]).sum() / (OR.sigmoid(zg[gi]).sum() + 1e-20)) <= 1e-5
+
+
+@pytest.mark.parametrize("factor", [100.0, 1000.0])
+def test_layer_step_with_an_activation_outlier(factor):
+    """One hidden element at 100x / 1000x the rms of the rest (real models carry such
+    outliers): x is quantised to int16 with one step per 32-element chunk, so the
+    outlier costs resolution only within its own chunk and the layer stays at the bar."""
+    import torch
+    from routing_predicted_experts_gb300 import binding as B, model as M
+    sh, seed = S.LAYER35B(4), 0
+    lay = M.build_layer(seed, 0, sh)
+    h, zc, ids, ids_prev = _inputs(seed, sh)
+    h = h.copy()
+    h[777] = OB.f64_to_bf16(np.array([factor]))[0]
+    h[1500] = OB.f64_to_bf16(np.array([-factor / 3]))[0]
+    dm = B.dims(sh.d, sh.E, sh.F, sh.K)
+    ws = B.e0_workspace(dm)
+    out = B.e0_moe_decode_layer(dm, lay["routed"], lay["shared"], lay["lora"], lay["head"], bf16_dev(h)[None],
+                                to_dev(ids, torch.int32)[None], to_dev(zc, torch.float32)[None],
+                                to_dev(ids_prev, torch.int32)[None], ws)
+    torch.cuda.synchronize()
+    assert B.e0_get_device_status(ws) == 0
+    ref = OL.layer_step(h, OM.layer(seed, 0, sh), ids, zc, ids_prev, sh.K)
+    mx, mn = check_protocol(out["delta"][0].cpu().numpy(), ref["delta"], f"delta, outlier x{factor:g}")
+    check_protocol(out["next_logits"][0].cpu().numpy(), ref["next_logits"], f"next_logits, outlier x{factor:g}")
+    from _common import REPORT
+    REPORT.append(f"35B layer with a {factor:g}x activation outlier: delta max|err|/max|ref| {mx:.2e}, "
+                  f"mean|err|/mean|ref| {mn:.2e}")
