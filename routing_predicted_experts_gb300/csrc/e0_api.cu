@@ -237,7 +237,13 @@ e0_status build_plan(const PlanSpec& s, int ncta, Unit* units, uint8_t* counts, 
   //    next token) on the rest
   const int qstage = q4_rows_per_stage(d);
   const bool has_def = s.lres || s.head;
-  const int n_q = s.lora ? (s.lout + 4 * qstage - 1) / (4 * qstage) : 0;
+  // LoRA base rows per CTA in the split plan: whole stages, about as many bytes as an
+  // expert slab, so that those CTAs finish with the expert CTAs and as many CTAs as
+  // possible are left to the prerouter (whose CTAs must keep pace with the layers: the
+  // launch ends only when the last head is done)
+  const int slab_bytes = 64 * q4_row_bytes(d) + 20 * d;
+  const int q_rows = std::max(4 * qstage, slab_bytes / q4_row_bytes(d) / qstage * qstage);
+  const int n_q = s.lora ? (s.lout + q_rows - 1) / q_rows : 0;
   // B slices of one stage each: rows in multiples of 16 with lr * rows * 2 <= STAGE_BYTES
   const int b_rows = s.lora_ab && s.lr > 0 ? std::max(16, (STAGE_BYTES / (2 * s.lr)) / 16 * 16) : 0;
   const int n_ab = s.lora_ab && s.lr > 0 ? std::max(1, (s.lout + b_rows - 1) / b_rows) : 0;
@@ -274,8 +280,10 @@ e0_status build_plan(const PlanSpec& s, int ncta, Unit* units, uint8_t* counts, 
       L.push_back(Unit{U_LORA_A, 0, 0, (uint16_t)s.lr, UF_LOCAL_V});
       L.push_back(Unit{U_LORA_B, 0, (uint16_t)r0, (uint16_t)r1, 0});
     }
+    const int q_st = (s.lout + qstage - 1) / qstage;  // stages of LoRA base rows, spread evenly
     for (int i = 0; i < n_q; ++i) {
-      const int r0 = i * 4 * qstage, r1 = std::min(s.lout, r0 + 4 * qstage);
+      const int r0 = (int)((long long)q_st * i / n_q) * qstage;
+      const int r1 = std::min(s.lout, (int)((long long)q_st * (i + 1) / n_q) * qstage);
       lists[n_slabs + n_ab + i].push_back(Unit{U_QROWS, 0, (uint16_t)r0, (uint16_t)r1, 0});
     }
     // the prerouter's rows in contiguous runs, LRES on the first CTAs of the pool and

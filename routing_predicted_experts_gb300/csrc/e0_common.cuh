@@ -119,6 +119,12 @@ __device__ __forceinline__ void tma_bulk_g2s(void* dst, const void* src, uint32_
       : "memory");
 }
 
+// Bulk prefetch of global memory into L2 (no completion to wait for); src 16-byte
+// aligned, bytes a positive multiple of 16.
+__device__ __forceinline__ void l2_prefetch(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Order this thread's earlier generic-proxy accesses to shared memory before later
 // async-proxy (bulk copy) accesses.
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -43,6 +43,7 @@ struct Ctl {
   uint8_t defer[KINDS_MAX];   // per plan kind: this CTA holds only prerouter work
   int32_t sn[KINDS_MAX];
   uint32_t rt_tag[LMAX];      // staged: epoch each committed route is for
+  uint64_t ttype[8];          // diagnostics (tid 0): time per unit type in the current layer
   int32_t lv_layer;           // layer whose LoRA v (all ranks) this CTA computed into lvs, else -1
 };
 
@@ -755,10 +756,78 @@ __device__ __forceinline__ void issue_unit(Prod& pr, const LayerDesc& Ld, const 
   }
 }
 
+// L2 prefetch of the weight rows of one of this CTA's units (addresses as issue_unit
+// computes them); the routed expert slabs only once their layer's route is published.
+// Lanes take the contiguous ranges round robin.
+__device__ __forceinline__ void prefetch_unit(Prod& pr, const LayerDesc& Ld, const Unit& u, int l) {
+  const EngineParams& P = pr.P;
+  Ctl& C = pr.C;
+  const int d = P.d;
+  int n = 0;  // ranges seen so far: lane n issues range n
+  auto add = [&](const void* p, size_t b) {
+    if (p && b >= 16) {
+      if (pr.lane == n) l2_prefetch(p, (uint32_t)(b & ~size_t(15)));
+      ++n;
+    }
+  };
+  switch (u.type) {
+    case U_EXPERT: {
+      const bool shared = u.k >= P.K;
+      if (shared ? !Ld.has_shared : (!C.rt_ready[l] || !((C.rt_valid[l] >> u.k) & 1u))) return;
+      const int idx = shared ? 0 : C.rt_idx[l][u.k];
+      const int64_t xs = shared ? 0 : Ld.ex_stride;
+      auto at = [&](const auto* base, size_t dense_elems) {
+        return xs ? reinterpret_cast<decltype(base)>(reinterpret_cast<const uint8_t*>(base) + (size_t)idx * xs)
+                  : base + (size_t)idx * dense_elems;
+      };
+      const uint32_t* guq = at(shared ? Ld.sgu_q : Ld.gu_q, (size_t)(2 * P.F) * (d / 8));
+      const uint16_t* gus = at(shared ? Ld.sgu_s : Ld.gu_s, (size_t)(2 * P.F) * (d / 64));
+      const uint16_t* gub = at(shared ? Ld.sgu_b : Ld.gu_b, (size_t)(2 * P.F) * (d / 64));
+      const size_t r0 = 64 * (size_t)u.r0;
+      add(guq + r0 * (d / 8), (size_t)64 * d / 2);
+      add(gus + r0 * (d / 64), (size_t)64 * (d / 64) * 2);
+      add(gub + r0 * (d / 64), (size_t)64 * (d / 64) * 2);
+      add(at(shared ? Ld.sdn_q : Ld.dn_q, (size_t)(P.F / 32) * d * 4) + (size_t)u.r0 * d * 4, (size_t)d * 16);
+      add(at(shared ? Ld.sdn_s : Ld.dn_s, (size_t)(P.F / 64) * d) + (size_t)(u.r0 >> 1) * d, (size_t)d * 2);
+      add(at(shared ? Ld.sdn_b : Ld.dn_b, (size_t)(P.F / 64) * d) + (size_t)(u.r0 >> 1) * d, (size_t)d * 2);
+      break;
+    }
+    case U_QROWS:
+      add(Ld.lw_q + (size_t)u.r0 * (d / 8), (size_t)(u.r1 - u.r0) * d / 2);
+      add(Ld.lw_s + (size_t)u.r0 * (d / 64), (size_t)(u.r1 - u.r0) * (d / 64) * 2);
+      add(Ld.lw_b + (size_t)u.r0 * (d / 64), (size_t)(u.r1 - u.r0) * (d / 64) * 2);
+      break;
+    case U_LORA_A:
+      add(Ld.la + (size_t)u.r0 * d, (size_t)(u.r1 - u.r0) * d * 2);
+      break;
+    case U_HEAD:
+      add(Ld.w1h + (size_t)u.r0 * d, (size_t)(u.r1 - u.r0) * d * 2);
+      add(Ld.w2t + (size_t)u.r0 * P.E, (size_t)(u.r1 - u.r0) * P.E * 2);
+      break;
+    case U_LRES:
+      add(Ld.lres + (size_t)u.r0 * d, (size_t)(u.r1 - u.r0) * d * 2);
+      break;
+    default:
+      break;
+  }
+}
+
+// L2 prefetch of layer l's units of this CTA (issued one layer ahead of the stage ring,
+// so that DRAM keeps streaming through the grid-wide waits between layers).
+__device__ __forceinline__ void prefetch_layer(Prod& pr, int l) {
+  const EngineParams& P = pr.P;
+  if (l >= P.L || !pr.ok) return;
+  const LayerDesc& Ld = layer_at(P, l);
+  int nu;
+  const Unit* us = units_of(P, P.plan ? Ld.plan_kind : 0, blockIdx.x, nu);
+  for (int i = 0; i < nu; ++i) prefetch_unit(pr, Ld, us[i], l);
+}
+
 __device__ void producer(const EngineParams& P, Ctl& C, uint8_t* ring) {
   Prod pr{P, C, ring, 0u, true, (int)(threadIdx.x & 31), C.epoch & 1u, C.epoch % 3u, C.epoch};
   for (int l = 0; l < P.L && pr.ok; ++l) {
     const LayerDesc& Ld = layer_at(P, l);
+    prefetch_layer(pr, l + 1);
     // gate rows on this layer's input: its own gate, then the gate of the layer that
     // routes ahead from here
     const uint16_t* gates[2] = {gate_here(P, l) ? Ld.router : nullptr,
@@ -1541,16 +1610,22 @@ __device__ void consumer(const EngineParams& P, Ctl& C, uint8_t* ring) {
     }
     int nu;
     const Unit* us = units_of(P, P.plan ? Ld.plan_kind : 0, cta, nu);
+    if (P.trace && tid == 0)
+      for (int t = 0; t < 8; ++t) C.ttype[t] = 0;
     for (int i = 0; i < nu; ++i) {
       const uint64_t tu = (P.trace && tid == 0) ? globaltimer() : 0;
       consume_unit<D>(cs, Ld, us[i], l, acc, zh, zr);
-      if (P.trace && tid == 0) P.trace[((size_t)cta * P.L + l) * 16 + 8 + us[i].type] += globaltimer() - tu;
+      if (P.trace && tid == 0) C.ttype[us[i].type & 7] += globaltimer() - tu;
     }
     if (tid == 0) {
       stamp(P, l, 3);
       if (P.trace) {
-        P.trace[((size_t)cta * P.L + l) * 16 + 6] = cs.t_acq;
-        P.trace[((size_t)cta * P.L + l) * 16 + 7] = cs.n_acq;
+        // plain stores only (a read-modify-write here would stall the CTA's arrival)
+        uint64_t* tr = P.trace + ((size_t)cta * P.L + l) * 16;
+        tr[6] = cs.t_acq;
+        tr[7] = cs.n_acq;
+        for (int t = 1; t < 8; ++t)
+          if (t != U_ROUTER) tr[8 + t] = C.ttype[t];
       }
       cs.t_acq = 0;
       cs.n_acq = 0;

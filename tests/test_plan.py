@@ -79,7 +79,8 @@ def test_plan_with_head_covers_every_row(K):
 
 def test_plan_split_keeps_the_prerouter_off_the_critical_ctas():
     """K = 4 leaves room: prerouter rows only on deferred CTAs, which hold nothing else;
-    LoRA base rows in whole 64-row stage groups; every A unit that keeps v local holds all
+    LoRA base rows in runs of whole 16-row stages of at most an expert slab's bytes (so
+    those CTAs finish with the expert CTAs); every A unit that keeps v local holds all
     ranks, and no CTA without such a unit holds B rows (nobody would publish its v)."""
     d, lr = 2048, 16
     per_cta, defer = plan(0, d=d, K=4, lr=lr)
@@ -92,7 +93,9 @@ def test_plan_split_keeps_the_prerouter_off_the_critical_ctas():
             assert not types & {U_HEAD, U_LRES}
         for u in us:
             if u["type"] == U_QROWS:
-                assert u["r1"] - u["r0"] == 64 and u["r0"] % 64 == 0
+                n = u["r1"] - u["r0"]
+                assert n % 16 == 0 and u["r0"] % 16 == 0 and 64 <= n
+                assert n * (d // 2 + d // 16) <= 64 * (d // 2 + d // 16) + 20 * d  # <= one expert slab
         local = [u for u in us if u["type"] == U_LORA_A and u["flags"] & 1]
         if U_LORA_B in types:
             assert local and local[0]["r0"] == 0 and local[0]["r1"] == lr
