@@ -19,14 +19,19 @@ title and section:
   previous token].  §3.2 "Prediction-as-routing": the prediction is the routing.
 * same page, §3.3: unmerged recovery LoRA y = W_int4(x) + (alpha/r) * B A x.
 * same page, Appendix A "Softmax-topk": g = softmax(l), inds = top-k(g, K),
-  w = g[inds] / sum_inds g.
+  w = g[inds] / sum_inds g; and "Sigmoid-group": group scores from the top-2 sigmoids,
+  top groups kept, top-k within them, w = s * sigma / (sum sigma + 1e-20).
+* BigMoeOnEdge "Route-ahead" notes: layer L's selection is its own gate ranked on the
+  hidden state N layers earlier in the same forward pass.
 
 Modules:
   ``bf16``     bfloat16 <-> float conversion (round to nearest even).
   ``int4``     affine group-64 packing, unpacking and dequantisation.
-  ``routing``  softmax-top-k with renormalisation.
+  ``routing``  softmax-top-k with renormalisation; sigmoid-group routing; the gap a
+               routing decision rests on.
   ``layer``    router, prerouter head, SwiGLU expert, LoRA linear, layer-step,
-               prefill chunk and decode stack.
+               prefill chunk and one decode token through a stack (head-routed,
+               own-gate and route-ahead layers).
 
 Every function is pinned by ``tests/test_oracle_*.py`` against closed forms,
 invariants, textbook values, brute force or page-printed numbers; none is
