@@ -205,14 +205,16 @@ void waterfill(const PlanSpec& s, const std::vector<Granule>& gs, int c0, int c1
 // LoRA work goes one unit per CTA to the next CTAs and the prerouter's work (HEAD, LRES:
 // needed only by the next token) in contiguous runs to CTAs of its own, [n_crit, ncta),
 // which do not hold up the layer: defer[c] = 1 there, *n_crit_out = n_crit.  Otherwise
-// the divisible work is water-filled by cost.  The router rows of an own-gate layer go
-// to CTAs [0, crit_limit).
+// the divisible work is water-filled by cost.  With crit_limit > 0 every unit goes to
+// CTAs [0, crit_limit) (the router rows of an own-gate layer; the layers after a head
+// layer, whose CTAs [crit_limit, ncta) hold the deferred prerouter work).
 e0_status build_plan(const PlanSpec& s, int ncta, Unit* units, uint8_t* counts, uint8_t* defer = nullptr,
                      int* n_crit_out = nullptr, int crit_limit = 0) {
   std::vector<std::vector<Unit>> lists(ncta);
   std::vector<double> load(ncta, 0.0);
   const int d = s.d;
   const double c_exp = W_INT4 * (64.0 * q4_row_bytes(d) + 20.0 * d) + UNIT_COST;
+  const int limit = crit_limit > 0 ? std::min(crit_limit, ncta) : ncta;
   int n_slabs = 0;
   // 1. expert slabs, round robin
   if (s.routed || s.shared) {
@@ -222,7 +224,7 @@ e0_status build_plan(const PlanSpec& s, int ncta, Unit* units, uint8_t* counts, 
       if (k < kmax || s.shared) {
         if (k == kmax && !s.shared) break;
         for (int sl = 0; sl < s.F / 32; ++sl) {
-          const int c = idx++ % ncta;
+          const int c = idx++ % limit;
           lists[c].push_back(Unit{U_EXPERT, (uint8_t)(k < kmax ? k : s.K), (uint16_t)sl, (uint16_t)(sl + 1), 0});
           load[c] += c_exp;
         }
@@ -271,7 +273,6 @@ e0_status build_plan(const PlanSpec& s, int ncta, Unit* units, uint8_t* counts, 
   if (s.head)
     for (int i = 0; i < s.H; i += 8)
       def.push_back({U_HEAD, i, 8, W_BF16 * 8.0 * (2.0 * d + 2.0 * s.E + 2.0 * (1 + 2 * s.K))});
-  const int limit = crit_limit > 0 ? std::min(crit_limit, ncta) : ncta;
   if (split) {
     for (int i = 0; i < n_ab; ++i) {  // all ranks of v, then the B rows of an even slice
       auto& L = lists[n_slabs + i];
@@ -473,7 +474,7 @@ extern "C" e0_status e0_get_device_status(const void* ws, uint32_t* status_out, 
 extern "C" e0_status e0_debug_plan(int32_t d, int32_t E, int32_t F, int32_t K, int32_t H, int32_t lr, int32_t ncta,
                                    int32_t kind, void* units_out, uint8_t* counts_out, uint8_t* defer_out) {
   E0_REQUIRE(units_out && counts_out && defer_out, E0_ERR_INVALID, "e0_debug_plan: NULL argument");
-  E0_REQUIRE(ncta >= 1 && ncta <= MAX_CTAS && kind >= 0 && kind <= 2, E0_ERR_INVALID, "e0_debug_plan: ncta or kind");
+  E0_REQUIRE(ncta >= 1 && ncta <= MAX_CTAS && kind >= 0 && kind <= 3, E0_ERR_INVALID, "e0_debug_plan: ncta or kind");
   E0_REQUIRE(d > 0 && d % 256 == 0 && E >= 1 && F % 32 == 0 && K >= 1 && K <= E && lr >= 0 && lr <= RANKS_MAX &&
                  H >= 0 && H % 8 == 0,
              E0_ERR_SHAPE, "e0_debug_plan: shape");
@@ -489,9 +490,11 @@ extern "C" e0_status e0_debug_plan(int32_t d, int32_t E, int32_t F, int32_t K, i
   std::vector<Unit> tmp((size_t)ncta * MAXU);
   std::vector<uint8_t> tc(ncta), td(ncta);
   int n_crit = ncta;
-  ps.head = H > 0; ps.lres = true; ps.H = H;
-  e0_status st = build_plan(ps, ncta, tmp.data(), tc.data(), td.data(), &n_crit);
+  PlanSpec hs = ps;
+  hs.head = H > 0; hs.lres = true; hs.H = H;
+  e0_status st = build_plan(hs, ncta, tmp.data(), tc.data(), td.data(), &n_crit);
   if (st) return st;
+  if (kind == 3) return build_plan(ps, ncta, u, counts_out, nullptr, nullptr, n_crit);
   PlanSpec rs;
   rs.d = d; rs.E = E; rs.F = F; rs.K = K; rs.router = true;
   return build_plan(rs, ncta, u, counts_out, nullptr, nullptr, n_crit);
@@ -722,8 +725,9 @@ extern "C" e0_status e0_stack_create(e0_stack** out, const e0_dims* dims, const 
   st = device_ctas(dims->d, &ncta);
   if (st) return st;
   std::vector<LayerDesc> descs(L);
-  PlanSpec spec[2];
-  bool have_spec[2] = {false, false};
+  PlanSpec spec[KINDS_MAX];
+  bool have_spec[KINDS_MAX] = {};
+  bool head_before = false;  // a layer before this one has a head
   for (int l = 0; l < L; ++l) {
     LayerDesc& D = descs[l];
     std::memset(&D, 0, sizeof(D));
@@ -766,7 +770,8 @@ extern "C" e0_status e0_stack_create(e0_stack** out, const e0_dims* dims, const 
       E0_REQUIRE(l + src >= 0, E0_ERR_INVALID, "route-ahead by N needs N layers before the layer");
       D.ahead = -src;
     }
-    const int kind = D.has_head ? KIND_MAIN : KIND_MAIN_NOHEAD;
+    const int kind = D.has_head ? KIND_MAIN : (head_before ? KIND_TAIL : KIND_MAIN_NOHEAD);
+    head_before = head_before || D.has_head;
     if (have_spec[kind]) {
       E0_REQUIRE(std::memcmp(&spec[kind], &ps, sizeof(ps)) == 0, E0_ERR_UNSUPPORTED,
                  "stack layers of one kind must share one shape");
@@ -791,6 +796,11 @@ extern "C" e0_status e0_stack_create(e0_stack** out, const e0_dims* dims, const 
       if (st) return st;
       n_crit = std::min(n_crit, nc);
     }
+  if (have_spec[KIND_TAIL]) {
+    st = build_plan(spec[KIND_TAIL], ncta, units.data() + (size_t)KIND_TAIL * ncta * MAXU,
+                    counts.data() + (size_t)KIND_TAIL * ncta, nullptr, nullptr, n_crit);
+    if (st) return st;
+  }
   // route-ahead: the gate rows of layer l run on layer l - N's input (one target per layer)
   for (int l = 0; l < L; ++l)
     if (descs[l].ahead > 0) {

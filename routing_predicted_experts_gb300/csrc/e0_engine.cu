@@ -14,6 +14,7 @@ namespace e0eng {
 struct Ctl {
   uint64_t full[NSTAGES];
   uint64_t empty[NSTAGES];
+  uint64_t rt_bar[LMAX];      // per layer: completes (phase 0) when its route is published
   float res[DMAX];            // residual h of the layer, fp32 (exact bf16 values); x = res * xscale
   uint4 xq[4][DMAX / 32];     // x as int16: xq[t][c] = group t (of 4) of chunk c, stored [0,2,4,6,1,3,5,7]
                               // (group-major, so that lanes reading consecutive chunks hit distinct banks)
@@ -150,6 +151,17 @@ __device__ __forceinline__ bool wait_count(const EngineParams& P, Ctl& C, const 
 }
 
 __device__ __forceinline__ void cbar() { named_bar_sync(1, NCT); }
+
+// Mark layer l's route published (lane 0 of the routing warp, its only writer): the flag
+// for pollers that test it once, and one arrival on the layer's mbarrier, which the
+// consumers wait on suspended in try_wait (a flag spun on by every consumer thread
+// takes the shared-memory pipe from the routing warp while it computes the route).
+__device__ __forceinline__ void mark_route(Ctl& C, int l) {
+  if (C.rt_ready[l]) return;
+  __threadfence_block();
+  C.rt_ready[l] = 1;
+  mbar_arrive(&C.rt_bar[l]);
+}
 
 // Diagnostics: stamp %globaltimer into trace[cta][l][slot] when a trace buffer is set.
 // Slots: 0 consumer layer start, 1 dependency satisfied, 2 layer input built,
@@ -340,8 +352,7 @@ __device__ __forceinline__ void publish_route(Prod& pr, int l, int id, float w) 
   }
   __syncwarp();
   if (lane == 0) {
-    __threadfence_block();
-    C.rt_ready[l] = 1;
+    mark_route(C, l);
     stamp(P, l, 4);
   }
   __syncwarp();
@@ -384,8 +395,7 @@ __device__ __forceinline__ void load_routes(Prod& pr) {
       publish_route(pr, 0, id, w);
     } else if (lane == 0) {
       C.rt_valid[0] = 0u;
-      __threadfence_block();
-      C.rt_ready[0] = 1;
+      mark_route(C, 0);
     }
     __syncwarp();
     return;
@@ -548,7 +558,7 @@ __device__ __forceinline__ void compute_self_route(Prod& pr, int l) {
 __device__ __forceinline__ void need_route(Prod& pr, int l) {
   if (!pr.ok || pr.C.rt_ready[l]) return;
   const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1; !pr.C.rt_ready[l]; ++it) {
+  for (uint32_t it = 1; !mbar_try_wait(&pr.C.rt_bar[l], 0u); ++it) {
     if (!prod_keep_waiting(pr, t0, it)) {
       pr.ok = false;
       return;
@@ -860,19 +870,28 @@ __device__ void producer(const EngineParams& P, Ctl& C, uint8_t* ring) {
   }
 }
 
-// Stack bookkeeping of this CTA's layers in [l0, l1) (layer l on CTA l % ncta): record
-// the ids each layer used (the heads' previous-token one-hot at the next step) and commit
-// the next token's routing of every head-routed layer: the top-K of the logits the
-// previous layer's head produced.
-__device__ __forceinline__ void stack_bookkeeping(Prod& pr, int l0, int l1) {
+// The CTA that keeps the books of layer l: one of the CTAs that hold the prerouter's
+// deferred work when there are any (they hold no work of the layers after the last
+// head, so their routing warps may wait for the heads without holding up a route that
+// their consumers need), else CTA l.
+__device__ __forceinline__ int bookkeeper(const EngineParams& P, int l) {
+  const int nd = P.plan ? P.n_defer[KIND_MAIN] : 0;
+  return nd > 0 ? P.ncta - 1 - l % nd : l % P.ncta;
+}
+
+// Stack bookkeeping of layer l on CTA bookkeeper(l), once its route is published:
+// record the ids the layer used (the heads' previous-token one-hot at the next step)
+// and commit the next token's routing of a head-routed layer: the top-K of the logits
+// the previous layer's head produced.
+__device__ __forceinline__ void bookkeep_layer(Prod& pr, int l) {
   const EngineParams& P = pr.P;
   Ctl& C = pr.C;
+  if (bookkeeper(P, l) != (int)blockIdx.x) return;
   {
     const uint32_t pnext3 = (pr.epoch + 1) % 3u;
-    for (int l = blockIdx.x; l < P.L && pr.ok; l += P.ncta) {
-      if (l < l0 || l >= l1) continue;
-      compute_self_route(pr, l);
-      if (!pr.ok) break;
+    {
+      need_route(pr, l);
+      if (!pr.ok) return;
       if (pr.lane < P.K) {
         const bool v = (C.rt_valid[l] >> pr.lane) & 1u;
         const int id = v ? C.rt_ids[l][pr.lane] : -1;
@@ -888,7 +907,7 @@ __device__ __forceinline__ void stack_bookkeeping(Prod& pr, int l0, int l1) {
         if (!prod_wait_counter(pr, l - 1, on_head ? 1 : 0,
                                (uint32_t)(on_head ? P.n_defer[hk] : (P.plan ? P.n_arrive[hk] : P.ncta)))) {
           pr.ok = false;
-          break;
+          return;
         }
         const float* z = zhat_ptr(P, pnext3, l - 1);
 #pragma unroll 8
@@ -931,33 +950,60 @@ __device__ __forceinline__ void stack_bookkeeping(Prod& pr, int l0, int l1) {
 // complete) and, in the stack, the bookkeeping for the next token.
 __device__ void router_warp(const EngineParams& P, Ctl& C) {
   Prod pr{P, C, nullptr, 0u, true, (int)(threadIdx.x & 31), C.epoch & 1u, C.epoch % 3u, C.epoch};
-  // The leading layers that route with their own gate and have no head need nothing
-  // from the staged routes: publish theirs first and stage the rest afterwards (the
-  // staging takes several microseconds; a head's layer needs its previous-token ids).
-  if (P.mode == MODE_STACK)
-    for (int l = 0; l < P.L && pr.ok && self_routes(P, l) && !layer_at(P, l).has_head; ++l)
-      compute_self_route(pr, l);
-  load_routes(pr);
-  if (P.mode == MODE_STACK) {
-    // routes up to the last layer not routed from gate logits, then this CTA's
-    // bookkeeping of those layers (a committed route leaves as soon as its head is done,
-    // while the launch goes on), then the trailing gate-routed layers and theirs
-    int lc = 0;
+  // The steps in order, each kind from a single call site (so that its code is still in
+  // the instruction cache when the next layer needs it):
+  //   A  the own-gate routes of the leading layers without a head: they need nothing
+  //      staged (the staging takes several microseconds; a head's layer needs its
+  //      previous-token ids)
+  //   S  the staged routes and previous-token ids (load_routes)
+  //   B  the routes up to the last layer not routed from gate logits
+  //   C  this CTA's bookkeeping of those layers (a committed route leaves as soon as its
+  //      head is done, while the launch goes on)
+  //   D  the trailing gate-routed layers, E  their bookkeeping
+  const bool stack = P.mode == MODE_STACK;
+  int lead = 0, lc = 0;
+  if (stack) {
+    while (lead < P.L && self_routes(P, lead) && !layer_at(P, lead).has_head) ++lead;
     for (int l = 0; l < P.L; ++l)
       if (!self_routes(P, l)) lc = l + 1;
-    for (int l = 0; l < lc && pr.ok; ++l) {
-      if (self_routes(P, l))
-        compute_self_route(pr, l);
-      else
-        publish_staged_route(pr, l);
+    lc = max(lc, lead);
+  }
+  const int eA = lead, eS = eA + 1, eB = eS + (lc - lead), eC = eB + lc, eD = eC + (P.L - lc);
+  const int total = stack ? eD + (P.L - lc) : 1;
+  for (int st = 0; st < total && pr.ok; ++st) {
+    int act = 3, l = 0;  // 0 own-gate route, 1 staged route, 2 bookkeeping, 3 load_routes
+    if (stack) {
+      if (st < eA) {
+        act = 0;
+        l = st;
+      } else if (st < eS) {
+        act = 3;
+      } else if (st < eB) {
+        l = lead + st - eS;
+        act = self_routes(P, l) ? 0 : 1;
+      } else if (st < eC) {
+        act = 2;
+        l = st - eB;
+      } else if (st < eD) {
+        act = 0;
+        l = lc + st - eC;
+      } else {
+        act = 2;
+        l = lc + st - eD;
+      }
     }
-    stack_bookkeeping(pr, 0, lc);
-    for (int l = lc; l < P.L && pr.ok; ++l) compute_self_route(pr, l);
-    stack_bookkeeping(pr, lc, P.L);
+    if (act == 0)
+      compute_self_route(pr, l);
+    else if (act == 1)
+      publish_staged_route(pr, l);
+    else if (act == 2)
+      bookkeep_layer(pr, l);
+    else
+      load_routes(pr);
   }
   // After an abort, mark every route published so that no consumer waits on one.
   if (pr.lane == 0 && !pr.ok)
-    for (int l = 0; l < P.L; ++l) C.rt_ready[l] = 1;
+    for (int l = 0; l < P.L; ++l) mark_route(C, l);
 }
 
 // ------------------------------------------------------------------ consumers
@@ -1004,10 +1050,10 @@ struct Cons {
     // warp-uniform, so that the shuffles that follow a successful acquire see every lane
     return __all_sync(0xffffffffu, ok);
   }
-  // Wait until the routing warp has published layer l's route.  Every lane polls: a
-  // single polling lane followed by a warp barrier measured several times slower in
-  // the code that follows.
-  __device__ __forceinline__ void wait_route(int l) { wait_flag(P, C, &C.rt_ready[l]); }
+  // Wait until the routing warp has published layer l's route (every lane waits on the
+  // layer's mbarrier: a single waiting lane followed by a warp barrier measured several
+  // times slower in the code that follows).
+  __device__ __forceinline__ void wait_route(int l) { wait_mbar(P, C, &C.rt_bar[l], 0u); }
   // This warp is done reading the next cnt stages.
   __device__ void release(int cnt) {
     __syncwarp();
@@ -1748,6 +1794,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) engine_kernel(const __grid_consta
       mbar_init(&C.full[s], 1);
       mbar_init(&C.empty[s], NCW);
     }
+    for (int l = 0; l < LMAX; ++l) mbar_init(&C.rt_bar[l], 1);
     fence_mbar_init();
     for (int l = 0; l < LMAX; ++l) C.rt_ready[l] = 0;
     C.abort_flag = 0;

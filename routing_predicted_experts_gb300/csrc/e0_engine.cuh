@@ -46,7 +46,7 @@ constexpr int MAXU = 8;                       // units per CTA per plan kind
 constexpr int MAX_CTAS = 160;
 constexpr int HEAD_ROWS = 64;                 // max fc1 rows per U_HEAD unit
 constexpr int RANKS_MAX = 64;                 // max LoRA rank
-constexpr int KINDS_MAX = 3;
+constexpr int KINDS_MAX = 4;
 constexpr int LMAX = 48;                      // layers per launch
 constexpr float RMS_EPS = 1e-6f;
 
@@ -66,7 +66,9 @@ static_assert(sizeof(Unit) == 8, "Unit must stay 8 bytes");
 enum Mode : int32_t { MODE_LAYER = 0, MODE_HEAD = 1, MODE_QLINEAR = 2, MODE_STACK = 3 };
 
 // Plan kinds (stack mode): main phase with head / without head, router phase.
-enum Kind : int32_t { KIND_MAIN = 0, KIND_MAIN_NOHEAD = 1, KIND_ROUTER = 2 };
+// KIND_TAIL: the layers without a head that follow a layer with one; their work stays
+// off the CTAs that hold the prerouter's (deferred) work, which run behind the layers.
+enum Kind : int32_t { KIND_MAIN = 0, KIND_MAIN_NOHEAD = 1, KIND_ROUTER = 2, KIND_TAIL = 3 };
 
 struct LayerDesc {
   // routed experts
@@ -112,7 +114,7 @@ struct LayerDesc {
   const float* score_bias;  // sigmoid-group routing: selection bias of this layer's routing (nullable)
   const uint32_t* ready;    // stack, slot pools: word equal to the token index once this layer's
                             // experts and slot_of table are in place (nullable)
-  int32_t plan_kind;  // KIND_MAIN or KIND_MAIN_NOHEAD
+  int32_t plan_kind;  // KIND_MAIN, KIND_MAIN_NOHEAD or KIND_TAIL
   int32_t prerouted;  // 1: routing comes from the previous layer's head (after step 0)
   int32_t ahead;      // N > 0: route-ahead, this layer's gate runs on layer (l - N)'s input
   int32_t gate_for;   // stack: the layer whose route-ahead gate rows run on this layer's input, or -1

@@ -120,6 +120,24 @@ def test_plan_without_head_and_router_rows():
             assert not defer0[c]
 
 
+@pytest.mark.parametrize("K", [4, 8])
+def test_plan_after_a_head_layer_stays_off_the_deferred_ctas(K):
+    """A layer without a head after one with a head (the last layer of the stack): all of
+    its work, every row once, on the CTAs that layers with a head keep on the critical
+    path (the deferred CTAs run behind the layers with the prerouter's work)."""
+    d, E, F, H, lr = 2048, 256, 512, 1024, 16
+    per_cta, defer = plan(3, d, E, F, K, H, lr)
+    check_common(per_cta, d, E, F, K, lr)
+    assert not defer.any()
+    _, defer0 = plan(0, d, E, F, K, H, lr)
+    for c, us in enumerate(per_cta):
+        if defer0[c]:
+            assert len(us) == 0
+    if not defer0.any():  # no room for deferred CTAs: the same plan as kind 1
+        plain, _ = plan(1, d, E, F, K, H, lr)
+        assert [list(map(tuple, us)) for us in plain] == [list(map(tuple, us)) for us in per_cta]
+
+
 def test_plan_tiny_layer():
     d, E, F, K, H, lr = 256, 16, 128, 4, 64, 4
     for kind in (0, 1):
