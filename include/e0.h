@@ -255,9 +255,9 @@ e0_status e0_moe_decode_layer(const e0_dims* dims, const e0_experts* routed,
  *   the lower id), w = softmax over the selected logits; delta = sum_k w_k E_{ids_k}(x)
  *   + E_shared(x) + LoRA(x); h_out[t] = bf16(h_in[t] + delta).
  *   h_in, h_out: bf16 bits [T][d] (16-byte aligned); logits fp32 [T][E].
- *   delta_f32 fp32 [T][d], ids_out int32 [T][K], weights_out fp32 [T][K]: nullable.
- *   routed: all E experts resident (slot_of must be NULL); shared, lora nullable; the
- *   LoRA linear must be d x d.  Shapes: d and 2F multiples of 256, F of 64, E <= 1024,
+ *   delta_f32 fp32 [T][d] (16-byte aligned), ids_out int32 [T][K], weights_out fp32
+ *   [T][K]: nullable.  routed: all E experts resident (slot_of must be NULL); shared,
+ *   lora nullable; the LoRA linear must be d x d, its B^T 8-byte aligned.  Shapes: d and 2F multiples of 256, F of 64, E <= 1024,
  *   K <= 16, T*K <= 65536.
  *   workspace: caller-owned device memory of e0_prefill_workspace_size(dims, T,
  *   lora_out) bytes (lora_out = the LoRA output width, 0 without LoRA); its first 256
@@ -473,7 +473,9 @@ e0_status e0_debug_trace(uint64_t* buf, size_t bytes);
  * on the host (no device needed), for one layer kind: 0 a layer with a prerouter head
  * (routed and shared experts, d x d LoRA linear of rank lr, head of H fc1 rows), 1 the
  * same without a head, 2 the own-gate router rows (over the CTAs that kind 0 leaves on
- * the critical path).  units_out: ncta * 8 units of 8 bytes, {type u8, k u8, r0 u16,
+ * the critical path), 3 a layer without a head after one with a head (kind 1's work
+ * over the CTAs that kind 0 leaves on the critical path: the CTAs with prerouter work
+ * run behind the layers).  units_out: ncta * 8 units of 8 bytes, {type u8, k u8, r0 u16,
  * r1 u16, flags u16}, unit types as in the engine (1 expert slab, 2 LoRA base rows,
  * 3 LoRA A ranks, 4 head fc1 rows, 5 head residual rows, 6 gate rows, 7 LoRA B rows);
  * counts_out[ncta] units per CTA; defer_out[ncta] = 1 where a CTA holds only

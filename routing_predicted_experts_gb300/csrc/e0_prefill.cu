@@ -103,23 +103,33 @@ __device__ __forceinline__ __half2 bf16pair_to_h2(uint16_t v) {
 }
 
 // Dequantise 32 codes (one uint4: half of a 64-code weight row segment) to 16 fp16 pairs:
-// codes j and j + 4 of each 8-code word become one pair (1024 + c by the exponent trick,
-// then exactly c, then s*c + b), which is the element order [0,4,1,5,2,6,3,7] within
-// every group of 8 that the token rows use as well.
+// codes j and j + 4 of each 8-code word become one pair, which is the element order
+// [0,4,1,5,2,6,3,7] within every group of 8 that the token rows use as well.  A pair is
+// formed by the exponent trick without a shift for j = 0, 1 (and one shift of the word
+// by 8 for j = 2, 3): masked into the mantissa of 1024 (0x6400), a code c in the low
+// nibble of each half gives 1024 + c, in the high nibble 1024 + 16 c; c is recovered
+// exactly as t - 1024 or t / 16 - 64, then s * c + b.
 __device__ __forceinline__ void dequant32(const uint8_t* codes, __half2 s2, __half2 b2, uint32_t (&out)[16]) {
   const uint4 w0 = *reinterpret_cast<const uint4*>(codes);
   const uint32_t words[4] = {w0.x, w0.y, w0.z, w0.w};
-  const __half2 magic = __halves2half2(__ushort_as_half((unsigned short)0x6400), __ushort_as_half((unsigned short)0x6400));
+  const __half2 k1024 = __halves2half2(__ushort_as_half((unsigned short)0x6400), __ushort_as_half((unsigned short)0x6400));
+  const __half2 k16th = __halves2half2(__ushort_as_half((unsigned short)0x2C00), __ushort_as_half((unsigned short)0x2C00));
+  const __half2 km64 = __halves2half2(__ushort_as_half((unsigned short)0xD400), __ushort_as_half((unsigned short)0xD400));
 #pragma unroll
-  for (int mm = 0; mm < 4; ++mm)
+  for (int mm = 0; mm < 4; ++mm) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t t = ((words[mm] >> (4 * j)) & 0x000F000Fu) | 0x64006400u;
-      __half2 c = *reinterpret_cast<const __half2*>(&t);
-      c = __hsub2(c, magic);
-      const __half2 w = __hfma2(c, s2, b2);
-      out[4 * mm + j] = *reinterpret_cast<const uint32_t*>(&w);
+    for (int hb = 0; hb < 2; ++hb) {
+      const uint32_t v = words[mm] >> (8 * hb);
+      const uint32_t tl = (v & 0x000F000Fu) | 0x64006400u;  // codes 2hb, 2hb + 4: 1024 + c
+      const uint32_t th = (v & 0x00F000F0u) | 0x64006400u;  // codes 2hb + 1, 2hb + 5: 1024 + 16 c
+      const __half2 cl = __hsub2(*reinterpret_cast<const __half2*>(&tl), k1024);
+      const __half2 ch = __hfma2(*reinterpret_cast<const __half2*>(&th), k16th, km64);
+      const __half2 wl = __hfma2(cl, s2, b2);
+      const __half2 wh = __hfma2(ch, s2, b2);
+      out[4 * mm + 2 * hb] = *reinterpret_cast<const uint32_t*>(&wl);
+      out[4 * mm + 2 * hb + 1] = *reinterpret_cast<const uint32_t*>(&wh);
     }
+  }
 }
 
 __device__ __forceinline__ void cp_async_bar_arrive(uint64_t* bar) {
@@ -598,79 +608,94 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* h, int d, i
   }
 }
 
-// (alpha/r) B (A x) added to the LoRA base output of each token (fp32 x).
-// LORA_TOK tokens per CTA, so that each CTA reads A and B^T once for several tokens;
-// operands in 16-byte vectors (8 bf16).
-constexpr int LORA_TOK = 4;
-__global__ void __launch_bounds__(256) lora_ab_kernel(const uint16_t* h, const float* xscale, int T, int d, int out,
-                                                      const uint16_t* a, const uint16_t* bt, int r, float lscale,
-                                                      float* yl) {
-  __shared__ float v[LORA_TOK][e0eng::RANKS_MAX];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  const int t0 = blockIdx.x * LORA_TOK, nt = min(LORA_TOK, T - t0);
-  // v[t][q] = xscale_t * (A_q . h_t)
-  for (int q = warp; q < r; q += nw) {
-    float s[LORA_TOK];
+// LoRA down projection v[t][q] = xscale_t * (A_q . h_t) (= A x_t, fp32): one warp per
+// token and group of four ranks, the token's row read once for all four.
+constexpr int LA_RANKS = 4;
+__global__ void __launch_bounds__(256) lora_a_kernel(const uint16_t* h, const float* xscale, int T, int d,
+                                                     const uint16_t* a, int r, float* v) {
+  const int lane = threadIdx.x & 31;
+  const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int groups = (r + LA_RANKS - 1) / LA_RANKS;
+  if (gw >= T * groups) return;  // warp-uniform
+  const int t = gw / groups, q0 = (gw % groups) * LA_RANKS;
+  float s[LA_RANKS] = {};
+  const uint4* hp = reinterpret_cast<const uint4*>(h + (size_t)t * d);
+  for (int c = lane; c < d / 8; c += 32) {
+    const uint4 hv = __ldg(hp + c);
+    const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
 #pragma unroll
-    for (int u = 0; u < LORA_TOK; ++u) s[u] = 0.f;
-    const uint4* aq = reinterpret_cast<const uint4*>(a + (size_t)q * d);
-    for (int c = lane; c < d / 8; c += 32) {
-      const uint4 av = __ldg(aq + c);
-      const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
+    for (int u = 0; u < LA_RANKS; ++u)
+      if (q0 + u < r) {
+        const uint4 av = __ldg(reinterpret_cast<const uint4*>(a + (size_t)(q0 + u) * d) + c);
+        const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
 #pragma unroll
-      for (int u = 0; u < LORA_TOK; ++u)
-        if (u < nt) {
-          const uint4 hv = __ldg(reinterpret_cast<const uint4*>(h + (size_t)(t0 + u) * d) + c);
-          const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            s[u] = fmaf(__uint_as_float(aw[m] << 16), __uint_as_float(hw[m] << 16), s[u]);
-            s[u] = fmaf(__uint_as_float(aw[m] & 0xFFFF0000u), __uint_as_float(hw[m] & 0xFFFF0000u), s[u]);
-          }
+        for (int m = 0; m < 4; ++m) {
+          s[u] = fmaf(__uint_as_float(aw[m] << 16), __uint_as_float(hw[m] << 16), s[u]);
+          s[u] = fmaf(__uint_as_float(aw[m] & 0xFFFF0000u), __uint_as_float(hw[m] & 0xFFFF0000u), s[u]);
         }
-    }
-#pragma unroll
-    for (int u = 0; u < LORA_TOK; ++u) {
-      const float w = warp_sum(s[u]);
-      if (lane == 0 && u < nt) v[u][q] = w * xscale[t0 + u];
-    }
+      }
   }
-  __syncthreads();
-  // yl[t][i] += (alpha / r) * sum_q B^T[q][i] v[t][q]
-  for (int i = threadIdx.x; i < out; i += blockDim.x) {
-    float y[LORA_TOK];
 #pragma unroll
-    for (int u = 0; u < LORA_TOK; ++u) y[u] = 0.f;
-    for (int q = 0; q < r; ++q) {
-      const float b = bf16_bits_to_f32(bt[(size_t)q * out + i]);
-#pragma unroll
-      for (int u = 0; u < LORA_TOK; ++u) y[u] = fmaf(b, v[u][q], y[u]);
-    }
-#pragma unroll
-    for (int u = 0; u < LORA_TOK; ++u)
-      if (u < nt) yl[(size_t)(t0 + u) * out + i] += lscale * y[u];
+  for (int u = 0; u < LA_RANKS; ++u) {
+    const float w = warp_sum(s[u]);
+    if (lane == 0 && q0 + u < r) v[(size_t)t * r + q0 + u] = w * xscale[t];
   }
 }
 
-// h_out = bf16(h + sum_k y_(t,k) + y_shared + y_lora), the pairs summed in k order.
-__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* h, int d, int K, const int* inv,
+// h_out = bf16(h + sum_k y_(t,k) + y_shared + y_lora), the pairs summed in k order, with
+// y_lora = W_int4 x + (alpha/r) B v (the LoRA up projection formed here from v).  A thread
+// owns 4 adjacent outputs (16-byte loads) of CT tokens; B^T's rows stay in L1 across them.
+constexpr int CT = 4;
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* h, int T, int d, int K, const int* inv,
                                                       const float* yslot, const float* ys, const float* yl,
+                                                      const float* v, const uint16_t* bt, int r, float lscale,
                                                       uint16_t* h_out, float* delta) {
-  const int t = blockIdx.x;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    float s = 0.f;
-    for (int k = 0; k < K; ++k) s += yslot[(size_t)inv[t * K + k] * d + i];
-    if (ys) s += ys[(size_t)t * d + i];
-    if (yl) s += yl[(size_t)t * d + i];
-    if (delta) delta[(size_t)t * d + i] = s;
-    h_out[(size_t)t * d + i] = f32_to_bf16_bits(bf16_bits_to_f32(h[(size_t)t * d + i]) + s);
+  __shared__ float vs[CT][e0eng::RANKS_MAX];
+  const int t0 = blockIdx.y * CT, nt = min(CT, T - t0);
+  const int nv = v ? r : 0;
+  for (int i = threadIdx.x; i < nt * nv; i += blockDim.x) vs[i / nv][i % nv] = v[(size_t)t0 * nv + i];
+  __syncthreads();
+  const int i0 = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (i0 >= d) return;
+  for (int u = 0; u < nt; ++u) {
+    const int t = t0 + u;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < K; ++k) {
+      const float4 y = __ldg(reinterpret_cast<const float4*>(yslot + (size_t)inv[t * K + k] * d + i0));
+      s.x += y.x; s.y += y.y; s.z += y.z; s.w += y.w;
+    }
+    if (ys) {
+      const float4 y = __ldg(reinterpret_cast<const float4*>(ys + (size_t)t * d + i0));
+      s.x += y.x; s.y += y.y; s.z += y.z; s.w += y.w;
+    }
+    if (yl) {
+      float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int q = 0; q < nv; ++q) {
+        const uint2 bw = __ldg(reinterpret_cast<const uint2*>(bt + (size_t)q * d + i0));
+        const float vq = vs[u][q];
+        b.x = fmaf(__uint_as_float(bw.x << 16), vq, b.x);
+        b.y = fmaf(__uint_as_float(bw.x & 0xFFFF0000u), vq, b.y);
+        b.z = fmaf(__uint_as_float(bw.y << 16), vq, b.z);
+        b.w = fmaf(__uint_as_float(bw.y & 0xFFFF0000u), vq, b.w);
+      }
+      const float4 y = __ldg(reinterpret_cast<const float4*>(yl + (size_t)t * d + i0));
+      s.x += y.x + lscale * b.x; s.y += y.y + lscale * b.y; s.z += y.z + lscale * b.z; s.w += y.w + lscale * b.w;
+    }
+    if (delta) *reinterpret_cast<float4*>(delta + (size_t)t * d + i0) = s;
+    const uint2 hw = *reinterpret_cast<const uint2*>(h + (size_t)t * d + i0);
+    uint2 o;
+    o.x = (uint32_t)f32_to_bf16_bits(__uint_as_float(hw.x << 16) + s.x) |
+          ((uint32_t)f32_to_bf16_bits(__uint_as_float(hw.x & 0xFFFF0000u) + s.y) << 16);
+    o.y = (uint32_t)f32_to_bf16_bits(__uint_as_float(hw.y << 16) + s.z) |
+          ((uint32_t)f32_to_bf16_bits(__uint_as_float(hw.y & 0xFFFF0000u) + s.w) << 16);
+    *reinterpret_cast<uint2*>(h_out + (size_t)t * d + i0) = o;
   }
 }
 
 // ------------------------------------------------------------------ workspace
 struct PfLayout {
   size_t ids, w, row_off, tile_off, one_row, one_tile, inv, perm, wrow, xscale, x16, x16s, a16s, yslot, as16, ys, yl,
-      total;
+      lv, total;
 };
 
 inline size_t al(size_t x) { return (x + 255) & ~size_t(255); }
@@ -696,6 +721,7 @@ PfLayout pf_layout(int d, int E, int F, int K, int T, int out, bool shared, bool
   L.as16 = o;     o = al(o + (shared ? 2 * (size_t)T * F : 0));
   L.ys = o;       o = al(o + (shared ? 4 * (size_t)T * d : 0));
   L.yl = o;       o = al(o + (lora ? 4 * (size_t)T * out : 0));
+  L.lv = o;       o = al(o + (lora ? 4 * (size_t)T * e0eng::RANKS_MAX : 0));
   L.total = o;
   return L;
 }
@@ -760,7 +786,10 @@ e0_status e0pf_grouped_layer(const e0_dims* dims, const e0_experts* routed, cons
     E0_REQUIRE(lora->out == d, E0_ERR_SHAPE, "e0_moe_prefill_layer: the LoRA linear must be d x d");
     E0_REQUIRE(lora->r >= 0 && lora->r <= e0eng::RANKS_MAX, E0_ERR_SHAPE, "e0_moe_prefill_layer: LoRA rank must be in [0, 64]");
   }
-  E0_REQUIRE(al16p(h_in) && al16p(h_out), E0_ERR_INVALID, "e0_moe_prefill_layer: h_in/h_out must be 16-byte aligned");
+  E0_REQUIRE(al16p(h_in) && al16p(h_out) && (!delta_f32 || al16p(delta_f32)), E0_ERR_INVALID,
+             "e0_moe_prefill_layer: h_in/h_out/delta_f32 must be 16-byte aligned");
+  E0_REQUIRE(!has_lora || !lora->bt || ((uintptr_t)lora->bt & 7u) == 0, E0_ERR_INVALID,
+             "e0_moe_prefill_layer: the LoRA B^T matrix must be 8-byte aligned");
   E0_REQUIRE(!has_lora || !lora->a || al16p(lora->a), E0_ERR_INVALID,
              "e0_moe_prefill_layer: the LoRA A matrix must be 16-byte aligned");
   const PfLayout L = pf_layout(d, E, F, K, T, out, true, has_lora);
@@ -836,6 +865,7 @@ e0_status e0pf_grouped_layer(const e0_dims* dims, const e0_experts* routed, cons
     E0_CHECK_CUDA((launch_gemm<E0_LAYOUT_COLSLAB, EPI_F32>(g, st)));
   }
   float* yl = nullptr;
+  float* lv = nullptr;
   if (has_lora) {
     yl = (float*)P(L.yl);
     g.A = x16; g.lda = d; g.K = d; g.N = out; g.ngroups = 1; g.row_off = one_row; g.tile_off = one_tile;
@@ -843,12 +873,15 @@ e0_status e0pf_grouped_layer(const e0_dims* dims, const e0_experts* routed, cons
     g.out16 = nullptr; g.out32 = yl; g.ldo = out; g.rowscale = nullptr;
     E0_CHECK_CUDA((launch_gemm<E0_LAYOUT_ROWS, EPI_F32>(g, st)));
     if (lora->r > 0 && lora->a && lora->bt) {
-      lora_ab_kernel<<<(T + LORA_TOK - 1) / LORA_TOK, 256, 0, st>>>(h_in, xscale, T, d, out, lora->a, lora->bt, lora->r,
-                                                                     lora->alpha / lora->r, yl);
+      lv = (float*)P(L.lv);
+      const int warps = T * ((lora->r + LA_RANKS - 1) / LA_RANKS);
+      lora_a_kernel<<<(warps + 7) / 8, 256, 0, st>>>(h_in, xscale, T, d, lora->a, lora->r, lv);
       E0_CHECK_CUDA(cudaGetLastError());
     }
   }
-  combine_kernel<<<T, 256, 0, st>>>(h_in, d, K, inv, yslot, ys, yl, h_out, delta_f32);
+  const dim3 cgrid((d / 4 + 255) / 256, (T + CT - 1) / CT);
+  combine_kernel<<<cgrid, 256, 0, st>>>(h_in, T, d, K, inv, yslot, ys, yl, lv, lv ? lora->bt : nullptr,
+                                        lv ? lora->r : 0, lv ? lora->alpha / lora->r : 0.f, h_out, delta_f32);
   E0_CHECK_CUDA(cudaGetLastError());
   return E0_OK;
 }
