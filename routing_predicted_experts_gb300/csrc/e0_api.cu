@@ -267,7 +267,7 @@ e0_status build_plan(const PlanSpec& s, int ncta, Unit* units, uint8_t* counts, 
       crit.push_back({U_QROWS, r, nr, W_QROWS * nr * (double)q4_row_bytes(d) + W_BF16 * nr * 2.0 * s.lr});
     }
   if (s.router)
-    for (int e = 0; e < s.E; e += 8) crit.push_back({U_ROUTER, e, 8, W_BF16 * 8.0 * 2.0 * d});
+    for (int e = 0; e < s.E; e += 4) crit.push_back({U_ROUTER, e, std::min(4, s.E - e), W_BF16 * 4.0 * 2.0 * d});
   if (s.lres)
     for (int e = 0; e < s.E; e += 8) def.push_back({U_LRES, e, 8, W_BF16 * 8.0 * 2.0 * d});
   if (s.head)
