@@ -257,7 +257,8 @@ e0_status e0_moe_decode_layer(const e0_dims* dims, const e0_experts* routed,
  *   h_in, h_out: bf16 bits [T][d] (16-byte aligned); logits fp32 [T][E].
  *   delta_f32 fp32 [T][d] (16-byte aligned), ids_out int32 [T][K], weights_out fp32
  *   [T][K]: nullable.  routed: all E experts resident (slot_of must be NULL); shared,
- *   lora nullable; the LoRA linear must be d x d, its B^T 8-byte aligned.  Shapes: d and 2F multiples of 256, F of 64, E <= 1024,
+ *   lora nullable; the LoRA linear must be d x d, its B^T 8-byte aligned; every int4
+ *   code, scale and bias array 16-byte aligned.  Shapes: d and 2F multiples of 256, F of 64, E <= 1024,
  *   K <= 16, T*K <= 65536.
  *   workspace: caller-owned device memory of e0_prefill_workspace_size(dims, T,
  *   lora_out) bytes (lora_out = the LoRA output width, 0 without LoRA); its first 256

@@ -40,19 +40,28 @@ namespace e0pf {
 constexpr int WM = 128;                      // weight rows per tile: the MMA's M
 constexpr int TT = 64;                       // token rows per tile, at most: the MMA's N
 constexpr int BK = 64;                       // reduction block
-constexpr int STAGES = 14;                   // copy stages in flight: token rows and codes
 constexpr int NWD = 2;                       // dequantise -> MMA hand-over buffers
 constexpr int X_BYTES = TT * BK * 2;         // 8 KB of fp16 token rows
 constexpr int Q_BYTES = WM * BK / 2;         // 4 KB of int4 codes
 constexpr int RAW_BYTES = X_BYTES + Q_BYTES;
-constexpr int BKD = 2 * BK;                  // reduction block of one dequantise -> MMA hand-over
-// A hand-over carries the MMA's operands for two k-blocks: the dequantised weights (A) in
-// tensor memory, 64 columns (lane = weight row, two fp16 per column), and a copy of the
-// token rows (B) in shared memory, so that a copy stage is free as soon as it has been
-// converted and only the hand-over buffers wait for the tensor core.
-constexpr int A_COLS = BKD / 2;              // tensor-memory columns of one hand-over's weights
-constexpr int HB_BYTES = 2 * X_BYTES;        // 16 KB of token rows per hand-over buffer
 constexpr int EMAXP = 1024;
+// A hand-over carries the MMA's operands for HK k-blocks (HK = 4 when the reduction
+// length allows it, else 2): the dequantised weights (A) in tensor memory, 32 columns per
+// k-block (lane = weight row, two fp16 per column), and a copy of the token rows (B) in
+// shared memory, so that a copy stage is free as soon as it has been converted and only
+// the hand-over buffers wait for the tensor core.  Four k-blocks per hand-over halve the
+// waits, fences and index work per converted weight.
+template <int HK>
+struct Cfg {
+  static constexpr int STAGES = HK == 4 ? 12 : 14;       // copy stages in flight
+  static constexpr int A_COLS = HK * BK / 2;             // tensor-memory columns of one hand-over
+  static constexpr int HB_BYTES = HK * X_BYTES;          // token rows of one hand-over buffer
+  static constexpr int TMEM_COLS = 2 * TT + NWD * A_COLS <= 256 ? 256 : 512;
+  static constexpr size_t SMEM = 1024 + (size_t)STAGES * RAW_BYTES + NWD * HB_BYTES + 2 * (EMAXP + 1) * sizeof(int);
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+  static_assert(STAGES % HK == 0, "a hand-over's stages sit in one ring pass");
+  static_assert(2 * TT + NWD * A_COLS <= TMEM_COLS, "tensor memory columns");
+};
 // roles: warps 0..3 copy (job j by warp j % 4), warps 4..19 dequantise, warp 20 issues the
 // MMAs, warps 21..24 run the epilogue (tensor-memory lane quadrants 1, 2, 3, 0)
 constexpr int W_COPY = 0, N_COPY = 4, W_DQ0 = 4, N_DQ = 16, W_MMA = 20, W_EPI0 = 21, N_EPI = 4;
@@ -61,17 +70,10 @@ constexpr int W_COPY = 0, N_COPY = 4, W_DQ0 = 4, N_DQ = 16, W_MMA = 20, W_EPI0 =
 constexpr int DQ_GROUPS = 2, N_DQG = N_DQ / DQ_GROUPS;
 // warp i of a group writes tensor-memory lanes 32 (warp % 4) .. + 31 (the lane quadrant a
 // warp may access) and half i / 4 of each 64-wide k-block: 4 code words, 16 columns
-constexpr int TMEM_COLS = 2 * TT + NWD * A_COLS;
 constexpr int GT = 32 * (W_EPI0 + N_EPI);
-constexpr size_t GEMM_SMEM = 1024 + (size_t)STAGES * RAW_BYTES + NWD * HB_BYTES + 2 * (EMAXP + 1) * sizeof(int);
 static_assert(X_BYTES % 1024 == 0 && RAW_BYTES % 1024 == 0, "stages stay 1024-byte aligned");
-static_assert(2 * TT >= 32 && (2 * TT & (2 * TT - 1)) == 0, "tensor memory columns: a power of two >= 32");
-static_assert(GEMM_SMEM <= 227 * 1024, "shared memory");
 static_assert(N_DQG == 8 && WM == 128 && W_DQ0 % 4 == 0, "two warps per lane quadrant in a group, one per half block");
-static_assert(TMEM_COLS == 256, "tensor memory columns: a power of two >= 32");
 static_assert(NWD == DQ_GROUPS, "one hand-over buffer per dequantising group");
-static_assert(STAGES % 2 == 0, "a hand-over's two stages sit in one ring pass");
-static_assert(BKD % BK == 0 && BKD / BK == 2, "a hand-over covers two copy stages");
 
 enum Epi : int { EPI_SWIGLU = 0, EPI_F32 = 1 };
 
@@ -143,8 +145,10 @@ __device__ __forceinline__ void cp_async_bar_arrive(uint64_t* bar) {
 // [token] lives in tensor memory, double-buffered so the epilogue of one tile overlaps
 // the next tile's MMAs.  Copy, dequantisation, MMA and epilogue run in their own warps,
 // handing stages over through mbarriers; every wait is bounded.
-template <int LAYOUT, int EPI>
+template <int LAYOUT, int EPI, int HK>
 __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ GemmArgs g) {
+  using C = Cfg<HK>;
+  constexpr int STAGES = C::STAGES, A_COLS = C::A_COLS, HB_BYTES = C::HB_BYTES, TMEM_COLS = C::TMEM_COLS;
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
   uint8_t* raw = sm;                                // STAGES x [token rows | codes]
@@ -258,57 +262,77 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
     const int dt = tid - 32 * W_DQ0, grp = dt / (32 * N_DQG), gtid = dt % (32 * N_DQG);
     const int n = 32 * (warp & 3) + lane, h = (gtid >> 5) >> 2;
     const uint32_t a_lane = (uint32_t)(32 * (warp & 3)) << 16;
-    // scales and biases of this row for the two k-blocks of hand-over p (prefetched two
-    // hand-overs of the group ahead); the tile of the last fetch is cached
+    // scales and biases of this row for the HK k-blocks of hand-over p, as HK / 2 words
+    // of two bf16 each (prefetched two hand-overs of the group ahead; in the rows layout
+    // they are HK contiguous bf16: one vector load); the tile of the last fetch is cached
     int t_i = -1;
     Tile tt{};
-    auto fetch = [&](int p, uint16_t (&sv)[2], uint16_t (&bv)[2]) {
-      sv[0] = sv[1] = bv[0] = bv[1] = 0;
-      if (2 * p >= jobs) return;
-      const int j0 = 2 * p, i = j0 / KB, kb = j0 % KB;
+    using SW = uint32_t[HK / 2];
+    auto fetch = [&](int p, SW& sv, SW& bv) {
+#pragma unroll
+      for (int u = 0; u < HK / 2; ++u) sv[u] = bv[u] = 0u;
+      if (HK * p >= jobs) return;
+      const int j0 = HK * p, i = j0 / KB, kb = j0 % KB;
       if (i != t_i) {
         t_i = i;
         tt = tile_of(i);
       }
+      if (LAYOUT == E0_LAYOUT_ROWS) {
+        // K / 64 is a multiple of HK and kb of HK: HK * 2 bytes, aligned
+        const size_t idx = ((size_t)tt.slot * g.N + tt.n0 + n) * (g.K / 64) + kb;
+        if (HK == 4) {
+          const uint2 a = __ldg(reinterpret_cast<const uint2*>(g.s + idx));
+          const uint2 b = __ldg(reinterpret_cast<const uint2*>(g.b + idx));
+          sv[0] = a.x; sv[HK / 2 - 1] = a.y;
+          bv[0] = b.x; bv[HK / 2 - 1] = b.y;
+        } else {
+          sv[0] = __ldg(reinterpret_cast<const uint32_t*>(g.s + idx));
+          bv[0] = __ldg(reinterpret_cast<const uint32_t*>(g.b + idx));
+        }
+      } else {
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        size_t idx;
-        if (LAYOUT == E0_LAYOUT_ROWS)
-          idx = ((size_t)tt.slot * g.N + tt.n0 + n) * (g.K / 64) + kb + u;
-        else
-          idx = ((size_t)tt.slot * (g.K / 64) + kb + u) * g.N + tt.n0 + n;
-        sv[u] = __ldg(g.s + idx);
-        bv[u] = __ldg(g.b + idx);
+        for (int u = 0; u < HK; ++u) {
+          const size_t idx = ((size_t)tt.slot * (g.K / 64) + kb + u) * g.N + tt.n0 + n;
+          const uint32_t sh = (uint32_t)__ldg(g.s + idx), bh = (uint32_t)__ldg(g.b + idx);
+          sv[u / 2] |= sh << (16 * (u & 1));
+          bv[u / 2] |= bh << (16 * (u & 1));
+        }
       }
     };
     // three hand-overs of scales in flight: current, next and the one after
-    uint16_t cs[2], cb[2], ns[2], nb[2], ms[2], mb[2];
+    SW cs, cb, ns, nb, ms, mb;
     fetch(grp, cs, cb);
     fetch(grp + DQ_GROUPS, ns, nb);
     fetch(grp + 2 * DQ_GROUPS, ms, mb);
     int x_i = -1, x_bytes = X_BYTES;  // token-row bytes to hand over: the tile's rows rounded to 16
-    for (int p = grp; 2 * p < jobs; p += DQ_GROUPS) {
-      const int j0 = 2 * p, buf = p % NWD;  // this group's buffer: p % NWD == grp
+    int st0 = (HK * grp) % STAGES;      // first stage of hand-over p, and its ring pass
+    uint32_t ph0 = (uint32_t)((HK * grp) / STAGES) & 1u;
+    for (int p = grp; HK * p < jobs; p += DQ_GROUPS) {
+      const int j0 = HK * p, buf = p % NWD;  // this group's buffer: p % NWD == grp
       if (j0 / KB != x_i) {
         x_i = j0 / KB;
         x_bytes = ((tile_of(x_i).rows + 15) & ~15) * 128;
       }
-      if (!wait(&full[j0 % STAGES], (j0 / STAGES) & 1)) break;
-      if (!wait(&full[(j0 + 1) % STAGES], ((j0 + 1) / STAGES) & 1)) break;
+      bool ok = true;
+#pragma unroll
+      for (int h2 = 0; h2 < HK; ++h2) ok = ok && wait(&full[st0 + h2], ph0);
+      if (!ok) break;
       if (p >= NWD && !wait(&wd_empty[buf], (p / NWD - 1) & 1)) break;
       fence_after_sync();  // the MMAs that read this buffer's tensor memory are complete
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
+      for (int h2 = 0; h2 < HK; ++h2) {
         uint32_t w[16];
-        dequant32(raw + (size_t)((j0 + h2) % STAGES) * RAW_BYTES + X_BYTES + n * 32 + h * 16, bf16pair_to_h2(cs[h2]),
-                  bf16pair_to_h2(cb[h2]), w);
-        tmem_st16(tmem + a_lane + (uint32_t)(2 * TT + buf * A_COLS + h2 * (A_COLS / 2) + h * 16), w);
+        const uint32_t sw = cs[h2 / 2], bw = cb[h2 / 2];
+        dequant32(raw + (size_t)(st0 + h2) * RAW_BYTES + X_BYTES + n * 32 + h * 16,
+                  bf16pair_to_h2((uint16_t)(sw >> (16 * (h2 & 1)))), bf16pair_to_h2((uint16_t)(bw >> (16 * (h2 & 1)))),
+                  w);
+        tmem_st16(tmem + a_lane + (uint32_t)(2 * TT + buf * A_COLS + h2 * (BK / 2) + h * 16), w);
       }
-      // token rows of both k-blocks into the hand-over buffer (16-byte chunks keep their
+      // token rows of the k-blocks into the hand-over buffer (16-byte chunks keep their
       // swizzled places; the MMA reads the tile's rows rounded up to 16)
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const uint4* src = reinterpret_cast<const uint4*>(raw + (size_t)((j0 + h2) % STAGES) * RAW_BYTES);
+      for (int h2 = 0; h2 < HK; ++h2) {
+        const uint4* src = reinterpret_cast<const uint4*>(raw + (size_t)(st0 + h2) * RAW_BYTES);
         uint4* dst = reinterpret_cast<uint4*>(hbuf + (size_t)buf * HB_BYTES + (size_t)h2 * X_BYTES);
         for (int c = gtid; c < x_bytes / 16; c += 32 * N_DQG) dst[c] = src[c];
       }
@@ -319,17 +343,22 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&wd_full[buf]);
-        mbar_arrive(&empty[j0 % STAGES]);  // this warp is done with both copy stages
-        mbar_arrive(&empty[(j0 + 1) % STAGES]);
+#pragma unroll
+        for (int h2 = 0; h2 < HK; ++h2) mbar_arrive(&empty[st0 + h2]);  // this warp is done with the stages
       }
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < HK / 2; ++u) {
         cs[u] = ns[u];
         cb[u] = nb[u];
         ns[u] = ms[u];
         nb[u] = mb[u];
       }
       fetch(p + 3 * DQ_GROUPS, ms, mb);
+      st0 += HK * DQ_GROUPS;  // the group's next hand-over
+      while (st0 >= STAGES) {
+        st0 -= STAGES;
+        ph0 ^= 1u;
+      }
     }
   } else if (warp == W_MMA) {
     // ---------------- the MMA warp: every lane walks the hand-overs (operand addresses
@@ -337,8 +366,8 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
     int cur_i = -1;
     Tile T{};
     uint32_t idesc = 0;
-    for (int p = 0; 2 * p < jobs; ++p) {
-      const int j0 = 2 * p, kb = j0 % KB, buf = p % NWD;
+    for (int p = 0; HK * p < jobs; ++p) {
+      const int j0 = HK * p, kb = j0 % KB, buf = p % NWD;
       const int i = j0 / KB, ab = i & 1;
       if (i != cur_i) {
         cur_i = i;
@@ -351,8 +380,8 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
       fence_after_sync();
       if (elect_one()) {
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const uint32_t a_col = tmem + (uint32_t)(2 * TT + buf * A_COLS + h2 * (A_COLS / 2));
+        for (int h2 = 0; h2 < HK; ++h2) {
+          const uint32_t a_col = tmem + (uint32_t)(2 * TT + buf * A_COLS + h2 * (BK / 2));
           const uint64_t xd = sdesc_k128(smem_u32(hbuf + (size_t)buf * HB_BYTES + (size_t)h2 * X_BYTES));
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)  // a 16-wide k step: 8 columns of A, 32 bytes of B
@@ -360,7 +389,7 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
                        kb > 0 || h2 > 0 || kk > 0);
         }
         commit(&wd_empty[buf]);
-        if (kb + 2 == KB) commit(&acc_full[ab]);
+        if (kb + HK == KB) commit(&acc_full[ab]);
       }
       __syncwarp();
     }
@@ -729,17 +758,32 @@ PfLayout pf_layout(int d, int E, int F, int K, int T, int out, bool shared, bool
 int g_num_sms = 0;
 std::once_flag g_sm_once;
 
-template <int LAYOUT, int EPI>
-cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
+template <int LAYOUT, int EPI, int HK>
+cudaError_t launch_gemm_hk(const GemmArgs& a, cudaStream_t st) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_q4_kernel<LAYOUT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)GEMM_SMEM);
+    attr_err = cudaFuncSetAttribute(gemm_q4_kernel<LAYOUT, EPI, HK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)Cfg<HK>::SMEM);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  gemm_q4_kernel<LAYOUT, EPI><<<g_num_sms, GT, GEMM_SMEM, st>>>(a);
+  gemm_q4_kernel<LAYOUT, EPI, HK><<<g_num_sms, GT, Cfg<HK>::SMEM, st>>>(a);
   return cudaGetLastError();
+}
+
+// Four k-blocks per hand-over when the reduction length allows it.  The rows layout
+// always reduces over d (a multiple of 256: 4 k-blocks divide it); the column-slab layout
+// reduces over F (a multiple of 128).
+template <int LAYOUT, int EPI>
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
+  const int KB = a.K / BK;
+  if constexpr (LAYOUT == E0_LAYOUT_ROWS) {
+    if (KB % 4 != 0) return cudaErrorInvalidValue;
+    return launch_gemm_hk<LAYOUT, EPI, 4>(a, st);
+  } else {
+    if (KB % 4 == 0) return launch_gemm_hk<LAYOUT, EPI, 4>(a, st);
+    return launch_gemm_hk<LAYOUT, EPI, 2>(a, st);
+  }
 }
 
 }  // namespace e0pf
@@ -792,6 +836,13 @@ e0_status e0pf_grouped_layer(const e0_dims* dims, const e0_experts* routed, cons
              "e0_moe_prefill_layer: the LoRA B^T matrix must be 8-byte aligned");
   E0_REQUIRE(!has_lora || !lora->a || al16p(lora->a), E0_ERR_INVALID,
              "e0_moe_prefill_layer: the LoRA A matrix must be 16-byte aligned");
+  {
+    // the codes are copied and the scales read with vector accesses
+    auto al_q4 = [](const e0_q4& m) { return al16p(m.q) && al16p(m.scale) && al16p(m.bias); };
+    E0_REQUIRE(al_q4(routed->gate_up) && al_q4(routed->down) &&
+                   (!has_shared || (al_q4(shared->gate_up) && al_q4(shared->down))) && (!has_lora || al_q4(lora->w)),
+               E0_ERR_INVALID, "e0_moe_prefill_layer: int4 codes, scales and biases must be 16-byte aligned");
+  }
   const PfLayout L = pf_layout(d, E, F, K, T, out, true, has_lora);
   E0_REQUIRE(workspace_bytes >= L.total, E0_ERR_NOMEM, "e0_moe_prefill_layer: workspace too small");
   std::call_once(g_sm_once, [] {
