@@ -649,6 +649,7 @@ __global__ void __launch_bounds__(256) lora_a_kernel(const uint16_t* h, const fl
   const int t = gw / groups, q0 = (gw % groups) * LA_RANKS;
   float s[LA_RANKS] = {};
   const uint4* hp = reinterpret_cast<const uint4*>(h + (size_t)t * d);
+#pragma unroll 4
   for (int c = lane; c < d / 8; c += 32) {
     const uint4 hv = __ldg(hp + c);
     const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
@@ -673,52 +674,58 @@ __global__ void __launch_bounds__(256) lora_a_kernel(const uint16_t* h, const fl
 
 // h_out = bf16(h + sum_k y_(t,k) + y_shared + y_lora), the pairs summed in k order, with
 // y_lora = W_int4 x + (alpha/r) B v (the LoRA up projection formed here from v).  A thread
-// owns 4 adjacent outputs (16-byte loads) of CT tokens; B^T's rows stay in L1 across them.
-constexpr int CT = 4;
+// owns 4 adjacent outputs of one token (16-byte loads); the pair rows' indices are read
+// first so that all K row loads are in flight together.
+constexpr int CK = 16;  // K at most
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* h, int T, int d, int K, const int* inv,
                                                       const float* yslot, const float* ys, const float* yl,
                                                       const float* v, const uint16_t* bt, int r, float lscale,
                                                       uint16_t* h_out, float* delta) {
-  __shared__ float vs[CT][e0eng::RANKS_MAX];
-  const int t0 = blockIdx.y * CT, nt = min(CT, T - t0);
+  __shared__ float vs[e0eng::RANKS_MAX];
+  __shared__ int rows[CK];
+  const int t = blockIdx.x;
   const int nv = v ? r : 0;
-  for (int i = threadIdx.x; i < nt * nv; i += blockDim.x) vs[i / nv][i % nv] = v[(size_t)t0 * nv + i];
+  for (int i = threadIdx.x; i < nv; i += blockDim.x) vs[i] = v[(size_t)t * nv + i];
+  if (threadIdx.x < K) rows[threadIdx.x] = inv[t * K + threadIdx.x];
   __syncthreads();
-  const int i0 = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
+  const int i0 = 4 * (blockIdx.y * blockDim.x + threadIdx.x);
   if (i0 >= d) return;
-  for (int u = 0; u < nt; ++u) {
-    const int t = t0 + u;
-    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = 0; k < K; ++k) {
-      const float4 y = __ldg(reinterpret_cast<const float4*>(yslot + (size_t)inv[t * K + k] * d + i0));
-      s.x += y.x; s.y += y.y; s.z += y.z; s.w += y.w;
+  float4 y[CK];
+#pragma unroll
+  for (int k = 0; k < CK; ++k)
+    if (k < K) y[k] = __ldg(reinterpret_cast<const float4*>(yslot + (size_t)rows[k] * d + i0));
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < CK; ++k)
+    if (k < K) {
+      s.x += y[k].x; s.y += y[k].y; s.z += y[k].z; s.w += y[k].w;
     }
-    if (ys) {
-      const float4 y = __ldg(reinterpret_cast<const float4*>(ys + (size_t)t * d + i0));
-      s.x += y.x; s.y += y.y; s.z += y.z; s.w += y.w;
-    }
-    if (yl) {
-      float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int q = 0; q < nv; ++q) {
-        const uint2 bw = __ldg(reinterpret_cast<const uint2*>(bt + (size_t)q * d + i0));
-        const float vq = vs[u][q];
-        b.x = fmaf(__uint_as_float(bw.x << 16), vq, b.x);
-        b.y = fmaf(__uint_as_float(bw.x & 0xFFFF0000u), vq, b.y);
-        b.z = fmaf(__uint_as_float(bw.y << 16), vq, b.z);
-        b.w = fmaf(__uint_as_float(bw.y & 0xFFFF0000u), vq, b.w);
-      }
-      const float4 y = __ldg(reinterpret_cast<const float4*>(yl + (size_t)t * d + i0));
-      s.x += y.x + lscale * b.x; s.y += y.y + lscale * b.y; s.z += y.z + lscale * b.z; s.w += y.w + lscale * b.w;
-    }
-    if (delta) *reinterpret_cast<float4*>(delta + (size_t)t * d + i0) = s;
-    const uint2 hw = *reinterpret_cast<const uint2*>(h + (size_t)t * d + i0);
-    uint2 o;
-    o.x = (uint32_t)f32_to_bf16_bits(__uint_as_float(hw.x << 16) + s.x) |
-          ((uint32_t)f32_to_bf16_bits(__uint_as_float(hw.x & 0xFFFF0000u) + s.y) << 16);
-    o.y = (uint32_t)f32_to_bf16_bits(__uint_as_float(hw.y << 16) + s.z) |
-          ((uint32_t)f32_to_bf16_bits(__uint_as_float(hw.y & 0xFFFF0000u) + s.w) << 16);
-    *reinterpret_cast<uint2*>(h_out + (size_t)t * d + i0) = o;
+  if (ys) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(ys + (size_t)t * d + i0));
+    s.x += a.x; s.y += a.y; s.z += a.z; s.w += a.w;
   }
+  if (yl) {
+    float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int q = 0; q < nv; ++q) {
+      const uint2 bw = __ldg(reinterpret_cast<const uint2*>(bt + (size_t)q * d + i0));
+      const float vq = vs[q];
+      b.x = fmaf(__uint_as_float(bw.x << 16), vq, b.x);
+      b.y = fmaf(__uint_as_float(bw.x & 0xFFFF0000u), vq, b.y);
+      b.z = fmaf(__uint_as_float(bw.y << 16), vq, b.z);
+      b.w = fmaf(__uint_as_float(bw.y & 0xFFFF0000u), vq, b.w);
+    }
+    const float4 a = __ldg(reinterpret_cast<const float4*>(yl + (size_t)t * d + i0));
+    s.x += a.x + lscale * b.x; s.y += a.y + lscale * b.y; s.z += a.z + lscale * b.z; s.w += a.w + lscale * b.w;
+  }
+  if (delta) *reinterpret_cast<float4*>(delta + (size_t)t * d + i0) = s;
+  const uint2 hw = *reinterpret_cast<const uint2*>(h + (size_t)t * d + i0);
+  uint2 o;
+  o.x = (uint32_t)f32_to_bf16_bits(__uint_as_float(hw.x << 16) + s.x) |
+        ((uint32_t)f32_to_bf16_bits(__uint_as_float(hw.x & 0xFFFF0000u) + s.y) << 16);
+  o.y = (uint32_t)f32_to_bf16_bits(__uint_as_float(hw.y << 16) + s.z) |
+        ((uint32_t)f32_to_bf16_bits(__uint_as_float(hw.y & 0xFFFF0000u) + s.w) << 16);
+  *reinterpret_cast<uint2*>(h_out + (size_t)t * d + i0) = o;
 }
 
 // ------------------------------------------------------------------ workspace
@@ -930,7 +937,7 @@ e0_status e0pf_grouped_layer(const e0_dims* dims, const e0_experts* routed, cons
       E0_CHECK_CUDA(cudaGetLastError());
     }
   }
-  const dim3 cgrid((d / 4 + 255) / 256, (T + CT - 1) / CT);
+  const dim3 cgrid(T, (d / 4 + 255) / 256);
   combine_kernel<<<cgrid, 256, 0, st>>>(h_in, T, d, K, inv, yslot, ys, yl, lv, lv ? lora->bt : nullptr,
                                         lv ? lora->r : 0, lv ? lora->alpha / lora->r : 0.f, h_out, delta_f32);
   E0_CHECK_CUDA(cudaGetLastError());
