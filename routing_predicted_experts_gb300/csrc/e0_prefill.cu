@@ -45,6 +45,7 @@ constexpr int X_BYTES = TT * BK * 2;         // 8 KB of fp16 token rows
 constexpr int Q_BYTES = WM * BK / 2;         // 4 KB of int4 codes
 constexpr int RAW_BYTES = X_BYTES + Q_BYTES;
 constexpr int EMAXP = 1024;
+constexpr int MAXT = 256;  // tiles of a CTA whose placement is tabulated in shared memory
 // A hand-over carries the MMA's operands for HK k-blocks (HK = 4 when the reduction
 // length allows it, else 2): the dequantised weights (A) in tensor memory, 32 columns per
 // k-block (lane = weight row, two fp16 per column), and a copy of the token rows (B) in
@@ -57,7 +58,8 @@ struct Cfg {
   static constexpr int A_COLS = HK * BK / 2;             // tensor-memory columns of one hand-over
   static constexpr int HB_BYTES = HK * X_BYTES;          // token rows of one hand-over buffer
   static constexpr int TMEM_COLS = 2 * TT + NWD * A_COLS <= 256 ? 256 : 512;
-  static constexpr size_t SMEM = 1024 + (size_t)STAGES * RAW_BYTES + NWD * HB_BYTES + 2 * (EMAXP + 1) * sizeof(int);
+  static constexpr size_t SMEM =
+      1024 + (size_t)STAGES * RAW_BYTES + NWD * HB_BYTES + 2 * (EMAXP + 1) * sizeof(int) + MAXT * sizeof(uint2);
   static_assert(SMEM <= 227 * 1024, "shared memory");
   static_assert(STAGES % HK == 0, "a hand-over's stages sit in one ring pass");
   static_assert(2 * TT + NWD * A_COLS <= TMEM_COLS, "tensor memory columns");
@@ -155,6 +157,7 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
   uint8_t* hbuf = sm + (size_t)STAGES * RAW_BYTES;  // NWD x token rows of a hand-over
   int* s_row = reinterpret_cast<int*>(hbuf + NWD * HB_BYTES);
   int* s_tile = s_row + (EMAXP + 1);
+  uint2* s_tt = reinterpret_cast<uint2*>(s_tile + (EMAXP + 1));  // [MAXT] this CTA's tiles
   __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], wd_full[NWD], wd_empty[NWD], acc_full[2], acc_empty[2], fin;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int s_abort;
@@ -192,7 +195,7 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
   const int jobs = my_tiles * KB;
 
   // tile i of this CTA: token rows, weight rows and weight slot (group search in shared memory)
-  auto tile_of = [&](int i) -> Tile {
+  auto find_tile = [&](int i) -> Tile {
     const int t = (int)blockIdx.x + i * (int)gridDim.x;
     int lo = 0, hi = g.ngroups;  // s_tile[lo] * WT <= t < s_tile[hi] * WT
     while (hi - lo > 1) {
@@ -206,6 +209,23 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
     T.rows = min(TT, s_row[lo + 1] - T.m0);
     T.n0 = (local / tt_g) * WM;
     T.slot = lo;
+    return T;
+  };
+  // the first MAXT tiles tabulated once (every role looks tiles up, several times each):
+  // {m0, rows | n0 / WM << 8 | slot << 20}
+  for (int i = tid; i < my_tiles && i < MAXT; i += GT) {
+    const Tile T = find_tile(i);
+    s_tt[i] = make_uint2((uint32_t)T.m0, (uint32_t)T.rows | ((uint32_t)(T.n0 / WM) << 8) | ((uint32_t)T.slot << 20));
+  }
+  __syncthreads();
+  auto tile_of = [&](int i) -> Tile {
+    if (i >= MAXT) return find_tile(i);
+    const uint2 e = s_tt[i];
+    Tile T;
+    T.m0 = (int)e.x;
+    T.rows = (int)(e.y & 0xFFu);
+    T.n0 = (int)((e.y >> 8) & 0xFFFu) * WM;
+    T.slot = (int)(e.y >> 20);
     return T;
   };
   // bounded wait: false after an abort or once the time limit passes (sets the status)
@@ -428,13 +448,13 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
             }
           }
         } else {
+          // lane c brings the factor of token row c of the chunk
+          const float fl = g.rowscale && lane < nc ? g.rowscale[T.m0 + c0 + lane] : 1.0f;
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (c < nc) {
-              const int row = T.m0 + c0 + c;
-              const float f = g.rowscale ? g.rowscale[row] : 1.0f;
-              g.out32[(size_t)row * g.ldo + nout] = f * __uint_as_float(v[c]);
-            }
+          for (int c = 0; c < 32; ++c) {
+            const float f = __shfl_sync(0xffffffffu, fl, c);
+            if (c < nc) g.out32[(size_t)(T.m0 + c0 + c) * g.ldo + nout] = f * __uint_as_float(v[c]);
+          }
         }
       }
       fence_before_sync();
