@@ -75,7 +75,7 @@ constexpr int DQ_GROUPS = 2, N_DQG = N_DQ / DQ_GROUPS;
 constexpr int GT = 32 * (W_EPI0 + N_EPI);
 static_assert(X_BYTES % 1024 == 0 && RAW_BYTES % 1024 == 0, "stages stay 1024-byte aligned");
 static_assert(N_DQG == 8 && WM == 128 && W_DQ0 % 4 == 0, "two warps per lane quadrant in a group, one per half block");
-static_assert(NWD == DQ_GROUPS, "one hand-over buffer per dequantising group");
+static_assert(NWD == DQ_GROUPS && NWD == 2, "one hand-over buffer per dequantising group; p & 1 picks it");
 
 enum Epi : int { EPI_SWIGLU = 0, EPI_F32 = 1 };
 
@@ -135,6 +135,20 @@ __device__ __forceinline__ void dequant32(const uint8_t* codes, __half2 s2, __ha
     }
   }
 }
+
+// Position of a job (tile i, k-block kb) tracked as the job index advances, so that the
+// loops divide by the runtime k-block count only once.
+struct JobPos {
+  int i, kb;
+  __device__ __forceinline__ JobPos(int j, int KB) : i(j / KB), kb(j % KB) {}
+  __device__ __forceinline__ void advance(int n, int KB) {
+    kb += n;
+    while (kb >= KB) {
+      kb -= KB;
+      ++i;
+    }
+  }
+};
 
 __device__ __forceinline__ void cp_async_bar_arrive(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -249,14 +263,15 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
     // ---------------- copies: token rows and codes of job j into stage j % STAGES
     int cur_i = -1;
     Tile T{};
-    for (int j = warp - W_COPY; j < jobs; j += N_COPY) {
+    JobPos jp(warp - W_COPY, KB);
+    for (int j = warp - W_COPY; j < jobs; j += N_COPY, jp.advance(N_COPY, KB)) {
       const int st = j % STAGES, round = j / STAGES;
       if (round > 0 && !wait(&empty[st], (round - 1) & 1)) break;
-      if (j / KB != cur_i) {
-        cur_i = j / KB;
+      if (jp.i != cur_i) {
+        cur_i = jp.i;
         T = tile_of(cur_i);
       }
-      const int kb = j % KB;
+      const int kb = jp.kb;
       uint8_t* sx = raw + (size_t)st * RAW_BYTES;
       uint8_t* sq = sx + X_BYTES;
       for (int c = lane; c < T.rows * 8; c += 32) {
@@ -288,11 +303,14 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
     int t_i = -1;
     Tile tt{};
     using SW = uint32_t[HK / 2];
+    // the fetches come in order, p = grp, grp + 2, ...: their job position advances
+    JobPos fp(HK * grp, KB);
     auto fetch = [&](int p, SW& sv, SW& bv) {
 #pragma unroll
       for (int u = 0; u < HK / 2; ++u) sv[u] = bv[u] = 0u;
       if (HK * p >= jobs) return;
-      const int j0 = HK * p, i = j0 / KB, kb = j0 % KB;
+      const int i = fp.i, kb = fp.kb;
+      fp.advance(HK * DQ_GROUPS, KB);
       if (i != t_i) {
         t_i = i;
         tt = tile_of(i);
@@ -327,17 +345,18 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
     int x_i = -1, x_bytes = X_BYTES;  // token-row bytes to hand over: the tile's rows rounded to 16
     int st0 = (HK * grp) % STAGES;      // first stage of hand-over p, and its ring pass
     uint32_t ph0 = (uint32_t)((HK * grp) / STAGES) & 1u;
-    for (int p = grp; HK * p < jobs; p += DQ_GROUPS) {
-      const int j0 = HK * p, buf = p % NWD;  // this group's buffer: p % NWD == grp
-      if (j0 / KB != x_i) {
-        x_i = j0 / KB;
+    JobPos hp(HK * grp, KB);  // this hand-over's first job
+    for (int p = grp; HK * p < jobs; p += DQ_GROUPS, hp.advance(HK * DQ_GROUPS, KB)) {
+      const int buf = p & (NWD - 1);  // this group's buffer: p % NWD == grp
+      if (hp.i != x_i) {
+        x_i = hp.i;
         x_bytes = ((tile_of(x_i).rows + 15) & ~15) * 128;
       }
       bool ok = true;
 #pragma unroll
       for (int h2 = 0; h2 < HK; ++h2) ok = ok && wait(&full[st0 + h2], ph0);
       if (!ok) break;
-      if (p >= NWD && !wait(&wd_empty[buf], (p / NWD - 1) & 1)) break;
+      if (p >= NWD && !wait(&wd_empty[buf], ((p >> 1) - 1) & 1)) break;
       fence_after_sync();  // the MMAs that read this buffer's tensor memory are complete
 #pragma unroll
       for (int h2 = 0; h2 < HK; ++h2) {
@@ -386,9 +405,10 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
     int cur_i = -1;
     Tile T{};
     uint32_t idesc = 0;
-    for (int p = 0; HK * p < jobs; ++p) {
-      const int j0 = HK * p, kb = j0 % KB, buf = p % NWD;
-      const int i = j0 / KB, ab = i & 1;
+    JobPos mp(0, KB);
+    for (int p = 0; HK * p < jobs; ++p, mp.advance(HK, KB)) {
+      const int kb = mp.kb, buf = p & (NWD - 1);
+      const int i = mp.i, ab = i & 1;
       if (i != cur_i) {
         cur_i = i;
         T = tile_of(i);
@@ -396,7 +416,7 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
         // the epilogue is done with this accumulator
         if (!__all_sync(0xffffffffu, i < 2 || wait(&acc_empty[ab], ((i >> 1) - 1) & 1))) break;
       }
-      if (!__all_sync(0xffffffffu, wait(&wd_full[buf], (p / NWD) & 1))) break;
+      if (!__all_sync(0xffffffffu, wait(&wd_full[buf], (p >> 1) & 1))) break;
       fence_after_sync();
       if (elect_one()) {
 #pragma unroll
