@@ -101,11 +101,6 @@ struct Tile {
   int m0, rows, n0, slot;
 };
 
-__device__ __forceinline__ __half2 bf16pair_to_h2(uint16_t v) {
-  const __half h = __float2half_rn(__uint_as_float((uint32_t)v << 16));
-  return __halves2half2(h, h);
-}
-
 // Dequantise 32 codes (one uint4: half of a 64-code weight row segment) to 16 fp16 pairs:
 // codes j and j + 4 of each 8-code word become one pair, which is the element order
 // [0,4,1,5,2,6,3,7] within every group of 8 that the token rows use as well.  A pair is
@@ -264,8 +259,12 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
     int cur_i = -1;
     Tile T{};
     JobPos jp(warp - W_COPY, KB);
+    int st = (warp - W_COPY) % STAGES, round = (warp - W_COPY) / STAGES;
+    // lane roles: 16-byte chunk ch of token rows r0, r0 + 4, ... (chunk stored at ch ^ (r % 8));
+    // code row (lane >> 1) + 16 m, half lane & 1
+    const int ch = lane & 7, r0 = lane >> 3, qn = lane >> 1, qh = lane & 1;
+    const uint32_t xsw0 = (uint32_t)((ch ^ r0) << 4), xsw1 = (uint32_t)((ch ^ (r0 + 4)) << 4);
     for (int j = warp - W_COPY; j < jobs; j += N_COPY, jp.advance(N_COPY, KB)) {
-      const int st = j % STAGES, round = j / STAGES;
       if (round > 0 && !wait(&empty[st], (round - 1) & 1)) break;
       if (jp.i != cur_i) {
         cur_i = jp.i;
@@ -274,21 +273,28 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
       const int kb = jp.kb;
       uint8_t* sx = raw + (size_t)st * RAW_BYTES;
       uint8_t* sq = sx + X_BYTES;
-      for (int c = lane; c < T.rows * 8; c += 32) {
-        const int r = c >> 3, ch = c & 7;
-        cp_async16(sx + r * 128 + ((ch ^ (r & 7)) << 4), g.A + (size_t)(T.m0 + r) * g.lda + kb * BK + ch * 8, 16u);
+      const __half* xsrc = g.A + (size_t)(T.m0 + r0) * g.lda + kb * BK + ch * 8;
+      const size_t xstep = (size_t)4 * g.lda;
+      uint8_t* xdst = sx + r0 * 128;
+      for (int r = r0, k = 0; r < T.rows; r += 4, ++k, xsrc += xstep, xdst += 4 * 128)
+        cp_async16(xdst + ((k & 1) ? xsw1 : xsw0), xsrc, 16u);
+      const uint32_t* qsrc;
+      size_t qstep;
+      if (LAYOUT == E0_LAYOUT_ROWS) {
+        qsrc = g.q + ((size_t)T.slot * g.N + T.n0 + qn) * (g.K / 8) + kb * 8 + qh * 4;
+        qstep = (size_t)16 * (g.K / 8);
+      } else {
+        qsrc = g.q + (((size_t)T.slot * (g.K / 32) + 2 * kb + qh) * g.N + T.n0 + qn) * 4;
+        qstep = 16 * 4;
       }
 #pragma unroll
-      for (int c = lane; c < WM * 2; c += 32) {
-        const int n = c >> 1, h = c & 1;
-        const uint32_t* src;
-        if (LAYOUT == E0_LAYOUT_ROWS)
-          src = g.q + ((size_t)T.slot * g.N + T.n0 + n) * (g.K / 8) + kb * 8 + h * 4;
-        else
-          src = g.q + ((size_t)T.slot * (g.K / 32) + 2 * kb + h) * (size_t)g.N * 4 + (size_t)(T.n0 + n) * 4;
-        cp_async16(sq + n * 32 + h * 16, src, 16u);
-      }
+      for (int m = 0; m < WM * 2 / 32; ++m) cp_async16(sq + (qn + 16 * m) * 32 + qh * 16, qsrc + m * qstep, 16u);
       cp_async_bar_arrive(&full[st]);  // completes when this lane's copies have landed
+      st += N_COPY;
+      if (st >= STAGES) {
+        st -= STAGES;
+        ++round;
+      }
     }
     cp_async_wait<0>();
   } else if (warp >= W_DQ0 && warp < W_DQ0 + N_DQ) {
@@ -358,13 +364,19 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
       if (!ok) break;
       if (p >= NWD && !wait(&wd_empty[buf], ((p >> 1) - 1) & 1)) break;
       fence_after_sync();  // the MMAs that read this buffer's tensor memory are complete
+      // the scales and biases of two k-blocks at a time to fp16 (one packing conversion)
+      __half2 sp[HK / 2], bp[HK / 2];
+#pragma unroll
+      for (int u = 0; u < HK / 2; ++u) {
+        sp[u] = __floats2half2_rn(__uint_as_float(cs[u] << 16), __uint_as_float(cs[u] & 0xFFFF0000u));
+        bp[u] = __floats2half2_rn(__uint_as_float(cb[u] << 16), __uint_as_float(cb[u] & 0xFFFF0000u));
+      }
 #pragma unroll
       for (int h2 = 0; h2 < HK; ++h2) {
         uint32_t w[16];
-        const uint32_t sw = cs[h2 / 2], bw = cb[h2 / 2];
-        dequant32(raw + (size_t)(st0 + h2) * RAW_BYTES + X_BYTES + n * 32 + h * 16,
-                  bf16pair_to_h2((uint16_t)(sw >> (16 * (h2 & 1)))), bf16pair_to_h2((uint16_t)(bw >> (16 * (h2 & 1)))),
-                  w);
+        const __half2 s2 = (h2 & 1) ? __high2half2(sp[h2 / 2]) : __low2half2(sp[h2 / 2]);
+        const __half2 b2 = (h2 & 1) ? __high2half2(bp[h2 / 2]) : __low2half2(bp[h2 / 2]);
+        dequant32(raw + (size_t)(st0 + h2) * RAW_BYTES + X_BYTES + n * 32 + h * 16, s2, b2, w);
         tmem_st16(tmem + a_lane + (uint32_t)(2 * TT + buf * A_COLS + h2 * (BK / 2) + h * 16), w);
       }
       // token rows of the k-blocks into the hand-over buffer (16-byte chunks keep their
