@@ -418,7 +418,10 @@ e0_status e0_stage_slots(e0_slot_pool* pool, const int32_t* layers, int32_t n_la
                          const int32_t* next_ids, const int32_t* rows, int32_t K, uint32_t tag,
                          e0_stream copy_stream, e0_event after, e0_stage_stats* stats);
 /* The same with HOST ids [n_layers][K]: priming a pool before the first token (whose
- * routing no head committed) or a routing the host already knows. */
+ * routing no head committed) or a routing the host already knows.  The slots a staging
+ * may overwrite are those of neither this staging nor the previous one of the layer:
+ * pass as `after` the last launch that may read such a slot (NULL only when none is
+ * still queued or running). */
 e0_status e0_stage_slots_host(e0_slot_pool* pool, const int32_t* layers, int32_t n_layers,
                               const int32_t* ids, int32_t K, uint32_t tag, e0_stream copy_stream,
                               e0_event after, e0_stage_stats* stats);
