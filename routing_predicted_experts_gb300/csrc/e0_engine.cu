@@ -828,15 +828,6 @@ __device__ __forceinline__ void prefetch_layer(Prod& pr, int l) {
   const EngineParams& P = pr.P;
   if (l >= P.L || !pr.ok) return;
   const LayerDesc& Ld = layer_at(P, l);
-  // this CTA's gate rows on the layer's input (its own gate, the gate it routes ahead)
-  const uint16_t* gates[2] = {gate_here(P, l) ? Ld.router : nullptr,
-                              P.mode == MODE_STACK && Ld.gate_for >= 0 ? layer_at(P, Ld.gate_for).router : nullptr};
-  int nr;
-  const Unit* rs = units_of(P, KIND_ROUTER, blockIdx.x, nr);
-  for (int g = 0; g < 2; ++g)
-    if (gates[g])
-      for (int i = 0; i < nr && i < 32; ++i)
-        if (pr.lane == i) l2_prefetch(gates[g] + (size_t)rs[i].r0 * P.d, (uint32_t)(rs[i].r1 - rs[i].r0) * P.d * 2);
   int nu;
   const Unit* us = units_of(P, P.plan ? Ld.plan_kind : 0, blockIdx.x, nu);
   for (int i = 0; i < nu; ++i) prefetch_unit(pr, Ld, us[i], l);
