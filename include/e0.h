@@ -194,8 +194,9 @@ e0_status e0_get_device_status(const void* workspace, uint32_t* status_out, e0_s
  *   logit_bias: fp32 [E] added to the logits before top-K (nullable).
  *   logits_out fp32 [T][E]; ids_out int32 [T][K] (descending, ties -> lower id);
  *   weights_out fp32 [T][K] renormalised softmax over ids_out (nullable).
- *   T > 1 (at most 16) reads each head weight row once for all tokens; the workspace
- *   must then be 256-byte aligned and hold e0_decode_workspace_size(dims, T, 0, H).
+ *   T > 1 (at most 16) reads each head weight row once for all tokens; h must then be
+ *   16-byte aligned and the workspace 256-byte aligned, holding
+ *   e0_decode_workspace_size(dims, T, 0, H).
  * ------------------------------------------------------------------------------ */
 e0_status e0_prerouter_forward(const e0_prerouter* head, int32_t d, int32_t E,
                                const uint16_t* h, const int32_t* ids_cur,

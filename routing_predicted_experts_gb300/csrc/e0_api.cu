@@ -627,6 +627,7 @@ extern "C" e0_status e0_prerouter_forward(const e0_prerouter* head, int32_t d, i
     E0_REQUIRE(T <= 16, E0_ERR_SHAPE, "e0_prerouter_forward: T must be <= 16");
     E0_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, E0_ERR_INVALID,
                "workspace must be 256-byte aligned");
+    E0_REQUIRE(al16(h), E0_ERR_INVALID, "e0_prerouter_forward: h must be 16-byte aligned for T > 1");
     E0_REQUIRE(workspace_bytes >= 256 + e0mt_head_scratch(&dm, T, head->H), E0_ERR_NOMEM,
                "workspace smaller than e0_decode_workspace_size(dims, T, 0, H)");
     uint8_t* ws = static_cast<uint8_t*>(workspace);

@@ -23,7 +23,7 @@ namespace e0mt {
 
 constexpr int TMAX = 16;        // tokens per call
 constexpr int ROWS_WARPS = 8;   // warps per CTA of rows_kernel
-constexpr int FC2_ROWS = 32;    // fc1 rows per CTA of fc2_kernel
+constexpr int FC2_ROWS = 16;    // fc1 rows per CTA of fc2_kernel
 
 __device__ __forceinline__ float bflo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bfhi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
@@ -35,9 +35,16 @@ __global__ void norm_kernel(const uint16_t* h, int d, int T, float* sc) {
   const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (t >= T) return;
   float ss = 0.f;
-  for (int i = lane; i < d; i += 32) {
-    const float v = bf(h[(size_t)t * d + i]);
-    ss += v * v;
+  const uint4* hp = reinterpret_cast<const uint4*>(h + (size_t)t * d);  // d is a multiple of 256
+  for (int c = lane; c < d / 8; c += 32) {
+    const uint4 v = hp[c];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const float a = bflo(w[m]), b = bfhi(w[m]);
+      ss = fmaf(a, a, ss);
+      ss = fmaf(b, b, ss);
+    }
   }
   ss = warp_sum(ss);
   if (lane == 0) sc[t] = rsqrtf(ss / (float)d + e0eng::RMS_EPS);
@@ -55,7 +62,7 @@ __device__ __forceinline__ float dot8(const uint4 w, const uint4 x) {
 }
 
 // Rows r < H of fc1's hidden block and rows H + e of the linear residual, against TP
-// token slots (tokens T..TP-1 are zero).  A warp takes two rows at a time; lane L owns
+// token slots (tokens T..TP-1 are zero).  A warp takes one row at a time; lane L owns
 // the 8 columns 8 L + 256 j, so a row is read with 16-byte loads, once.
 //   u[t][r] = x_t . W1h[r];   z[t][e] = x_t . Lres[e] + b2[e] + bias[e]
 template <int TP>
@@ -75,42 +82,27 @@ __global__ void __launch_bounds__(32 * ROWS_WARPS) rows_kernel(const uint16_t* h
   __syncthreads();
   const int R = H + E;
   const int nchunks = d / 256;
-  for (int pair = blockIdx.x * ROWS_WARPS + warp; 2 * pair < R; pair += gridDim.x * ROWS_WARPS) {
-    const int r0 = 2 * pair, r1 = r0 + 1;
-    const uint16_t* w0 = r0 < H ? w1h + (size_t)r0 * d : lres + (size_t)(r0 - H) * d;
-    const uint16_t* w1 = r1 < R ? (r1 < H ? w1h + (size_t)r1 * d : lres + (size_t)(r1 - H) * d) : nullptr;
-    float a0[TP], a1[TP];
+  for (int r = blockIdx.x * ROWS_WARPS + warp; r < R; r += gridDim.x * ROWS_WARPS) {
+    const uint16_t* w0 = r < H ? w1h + (size_t)r * d : lres + (size_t)(r - H) * d;
+    float a0[TP];
 #pragma unroll
-    for (int t = 0; t < TP; ++t) a0[t] = a1[t] = 0.f;
+    for (int t = 0; t < TP; ++t) a0[t] = 0.f;
     for (int j = 0; j < nchunks; ++j) {
       const int c = lane + 32 * j;  // 16-byte chunk index
       const uint4 q0 = __ldg(reinterpret_cast<const uint4*>(w0) + c);
-      const uint4 q1 = w1 ? __ldg(reinterpret_cast<const uint4*>(w1) + c) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-      for (int t = 0; t < TP; ++t) {
-        const uint4 x = reinterpret_cast<const uint4*>(hs + (size_t)t * d)[c];
-        a0[t] += dot8(q0, x);
-        a1[t] += dot8(q1, x);
-      }
+      for (int t = 0; t < TP; ++t) a0[t] += dot8(q0, reinterpret_cast<const uint4*>(hs + (size_t)t * d)[c]);
     }
 #pragma unroll
-    for (int t = 0; t < TP; ++t) {
-      a0[t] = warp_sum(a0[t]);
-      a1[t] = warp_sum(a1[t]);
-    }
+    for (int t = 0; t < TP; ++t) a0[t] = warp_sum(a0[t]);
     if (lane == 0) {
       for (int t = 0; t < T; ++t) {
-#pragma unroll
-        for (int s = 0; s < 2; ++s) {
-          const int r = s ? r1 : r0;
-          if (r >= R) continue;
-          const float v = (s ? a1[t] : a0[t]) * sc[t];
-          if (r < H) {
-            u[(size_t)t * H + r] = v;
-          } else {
-            const int e = r - H;
-            z[(size_t)t * E + e] = v + (b2 ? bf(b2[e]) : 0.f) + (bias ? bias[e] : 0.f);
-          }
+        const float v = a0[t] * sc[t];
+        if (r < H) {
+          u[(size_t)t * H + r] = v;
+        } else {
+          const int e = r - H;
+          z[(size_t)t * E + e] = v + (b2 ? bf(b2[e]) : 0.f) + (bias ? bias[e] : 0.f);
         }
       }
     }
@@ -205,8 +197,7 @@ cudaError_t launch_rows(const uint16_t* h, int d, int T, const float* sc, const 
   const size_t smem = (size_t)TP * d * sizeof(uint16_t);
   cudaError_t e = cudaFuncSetAttribute(rows_kernel<TP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int pairs = (hd->H + E + 1) / 2;
-  const int grid = (pairs + ROWS_WARPS - 1) / ROWS_WARPS;
+  const int grid = (hd->H + E + ROWS_WARPS - 1) / ROWS_WARPS;
   rows_kernel<TP><<<grid, 32 * ROWS_WARPS, smem, st>>>(h, d, T, sc, hd->w1h, hd->H, hd->lres, E, hd->b2, bias, u,
                                                        z);
   return cudaGetLastError();

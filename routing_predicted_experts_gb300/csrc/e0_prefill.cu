@@ -689,20 +689,19 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* h, int d, i
   }
 }
 
-// LoRA down projection v[t][q] = xscale_t * (A_q . h_t) (= A x_t, fp32): one warp per
-// token and group of four ranks, the token's row read once for all four.
+// LoRA down projection v[t][q] = xscale_t * (A_q . h_t) (= A x_t, fp32): one CTA per
+// token and group of four ranks, its eight warps splitting the row (one 16-byte chunk
+// per lane and pass), partial sums combined in shared memory.
 constexpr int LA_RANKS = 4;
 __global__ void __launch_bounds__(256) lora_a_kernel(const uint16_t* h, const float* xscale, int T, int d,
                                                      const uint16_t* a, int r, float* v) {
-  const int lane = threadIdx.x & 31;
-  const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  __shared__ float part[8][LA_RANKS];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int groups = (r + LA_RANKS - 1) / LA_RANKS;
-  if (gw >= T * groups) return;  // warp-uniform
-  const int t = gw / groups, q0 = (gw % groups) * LA_RANKS;
+  const int t = blockIdx.x / groups, q0 = (blockIdx.x % groups) * LA_RANKS;
   float s[LA_RANKS] = {};
   const uint4* hp = reinterpret_cast<const uint4*>(h + (size_t)t * d);
-#pragma unroll 4
-  for (int c = lane; c < d / 8; c += 32) {
+  for (int c = threadIdx.x; c < d / 8; c += blockDim.x) {
     const uint4 hv = __ldg(hp + c);
     const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
 #pragma unroll
@@ -720,7 +719,13 @@ __global__ void __launch_bounds__(256) lora_a_kernel(const uint16_t* h, const fl
 #pragma unroll
   for (int u = 0; u < LA_RANKS; ++u) {
     const float w = warp_sum(s[u]);
-    if (lane == 0 && q0 + u < r) v[(size_t)t * r + q0 + u] = w * xscale[t];
+    if (lane == 0) part[warp][u] = w;
+  }
+  __syncthreads();
+  if (threadIdx.x < LA_RANKS && q0 + (int)threadIdx.x < r) {
+    float tot = 0.f;
+    for (int w = 0; w < 8; ++w) tot += part[w][threadIdx.x];
+    v[(size_t)t * r + q0 + threadIdx.x] = tot * xscale[t];
   }
 }
 
@@ -984,8 +989,8 @@ e0_status e0pf_grouped_layer(const e0_dims* dims, const e0_experts* routed, cons
     E0_CHECK_CUDA((launch_gemm<E0_LAYOUT_ROWS, EPI_F32>(g, st)));
     if (lora->r > 0 && lora->a && lora->bt) {
       lv = (float*)P(L.lv);
-      const int warps = T * ((lora->r + LA_RANKS - 1) / LA_RANKS);
-      lora_a_kernel<<<(warps + 7) / 8, 256, 0, st>>>(h_in, xscale, T, d, lora->a, lora->r, lv);
+      lora_a_kernel<<<T * ((lora->r + LA_RANKS - 1) / LA_RANKS), 256, 0, st>>>(h_in, xscale, T, d, lora->a, lora->r,
+                                                                                 lv);
       E0_CHECK_CUDA(cudaGetLastError());
     }
   }
