@@ -54,3 +54,26 @@ def test_routing_family_parameters_are_checked_without_gpu():
     unknown = _lib.e0_dims(256, 64, 128, 8, 5, 0, 0, 0.0, None)
     assert lib.e0_moe_decode_layer(unknown, None, None, None, None, None, None, None, None, 1, None, None, None, None,
                                    None, None, 0, None) == _lib.E0_ERR_UNSUPPORTED
+
+
+def test_misaligned_prefill_weights_are_refused_without_gpu():
+    """The grouped path copies codes and reads scales with vector accesses: int4 arrays that
+    are not 16-byte aligned come back as an argument error before any CUDA call."""
+    lib = _lib.lib()
+    dm = _lib.e0_dims(256, 16, 128, 4)
+    base = 1 << 20  # never dereferenced: the call returns at the argument checks
+
+    def q4(off):
+        return _lib.e0_q4(base + off, base + 4096 + off, base + 8192 + off)
+
+    good = _lib.e0_experts(q4(0), q4(0), 16, None, 0, None)
+    bad = _lib.e0_experts(_lib.e0_q4(base, base + 4098, base + 8192), q4(0), 16, None, 0, None)
+    def call(experts, ws_bytes):
+        # h_in, logits, T, h_out, delta, ids_out, weights_out, workspace, bytes, stream
+        return lib.e0_moe_prefill_layer(dm, experts, None, None, base, base, 4, base, None, None, None, base, ws_bytes,
+                                        None)
+
+    assert call(bad, 1 << 30) == _lib.E0_ERR_INVALID
+    assert b"aligned" in lib.e0_last_error()
+    # with aligned weights the checks go on to the workspace size (none given here)
+    assert call(good, 0) == -5  # E0_ERR_NOMEM
