@@ -59,7 +59,7 @@ struct Cfg {
   static constexpr int HB_BYTES = HK * X_BYTES;          // token rows of one hand-over buffer
   static constexpr int TMEM_COLS = 2 * TT + NWD * A_COLS <= 256 ? 256 : 512;
   static constexpr size_t SMEM =
-      1024 + (size_t)STAGES * RAW_BYTES + NWD * HB_BYTES + 2 * (EMAXP + 1) * sizeof(int) + MAXT * sizeof(uint2);
+      1024 + (size_t)STAGES * RAW_BYTES + NWD * HB_BYTES + 2 * (EMAXP + 2) * sizeof(int) + MAXT * sizeof(uint2);
   static_assert(SMEM <= 227 * 1024, "shared memory");
   static_assert(STAGES % HK == 0, "a hand-over's stages sit in one ring pass");
   static_assert(2 * TT + NWD * A_COLS <= TMEM_COLS, "tensor memory columns");
@@ -93,10 +93,23 @@ struct GemmArgs {
   float* out32;           // EPI_F32: [rows][N]
   int ldo;
   const float* rowscale;  // EPI_F32: factor per row (nullable)
+  // one extra group after the ngroups (the shared expert), xrows > 0: its own token rows
+  // A2 [xrows][K] (same lda), weights q2/s2/b2 (one expert) and outputs out16b/out32b
+  // [xrows][...] (same ldo, no row factor), so that its tiles share the launch
+  int xrows;
+  const __half* A2;
+  const uint32_t* q2;
+  const uint16_t* s2;
+  const uint16_t* b2;
+  __half* out16b;
+  float* out32b;
   uint32_t* status;
   uint64_t timeout_ns;
 };
 
+// A tile: rows [m0, m0 + rows) of its group's token rows (of A, or of A2 for the extra
+// group, counted from 0 there), weight rows [n0, n0 + WM) of weight slot `slot`
+// (slot == ngroups: the extra group).
 struct Tile {
   int m0, rows, n0, slot;
 };
@@ -165,8 +178,8 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
   uint8_t* raw = sm;                                // STAGES x [token rows | codes]
   uint8_t* hbuf = sm + (size_t)STAGES * RAW_BYTES;  // NWD x token rows of a hand-over
   int* s_row = reinterpret_cast<int*>(hbuf + NWD * HB_BYTES);
-  int* s_tile = s_row + (EMAXP + 1);
-  uint2* s_tt = reinterpret_cast<uint2*>(s_tile + (EMAXP + 1));  // [MAXT] this CTA's tiles
+  int* s_tile = s_row + (EMAXP + 2);
+  uint2* s_tt = reinterpret_cast<uint2*>(s_tile + (EMAXP + 2));  // [MAXT] this CTA's tiles
   __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], wd_full[NWD], wd_empty[NWD], acc_full[2], acc_empty[2], fin;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int s_abort;
@@ -176,6 +189,11 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
   for (int i = tid; i <= g.ngroups; i += GT) {
     s_row[i] = g.row_off[i];
     s_tile[i] = g.tile_off[i];
+  }
+  const int ng = g.ngroups + (g.xrows > 0 ? 1 : 0);  // groups with the extra one
+  if (tid == 0 && g.xrows > 0) {
+    s_row[g.ngroups + 1] = g.row_off[g.ngroups] + g.xrows;
+    s_tile[g.ngroups + 1] = g.tile_off[g.ngroups] + (g.xrows + TT - 1) / TT;
   }
   if (tid == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -199,14 +217,14 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = tmem_slot;
-  const int total = s_tile[g.ngroups] * WT;
+  const int total = s_tile[ng] * WT;
   const int my_tiles = total > (int)blockIdx.x ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
   const int jobs = my_tiles * KB;
 
   // tile i of this CTA: token rows, weight rows and weight slot (group search in shared memory)
   auto find_tile = [&](int i) -> Tile {
     const int t = (int)blockIdx.x + i * (int)gridDim.x;
-    int lo = 0, hi = g.ngroups;  // s_tile[lo] * WT <= t < s_tile[hi] * WT
+    int lo = 0, hi = ng;  // s_tile[lo] * WT <= t < s_tile[hi] * WT
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
       if (s_tile[mid] * WT <= t) lo = mid; else hi = mid;
@@ -218,6 +236,7 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
     T.rows = min(TT, s_row[lo + 1] - T.m0);
     T.n0 = (local / tt_g) * WM;
     T.slot = lo;
+    if (lo == g.ngroups) T.m0 -= s_row[g.ngroups];  // the extra group's own rows
     return T;
   };
   // the first MAXT tiles tabulated once (every role looks tiles up, several times each):
@@ -273,7 +292,9 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
       const int kb = jp.kb;
       uint8_t* sx = raw + (size_t)st * RAW_BYTES;
       uint8_t* sq = sx + X_BYTES;
-      const __half* xsrc = g.A + (size_t)(T.m0 + r0) * g.lda + kb * BK + ch * 8;
+      const bool xt = T.slot == g.ngroups;  // the extra group: its own rows and weights
+      const int wslot = xt ? 0 : T.slot;
+      const __half* xsrc = (xt ? g.A2 : g.A) + (size_t)(T.m0 + r0) * g.lda + kb * BK + ch * 8;
       const size_t xstep = (size_t)4 * g.lda;
       uint8_t* xdst = sx + r0 * 128;
       for (int r = r0, k = 0; r < T.rows; r += 4, ++k, xsrc += xstep, xdst += 4 * 128)
@@ -281,10 +302,10 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
       const uint32_t* qsrc;
       size_t qstep;
       if (LAYOUT == E0_LAYOUT_ROWS) {
-        qsrc = g.q + ((size_t)T.slot * g.N + T.n0 + qn) * (g.K / 8) + kb * 8 + qh * 4;
+        qsrc = (xt ? g.q2 : g.q) + ((size_t)wslot * g.N + T.n0 + qn) * (g.K / 8) + kb * 8 + qh * 4;
         qstep = (size_t)16 * (g.K / 8);
       } else {
-        qsrc = g.q + (((size_t)T.slot * (g.K / 32) + 2 * kb + qh) * g.N + T.n0 + qn) * 4;
+        qsrc = (xt ? g.q2 : g.q) + (((size_t)wslot * (g.K / 32) + 2 * kb + qh) * g.N + T.n0 + qn) * 4;
         qstep = 16 * 4;
       }
 #pragma unroll
@@ -321,23 +342,27 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
         t_i = i;
         tt = tile_of(i);
       }
+      const bool xt = tt.slot == g.ngroups;  // the extra group's weights
+      const int wslot = xt ? 0 : tt.slot;
+      const uint16_t* gs = xt ? g.s2 : g.s;
+      const uint16_t* gb = xt ? g.b2 : g.b;
       if (LAYOUT == E0_LAYOUT_ROWS) {
         // K / 64 is a multiple of HK and kb of HK: HK * 2 bytes, aligned
-        const size_t idx = ((size_t)tt.slot * g.N + tt.n0 + n) * (g.K / 64) + kb;
+        const size_t idx = ((size_t)wslot * g.N + tt.n0 + n) * (g.K / 64) + kb;
         if (HK == 4) {
-          const uint2 a = __ldg(reinterpret_cast<const uint2*>(g.s + idx));
-          const uint2 b = __ldg(reinterpret_cast<const uint2*>(g.b + idx));
+          const uint2 a = __ldg(reinterpret_cast<const uint2*>(gs + idx));
+          const uint2 b = __ldg(reinterpret_cast<const uint2*>(gb + idx));
           sv[0] = a.x; sv[HK / 2 - 1] = a.y;
           bv[0] = b.x; bv[HK / 2 - 1] = b.y;
         } else {
-          sv[0] = __ldg(reinterpret_cast<const uint32_t*>(g.s + idx));
-          bv[0] = __ldg(reinterpret_cast<const uint32_t*>(g.b + idx));
+          sv[0] = __ldg(reinterpret_cast<const uint32_t*>(gs + idx));
+          bv[0] = __ldg(reinterpret_cast<const uint32_t*>(gb + idx));
         }
       } else {
 #pragma unroll
         for (int u = 0; u < HK; ++u) {
-          const size_t idx = ((size_t)tt.slot * (g.K / 64) + kb + u) * g.N + tt.n0 + n;
-          const uint32_t sh = (uint32_t)__ldg(g.s + idx), bh = (uint32_t)__ldg(g.b + idx);
+          const size_t idx = ((size_t)wslot * (g.K / 64) + kb + u) * g.N + tt.n0 + n;
+          const uint32_t sh = (uint32_t)__ldg(gs + idx), bh = (uint32_t)__ldg(gb + idx);
           sv[u / 2] |= sh << (16 * (u & 1));
           bv[u / 2] |= bh << (16 * (u & 1));
         }
@@ -462,6 +487,10 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
       if (!ok) break;
       const Tile T = tile_of(i);
       const int nout = T.n0 + r;
+      const bool xt = T.slot == g.ngroups;  // the extra group writes its own outputs
+      __half* out16 = xt ? g.out16b : g.out16;
+      float* out32 = xt ? g.out32b : g.out32;
+      const float* rowscale = xt ? nullptr : g.rowscale;
 #pragma unroll 1
       for (int c0 = 0; c0 < T.rows; c0 += 32) {
         uint32_t v[32];
@@ -476,16 +505,16 @@ __global__ void __launch_bounds__(GT, 1) gemm_q4_kernel(const __grid_constant__ 
             if ((lane & 1) == 0 && c < nc) {
               const int o = nout >> 1;  // output index
               const int pos = (o & ~7) + ((o & 7) < 4 ? 2 * (o & 7) : 2 * ((o & 7) - 4) + 1);
-              g.out16[(size_t)(T.m0 + c0 + c) * g.ldo + pos] = __float2half_rn(__fdividef(gt, 1.0f + __expf(-gt)) * up);
+              out16[(size_t)(T.m0 + c0 + c) * g.ldo + pos] = __float2half_rn(__fdividef(gt, 1.0f + __expf(-gt)) * up);
             }
           }
         } else {
           // lane c brings the factor of token row c of the chunk
-          const float fl = g.rowscale && lane < nc ? g.rowscale[T.m0 + c0 + lane] : 1.0f;
+          const float fl = rowscale && lane < nc ? rowscale[T.m0 + c0 + lane] : 1.0f;
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             const float f = __shfl_sync(0xffffffffu, fl, c);
-            if (c < nc) g.out32[(size_t)(T.m0 + c0 + c) * g.ldo + nout] = f * __uint_as_float(v[c]);
+            if (c < nc) out32[(size_t)(T.m0 + c0 + c) * g.ldo + nout] = f * __uint_as_float(v[c]);
           }
         }
       }
@@ -956,29 +985,29 @@ e0_status e0pf_grouped_layer(const e0_dims* dims, const e0_experts* routed, cons
   GemmArgs g{};
   g.status = status;
   g.timeout_ns = timeout;
-  // routed gate/up -> a
+  // routed gate/up -> a, with the shared expert as one more group (its tiles share the
+  // launch): its rows are the T token rows x16, its output as16
+  float* ys = has_shared ? (float*)P(L.ys) : nullptr;
+  __half* as16 = has_shared ? (__half*)P(L.as16) : nullptr;
   g.A = x16s; g.lda = d; g.K = d; g.N = 2 * F; g.ngroups = E; g.row_off = row_off; g.tile_off = tile_off;
   g.q = routed->gate_up.q; g.s = routed->gate_up.scale; g.b = routed->gate_up.bias;
   g.out16 = a16s; g.ldo = F; g.out32 = nullptr; g.rowscale = nullptr;
+  g.xrows = has_shared ? T : 0;
+  if (has_shared) {
+    g.A2 = x16; g.q2 = shared->gate_up.q; g.s2 = shared->gate_up.scale; g.b2 = shared->gate_up.bias;
+    g.out16b = as16; g.out32b = nullptr;
+  }
   E0_CHECK_CUDA((launch_gemm<E0_LAYOUT_ROWS, EPI_SWIGLU>(g, st)));
-  // routed down x w -> y per pair
+  // routed down x w -> y per pair; the shared expert's down projection -> ys
   g.A = a16s; g.lda = F; g.K = F; g.N = d;
   g.q = routed->down.q; g.s = routed->down.scale; g.b = routed->down.bias;
   g.out16 = nullptr; g.out32 = yslot; g.ldo = d; g.rowscale = (const float*)P(L.wrow);
-  E0_CHECK_CUDA((launch_gemm<E0_LAYOUT_COLSLAB, EPI_F32>(g, st)));
-  float* ys = nullptr;
   if (has_shared) {
-    __half* as16 = (__half*)P(L.as16);
-    ys = (float*)P(L.ys);
-    g.A = x16; g.lda = d; g.K = d; g.N = 2 * F; g.ngroups = 1; g.row_off = one_row; g.tile_off = one_tile;
-    g.q = shared->gate_up.q; g.s = shared->gate_up.scale; g.b = shared->gate_up.bias;
-    g.out16 = as16; g.ldo = F; g.out32 = nullptr; g.rowscale = nullptr;
-    E0_CHECK_CUDA((launch_gemm<E0_LAYOUT_ROWS, EPI_SWIGLU>(g, st)));
-    g.A = as16; g.lda = F; g.K = F; g.N = d;
-    g.q = shared->down.q; g.s = shared->down.scale; g.b = shared->down.bias;
-    g.out16 = nullptr; g.out32 = ys; g.ldo = d;
-    E0_CHECK_CUDA((launch_gemm<E0_LAYOUT_COLSLAB, EPI_F32>(g, st)));
+    g.A2 = as16; g.q2 = shared->down.q; g.s2 = shared->down.scale; g.b2 = shared->down.bias;
+    g.out16b = nullptr; g.out32b = ys;
   }
+  E0_CHECK_CUDA((launch_gemm<E0_LAYOUT_COLSLAB, EPI_F32>(g, st)));
+  g.xrows = 0;
   float* yl = nullptr;
   float* lv = nullptr;
   if (has_lora) {
