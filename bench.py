@@ -281,7 +281,9 @@ def run_prefill(args, local_rank: int = 0):
                    "peak_kind": "measured cuBLAS bf16 burst (fp16 has the same dense rate)"},
         "e2e": {"value": round(T / (e2e_ms / 1e3), 1), "unit": "tok/s", "h2d_bytes_per_step": T * sh.d * 2 + T * sh.E * 4,
                 "d2h_bytes_per_step": T * sh.d * 2},
-        "gpu_launches": 10 * args.steps,
+        # per chunk: route, sort, gather, gate/up and down GEMMs (shared expert inside),
+        # LoRA base GEMM, LoRA A, combine
+        "gpu_launches": 8 * args.steps,
         "clocks": sampler.summary(0, 0),
     }
 
