@@ -13,10 +13,12 @@
 //              with the fp32 accumulator in tensor memory:
 //                gate/up  [rows_e x d] x [d x 2F]  -> SwiGLU epilogue -> fp16 a [rows_e x F]
 //                down     [rows_e x F] x [F x d]   -> x w_(t,k)        -> fp32 y per pair
-//              the shared expert and the LoRA base run through the same kernel as one group
-//   lora_ab    (alpha/r) B (A x) on the CUDA cores, four tokens per CTA (r = 16: too thin
-//              for a tile)
-//   combine    h_out = bf16(h + sum_k y_(t,k) + y_shared + y_lora), sum over k in k order
+//              the shared expert rides in the gate/up and down launches as one more
+//              group (its own token rows, weights and outputs); the LoRA base runs
+//              through the same kernel as one group
+//   lora_a     v = A x on the CUDA cores (r = 16: too thin for a tile)
+//   combine    h_out = bf16(h + sum_k y_(t,k) + y_shared + y_lora), sum over k in k order,
+//              with y_lora = W_int4 x + (alpha/r) B v formed here
 //
 // fp16 (not bf16) operands: the dequantised weight s*q + b and x are each rounded once
 // to fp16 (11-bit significand), which keeps the rounding error of the products well
