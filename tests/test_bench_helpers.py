@@ -71,3 +71,19 @@ def test_pool_rule_hit_counts():
     # a cyclic trace over c + 1 experts: LRU misses every time after warm-up, Belady does not
     trace = [[e] for e in itertools.islice(itertools.cycle(range(4)), 40)]
     assert CS.lru_hits(trace, 3) == 0 and CS.belady_hits(trace, 3) > 0
+
+
+def test_traffic_record_applies_only_to_the_kernel_it_was_taken_on():
+    """The roofline's `traffic` comes from the committed capture's traffic/algorithmic
+    ratio, scaled to the workload, and only while the kernel sources hash to the value
+    recorded beside it (a changed kernel reports null until it is captured again)."""
+    import bench
+    import os
+    p = os.path.join(bench.ROOT, "profiles", "engine_stack_traffic.txt")
+    kv = dict(line.split(":", 1) for line in open(p) if ":" in line and not line.startswith("#"))
+    ratio = float(kv["traffic_over_algorithmic"])
+    assert 1.0 <= ratio < 1.05  # no re-reads beyond prefetched lines
+    if kv["kernel_src_sha"].strip() == bench._kernel_source_hash():
+        assert bench._traffic_per_launch(1000000) == round(ratio * 1000000)
+    else:
+        assert bench._traffic_per_launch(1000000) is None
